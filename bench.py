@@ -1,0 +1,405 @@
+#!/usr/bin/env python
+"""Benchmark: useful attention TFLOP/s of blockwise ring attention on GB300.
+
+One step = one pass of the whole hot path over one batch: the fused ring
+forward (ra_ring_attention) and, when the library has it, the blockwise
+backward (ra_ring_attention_bwd), on the long causal GQA workload
+(b=1, S=262,144, h=32, n_kv=8, d=128, N=8 striped shards, bf16 inputs drawn
+N(0,1) x 0.5).  Useful FLOPs: 2 b S^2 h d forward (causal), 2.5x that for the
+backward.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Prints one JSON line (rank 0).  Under torchrun each rank runs its own replica
+(weak scaling, no collective on the data path).
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "useful attention TFLOP/s fwd & bwd (causal, S=256K GQA) and % of BF16 tensor peak"
+WORKLOAD = "causal256k"
+
+# Per-launch DRAM traffic of the dominant kernels from one ncu capture, valid
+# only while the kernel source hashes match (see profiles/).
+TRAFFIC = {}
+
+
+def _args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            pk = json.load(f)
+        return {"hbm_gbs": pk["hbm_gbs"], "bf16": pk["bf16_tflops"],
+                "bf16_sustained": pk.get("bf16_tflops_sustained", pk["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16": 1900.0, "bf16_sustained": 1700.0, "source": "fallback"}
+
+
+def _src_sha(name):
+    with open(os.path.join(ROOT, "long_context_exact_gb300", "csrc", name), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for nm, val in zip(names, parts[5:9]):
+                    if val.lower() == "active":
+                        reasons.add(nm)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------- oracle arm
+def _cpu_oracle_sample(w, fwd_rows: int, bwd_rows: int, seed: int):
+    """Time the fp64 oracle on a bounded sample of the workload: forward on
+    `fwd_rows` random query rows (all heads), backward on `bwd_rows`.
+    Returns (useful FLOPs done, seconds, threads)."""
+    import numpy as np
+    import torch
+
+    from long_context_exact_gb300 import accounting
+    from long_context_exact_gb300.inputs import make_inputs
+    from oracle import oracle
+
+    oracle.build()
+    q, k, v, do = make_inputs(w.b, w.S, w.h, w.n_kv, w.d, w.seed, w.amplitude, with_dout=True)
+    rng = np.random.default_rng(seed)
+    rows_f = np.sort(rng.choice(w.S, fwd_rows, replace=False))
+    rows_b = np.sort(rng.choice(w.S, bwd_rows, replace=False))
+    per_row_fwd = accounting.fwd_useful_flops(w.b, w.S, w.h, w.d, w.causal) / w.S
+    t0 = time.perf_counter()
+    oracle.attn_fwd_rows(q, k, v, w.causal, rows=rows_f)
+    t1 = time.perf_counter()
+    flops = per_row_fwd * fwd_rows
+    if bwd_rows:
+        oracle.attn_bwd_rows(q, k, v, do, w.causal, rows=rows_b)
+        flops += 2.5 * per_row_fwd * bwd_rows
+    t2 = time.perf_counter()
+    threads = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    return flops, (t1 - t0), (t2 - t0), threads, torch
+
+
+def run_reference(a, rank, world):
+    if rank != 0:
+        return
+    from long_context_exact_gb300.inputs import WORKLOADS
+    w = WORKLOADS[a.workload]
+    fwd_rows, bwd_rows = 8, 2
+    vals = []
+    threads = 1
+    for _ in range(a.warmup):
+        _cpu_oracle_sample(w, fwd_rows, bwd_rows, seed=0)
+    for s in range(a.steps):
+        flops, _, secs, threads, _ = _cpu_oracle_sample(w, fwd_rows, bwd_rows, seed=s + 1)
+        vals.append((flops, secs))
+    tot_f = sum(f for f, _ in vals)
+    tot_s = sum(s for _, s in vals)
+    value = tot_f / tot_s / 1e12
+    sample = (f"fp64 oracle on {fwd_rows} forward + {bwd_rows} backward random query rows "
+              f"(all {w.h} heads) of the {w.name} workload per step")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": a.gpus, "steps": a.steps, "warmup": a.warmup,
+        "ms_per_step": tot_s / a.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "b": w.b, "S": w.S, "h": w.h, "n_kv": w.n_kv, "d": w.d,
+                   "n_shards": w.n_shards, "layout": "striped", "causal": w.causal},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+# ---------------------------------------------------------------- our arm
+def run_ours(a, rank, world, local_rank):
+    import torch
+
+    from long_context_exact_gb300 import accounting
+    from long_context_exact_gb300 import binding as ra
+    from long_context_exact_gb300 import build as lib_build
+    from long_context_exact_gb300.inputs import STRIPED, WORKLOADS
+
+    w = WORKLOADS[a.workload]
+    layout = STRIPED if STRIPED in w.layouts else w.layouts[0]
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if rank == 0:
+        lib_build.build()
+    if world > 1:
+        torch.distributed.barrier()
+    ra.load()
+
+    gen = torch.Generator(device=dev).manual_seed(w.seed + 1000 * rank)
+
+    def rnd(*shape):
+        x = torch.randn(shape, generator=gen, device=dev, dtype=torch.float32)
+        return x.mul_(w.amplitude).to(torch.bfloat16)
+
+    q = rnd(w.b, w.S, w.h, w.d)
+    k = rnd(w.b, w.S, w.n_kv, w.d)
+    v = rnd(w.b, w.S, w.n_kv, w.d)
+    do = rnd(w.b, w.S, w.h, w.d)
+    out = torch.empty((w.b, w.S, w.h, w.d), dtype=torch.float32, device=dev)
+    lse = torch.empty((w.b, w.h, w.S), dtype=torch.float32, device=dev)
+    dq = torch.empty_like(out)
+    dk = torch.empty((w.b, w.S, w.n_kv, w.d), dtype=torch.float32, device=dev)
+    dv = torch.empty_like(dk)
+    ws = torch.empty(max(ra.bwd_workspace_size(w.S, w.b, w.h, w.n_kv, w.d), 16),
+                     dtype=torch.uint8, device=dev)
+
+    have_bwd = True
+    try:
+        ra.ring_attention(q, k, v, w.n_shards, layout, w.causal, out=out, lse=lse)
+        ra.ring_attention_bwd(q, k, v, out, lse, do, w.n_shards, layout, w.causal, dq=dq, dk=dk,
+                              dv=dv, workspace=ws)
+    except ra.RAError as e:
+        if e.status != ra.RA_ERR_UNSUPPORTED:
+            raise
+        have_bwd = False
+    ra.stream_check()
+
+    stream = torch.cuda.current_stream()
+    ev = []
+
+    def step(record: bool):
+        e0 = torch.cuda.Event(enable_timing=True) if record else None
+        e1 = torch.cuda.Event(enable_timing=True) if record else None
+        e2 = torch.cuda.Event(enable_timing=True) if record else None
+        if record:
+            e0.record(stream)
+        ra.ring_attention(q, k, v, w.n_shards, layout, w.causal, out=out, lse=lse)
+        if record:
+            e1.record(stream)
+        if have_bwd:
+            ra.ring_attention_bwd(q, k, v, out, lse, do, w.n_shards, layout, w.causal, dq=dq,
+                                  dk=dk, dv=dv, workspace=ws)
+        if record:
+            e2.record(stream)
+            ev.append((e0, e1, e2))
+
+    for _ in range(a.warmup):
+        step(False)
+    ra.stream_check()
+
+    clocks = ClockSampler(local_rank)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    launches0 = ra.launch_count()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for _ in range(a.steps):
+        step(True)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    launches = ra.launch_count() - launches0
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+    ra.stream_check()
+    elapsed_ms = t_start.elapsed_time(t_end)
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+
+    f_fwd = accounting.fwd_useful_flops(w.b, w.S, w.h, w.d, w.causal)
+    f_bwd = accounting.bwd_useful_flops(w.b, w.S, w.h, w.d, w.causal) if have_bwd else 0.0
+    step_flops = f_fwd + f_bwd
+    value = step_flops * a.steps * world / (elapsed_ms / 1e3) / 1e12
+    fwd_ms = statistics.mean(e0.elapsed_time(e1) for e0, e1, _ in ev)
+    bwd_ms = statistics.mean(e1.elapsed_time(e2) for _, e1, e2 in ev) if have_bwd else 0.0
+    peaks = _peaks()
+
+    # dominant kernel: the one with the most time per step
+    if have_bwd and bwd_ms > fwd_ms:
+        dom, dom_ms, dom_flops, dom_src = "bwd", bwd_ms, f_bwd, "ra_bwd.cu"
+    else:
+        dom, dom_ms, dom_flops, dom_src = "fwd", fwd_ms, f_fwd, "ra_fwd.cu"
+    achieved = dom_flops / (dom_ms / 1e3) / 1e12
+    tr = TRAFFIC.get(dom)
+    traffic = tr["bytes_per_launch"] if tr and tr["src_sha"] == _src_sha(dom_src) else None
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_sustained"],
+                "unit": "TFLOP/s", "frac": achieved / peaks["bf16_sustained"],
+                "traffic": traffic, "kernel": dom,
+                "peak_note": f"{peaks['source']} bf16 sustained; frac of burst "
+                             f"{achieved / peaks['bf16']:.3f}"}
+
+    # end to end through the public API with host buffers
+    e2e = None
+    if not a.no_e2e:
+        hq_ = q.cpu().pin_memory()
+        hk_ = k.cpu().pin_memory()
+        hv_ = v.cpu().pin_memory()
+        hdo = do.cpu().pin_memory()
+        h_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+        h_lse = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+        h_dq = torch.empty(dq.shape, dtype=dq.dtype, pin_memory=True)
+        h_dk = torch.empty(dk.shape, dtype=dk.dtype, pin_memory=True)
+        h_dv = torch.empty(dv.shape, dtype=dv.dtype, pin_memory=True)
+        h2d = sum(t.numel() * t.element_size() for t in (hq_, hk_, hv_) + ((hdo,) if have_bwd else ()))
+        d2h = sum(t.numel() * t.element_size() for t in (h_out, h_lse) +
+                  ((h_dq, h_dk, h_dv) if have_bwd else ()))
+
+        def e2e_step():
+            q.copy_(hq_, non_blocking=True)
+            k.copy_(hk_, non_blocking=True)
+            v.copy_(hv_, non_blocking=True)
+            ra.ring_attention(q, k, v, w.n_shards, layout, w.causal, out=out, lse=lse)
+            h_out.copy_(out, non_blocking=True)
+            h_lse.copy_(lse, non_blocking=True)
+            if have_bwd:
+                do.copy_(hdo, non_blocking=True)
+                ra.ring_attention_bwd(q, k, v, out, lse, do, w.n_shards, layout, w.causal, dq=dq,
+                                      dk=dk, dv=dv, workspace=ws)
+                h_dq.copy_(dq, non_blocking=True)
+                h_dk.copy_(dk, non_blocking=True)
+                h_dv.copy_(dv, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        s0 = torch.cuda.Event(enable_timing=True)
+        s1 = torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        for _ in range(a.steps):
+            e2e_step()
+        s1.record(stream)
+        torch.cuda.synchronize()
+        ra.stream_check()
+        e2e_ms = s0.elapsed_time(s1)
+        if world > 1:
+            t = torch.tensor([e2e_ms], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        e2e = {"value": step_flops * a.steps * world / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": e2e_ms / a.steps}
+
+    cpu = None
+    if rank == 0 and world == 1 and not a.no_cpu_baseline:
+        fwd_rows, bwd_rows = 16, 4
+        flops, _, secs, threads, _ = _cpu_oracle_sample(w, fwd_rows, bwd_rows, seed=123)
+        cpu = {"value": flops / secs / 1e12, "unit": "TFLOP/s", "cores": threads,
+               "kind": "oracle",
+               "sample": f"fp64 oracle, {fwd_rows} forward + {bwd_rows} backward random query "
+                         f"rows x {w.h} heads of this workload, {secs:.1f} s"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": a.steps, "warmup": a.warmup, "ms_per_step": elapsed_ms / a.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": w.name, "b": w.b, "S": w.S, "h": w.h, "n_kv": w.n_kv,
+                       "d": w.d, "n_shards": w.n_shards,
+                       "layout": "striped" if layout == STRIPED else "contiguous",
+                       "causal": w.causal, "backward": have_bwd,
+                       "l2": "inputs larger than L2 (Q alone is "
+                             f"{q.numel() * 2 / 1e9:.2f} GB); no flush",
+                       "parallelism": f"replica x{world}"},
+            "pct_of_bf16_peak": 100.0 * value / world / peaks["bf16_sustained"],
+            "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
+            "fwd_tflops": f_fwd / (fwd_ms / 1e3) / 1e12,
+            "bwd_tflops": (f_bwd / (bwd_ms / 1e3) / 1e12) if have_bwd else None,
+            "clocks": clk, "e2e": e2e, "gpu_launches": launches, "roofline": roofline,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    a = _args()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if a.impl == "reference":
+        run_reference(a, rank, world)
+        return
+    if world > 1:
+        import torch
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl")
+    try:
+        run_ours(a, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,189 @@
+/*
+ * ra.h -- C ABI of the GB300 blockwise ring-attention engine.
+ *
+ * The engine computes exact softmax attention, O = softmax(scale * Q K^T) V,
+ * the way Ring Attention does: a resident query shard meets the key/value
+ * shards one after another in ring order and keeps an online-softmax state
+ * per query row (running max m, running sum l, unnormalised output O), then
+ * divides by l.  On one GPU the N devices of the ring are N virtual shards of
+ * one sequence.
+ *
+ * Sources (page title, then section):
+ *  - "Ring Attention with Blockwise Transformers: Mathematical Foundations,
+ *    Circular KV Passing, Overlapped Communication-Computation, and Linear
+ *    Context Scaling": "Blockwise Attention and Online Softmax Formulations"
+ *    (the update of m, l, O and the final division by l), "The Ring Attention
+ *    Protocol" (query block resident, key/value blocks rotate), "Causal
+ *    Masking Dynamics" (striped placement t -> t mod N), "The Backward Pass and
+ *    Gradient Exchange" (P recomputed from saved statistics).
+ *  - "Ring Attention for Infinite Context": "FlashAttention Integration" (the
+ *    rescale-merge of a running output with a block output).
+ *  - summary of "Ring Attention with Blockwise Transformers for Near-Infinite
+ *    Context": "The Ring Communication Protocol" (host i holds block
+ *    (i - idx) mod N on iteration idx), "The Backward Pass: Symmetric Ring
+ *    Operation".
+ *  - the magicnetworld.com article on ring attention's communication budget,
+ *    causal triangle and load imbalance: section 2 (symbols, GQA with h query
+ *    heads sharing n_kv KV heads), section 6 (causal mask; contiguous versus
+ *    striped placement).
+ *
+ * Conventions for every call:
+ *  - Tensors are dense, row-major, in DEVICE memory, and owned by the caller.
+ *    The library allocates no device memory.  Base pointers must be 16-byte
+ *    aligned.
+ *  - bf16 tensors are passed as raw 16-bit patterns (uint16_t).
+ *  - Query-side tensors are [b, rows, h, d]; key/value-side tensors are
+ *    [b, rows, n_kv, d].  Per-row statistics are [b, h, rows] float.
+ *  - GQA: query head hq reads KV head hq / (h / n_kv).
+ *  - Causal masking is inclusive: key position <= query position.
+ *  - `m` and `lse` are in natural-log units of the scaled logits
+ *    scale * <q, k>.  LSE = m + ln(l).  A row that sees no key has l = 0,
+ *    O = 0 and LSE = -inf.
+ *  - scale <= 0 selects 1/sqrt(d).
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Every
+ *    call only enqueues work on it and returns; nothing synchronises.
+ *  - Arguments are validated on the host before anything is launched; a
+ *    rejected call launches nothing and leaves every output untouched.
+ *  - Device-side waits are bounded; a wait that runs out sets a device error
+ *    word, and the kernel unwinds.  ra_stream_check() reports it.
+ *  - Supported: d in {64, 128}; h % n_kv == 0; the row counts of one call
+ *    below 2^31; n_shards >= 1 with S % n_shards == 0.
+ */
+#ifndef RA_H
+#define RA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  RA_OK = 0,
+  RA_ERR_INVALID_ARG = 1,     /* null/misaligned pointer, negative size, bad enum */
+  RA_ERR_UNSUPPORTED = 2,     /* shape the kernels do not handle */
+  RA_ERR_CUDA = 3,            /* a CUDA runtime call or launch failed */
+  RA_ERR_DEVICE_TIMEOUT = 4,  /* a bounded device-side wait ran out */
+  RA_ERR_WORKSPACE = 5        /* workspace missing or too small */
+} ra_status;
+
+typedef enum {
+  RA_LAYOUT_CONTIGUOUS = 0,   /* shard p holds tokens [p*L, (p+1)*L) */
+  RA_LAYOUT_STRIPED = 1       /* shard p holds tokens p, p+N, p+2N, ... */
+} ra_layout;
+
+typedef struct {
+  int b;      /* batch */
+  int h;      /* query heads */
+  int n_kv;   /* key/value heads (h % n_kv == 0) */
+  int d;      /* head dimension: 64 or 128 */
+} ra_dims;
+
+/* One ring step: fold one key/value block into the online-softmax state of a
+ * query block ("Blockwise Attention and Online Softmax Formulations"; the
+ * fourth page's "Incremental Blockwise Attention" steps 1-5):
+ *   m~ = rowmax(S), m' = max(m, m~), P = exp(S - m'),
+ *   l' = exp(m - m') l + rowsum(P),  O' = exp(m - m') O + P V,
+ * with S = scale * Q K^T over the visible keys.  The block's contribution is
+ * computed on the tensor cores and merged into the state with the second
+ * page's rescale-merge, so `m` is the exact running row max afterwards.
+ *   q      [b, Lq, h, d] bf16         k, v [b, Lk, n_kv, d] bf16
+ *   m, l   [b, h, Lq] float, in/out   o    [b, Lq, h, d] float, in/out
+ *   q_pos  [Lq] int32, k_pos [Lk] int32: token positions, used only when
+ *          causal != 0 (key c visible to query r iff k_pos[c] <= q_pos[r]).
+ * Initial state: m = -inf, l = 0, o = 0.  Rows with no visible key in this
+ * block are left unchanged.  Lq or Lk == 0 is a no-op. */
+ra_status ra_block_step(const uint16_t *q, const uint16_t *k, const uint16_t *v, float *m,
+                        float *l, float *o, const int32_t *q_pos, const int32_t *k_pos,
+                        int64_t Lq, int64_t Lk, ra_dims dims, int causal, float scale,
+                        void *stream);
+
+/* Final division ("... recovered by dividing by the accumulated normalizer"):
+ * o <- o / l in place, lse = m + ln(l).  Rows with l == 0 get o = 0 and
+ * lse = -inf.  o [b, Lq, h, d]; l, m, lse [b, h, Lq]. */
+ra_status ra_finalize(float *o, const float *l, const float *m, float *lse, int64_t Lq,
+                      ra_dims dims, void *stream);
+
+/* Rescale-merge of two normalised partial results over disjoint key sets
+ * ("FlashAttention Integration" on the second page, with each side's own LSE
+ * as its reference value):
+ *   mx = max(lse_a, lse_b), w_x = exp(lse_x - mx),
+ *   o = (w_a o_a + w_b o_b) / (w_a + w_b),  lse = mx + ln(w_a + w_b).
+ * A side with lse = -inf contributes nothing.  o_* [b, Lq, h, d] float;
+ * lse_* [b, h, Lq] float.  Outputs may alias side a. */
+ra_status ra_merge(const float *o_a, const float *lse_a, const float *o_b, const float *lse_b,
+                   float *o, float *lse, int64_t Lq, ra_dims dims, void *stream);
+
+/* The whole ring on one GPU: every query shard i visits key/value shards
+ * (i - s) mod N for s = 0..N-1 ("The Ring Communication Protocol"), with
+ * causal tiles that are fully masked skipped, and finalizes.  One fused
+ * launch; the online-softmax state stays in tensor memory.
+ *   q [b, S, h, d] bf16, k, v [b, S, n_kv, d] bf16, in natural token order
+ *   out [b, S, h, d] float, lse [b, h, S] float, in natural token order.
+ * The layout only changes which tokens form a shard (and so the visit order
+ * and the masked-tile pattern), never the result. */
+ra_status ra_ring_attention(const uint16_t *q, const uint16_t *k, const uint16_t *v, float *out,
+                            float *lse, int64_t S, int n_shards, ra_layout layout, int causal,
+                            float scale, ra_dims dims, void *stream);
+
+/* Bytes of device workspace ra_ring_attention_bwd needs (per-row
+ * D = rowsum(dO * O) and the log2-domain LSE). */
+size_t ra_bwd_workspace_size(int64_t S, ra_dims dims);
+
+/* Blockwise backward with recomputation ("The Backward Pass and Gradient
+ * Exchange"; "The Backward Pass: Symmetric Ring Operation"):
+ *   P = exp(scale Q K^T - LSE), D = rowsum(dO * O),
+ *   dV_j += P^T dO, dP = dO V^T, dS = P * (dP - D),
+ *   dQ_i += scale dS K,  dK_j += scale dS^T Q.
+ * Each key/value tile is visited by the query shards in ring order; dK/dV sum
+ * over the g query heads of a KV head.
+ *   q, dout [b, S, h, d] bf16; k, v [b, S, n_kv, d] bf16;
+ *   out [b, S, h, d] float and lse [b, h, S] float from ra_ring_attention;
+ *   dq [b, S, h, d] float, dk, dv [b, S, n_kv, d] float (overwritten).
+ *   workspace: device memory of at least ra_bwd_workspace_size() bytes. */
+ra_status ra_ring_attention_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                                const float *out, const float *lse, const uint16_t *dout,
+                                float *dq, float *dk, float *dv, void *workspace,
+                                size_t workspace_bytes, int64_t S, int n_shards, ra_layout layout,
+                                int causal, float scale, ra_dims dims, void *stream);
+
+/* Token placement maps (the third page's section 6 example; "Striped
+ * Attention" on the first page), computed on the device by the same functions
+ * the attention kernels use:
+ *   shard_of[t], local_of[t] for t in [0, S);  token_of[p * L + r] inverse.
+ * Any of the three device pointers may be NULL to skip that map. */
+ra_status ra_position_map(ra_layout layout, int64_t S, int n_shards, int32_t *shard_of,
+                          int32_t *local_of, int32_t *token_of, void *stream);
+
+/* Ring visit order on the device: order[i * N + s] = key/value shard that
+ * query shard i meets at ring step s, (i - s) mod N ("The Ring Communication
+ * Protocol", k_block_idx). */
+ra_status ra_ring_order(int n_shards, int32_t *order, void *stream);
+
+/* Synchronise `stream`, then read and clear the device error word.  Returns
+ * RA_ERR_DEVICE_TIMEOUT if a bounded device wait ran out since the last
+ * check, RA_ERR_CUDA on a CUDA error, RA_OK otherwise. */
+ra_status ra_stream_check(void *stream);
+
+/* Failure-detection self test: launches one CTA that waits on an mbarrier
+ * nothing will ever arrive on, with a wait budget of `budget_cycles` SM
+ * clocks (1 .. 2^31).  The wait runs out, the kernel records a timeout and
+ * returns; ra_stream_check() must then report RA_ERR_DEVICE_TIMEOUT. */
+ra_status ra_selftest_wait_timeout(long long budget_cycles, void *stream);
+
+/* Number of kernels this library has launched in this process (all entry
+ * points, all threads).  Lets a caller count the device work a region did. */
+uint64_t ra_launch_count(void);
+
+/* Message for the last non-OK status returned on the calling thread. */
+const char *ra_last_error(void);
+
+/* Library ABI version (major * 100 + minor). */
+int ra_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RA_H */

@@ -1,0 +1,342 @@
+// ra_api.cu -- the extern "C" boundary declared in include/ra.h: argument
+// validation, TMA tensor-map construction, kernel launches and error
+// reporting.  No device memory is allocated here.
+#include <cmath>
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <atomic>
+#include <mutex>
+#include <string>
+
+#include "ra_internal.cuh"
+
+namespace ra {
+namespace {
+
+thread_local std::string g_last_error;
+std::atomic<uint64_t> g_launches{0};
+
+// Count one kernel launch that the runtime accepted.
+cudaError_t counted(cudaError_t e, uint64_t n = 1) {
+  if (e == cudaSuccess) g_launches.fetch_add(n, std::memory_order_relaxed);
+  return e;
+}
+
+ra_status fail(ra_status st, const char *fmt, ...) __attribute__((format(printf, 2, 3)));
+ra_status fail(ra_status st, const char *fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+
+ra_status cuda_fail(cudaError_t e, const char *what) {
+  return fail(RA_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Pointers must be non-null and 16-byte aligned (TMA and float4 access).
+#define RA_CHECK_PTR(p)                                                                   \
+  do {                                                                                    \
+    if ((p) == nullptr) return fail(RA_ERR_INVALID_ARG, "%s is NULL", #p);                \
+    if (!aligned16(p)) return fail(RA_ERR_INVALID_ARG, "%s is not 16-byte aligned", #p);  \
+  } while (0)
+
+ra_status check_dims(const ra_dims &dm) {
+  if (dm.b < 0 || dm.h <= 0 || dm.n_kv <= 0 || dm.d <= 0)
+    return fail(RA_ERR_INVALID_ARG, "dims must be positive (b >= 0): b=%d h=%d n_kv=%d d=%d",
+                dm.b, dm.h, dm.n_kv, dm.d);
+  if (dm.h % dm.n_kv != 0)
+    return fail(RA_ERR_UNSUPPORTED, "h=%d is not a multiple of n_kv=%d", dm.h, dm.n_kv);
+  if (dm.d != 64 && dm.d != 128) return fail(RA_ERR_UNSUPPORTED, "d=%d (supported: 64, 128)", dm.d);
+  return RA_OK;
+}
+
+ra_status resolve_scale(float scale, int d, float *out) {
+  if (std::isnan(scale) || std::isinf(scale)) return fail(RA_ERR_INVALID_ARG, "scale is not finite");
+  *out = scale > 0.f ? scale : 1.0f / std::sqrt(static_cast<float>(d));
+  return RA_OK;
+}
+
+// ------------------------------------------------------------ tensor maps
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+// View a bf16 tensor [b, N*L, heads, d] whose rows are spread over N shards
+// of L rows each as a 5-D tensor with coordinates
+//   striped   : (x, head, shard, row, batch)   token = row * N + shard
+//   contiguous: (x, head, row, shard, batch)   token = shard * L + row
+// and a box of 64 columns x 128 rows of one head, 128-byte swizzled.
+ra_status make_map(CUtensorMap *map, const void *base, int layout, int b, int N, int L, int heads,
+                   int d) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return fail(RA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  const cuuint64_t tok = static_cast<cuuint64_t>(heads) * d * 2;  // bytes per token
+  cuuint64_t dims[5];
+  cuuint64_t strides[4];
+  cuuint32_t box[5];
+  const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  dims[0] = static_cast<cuuint64_t>(d);
+  dims[1] = static_cast<cuuint64_t>(heads);
+  strides[0] = static_cast<cuuint64_t>(d) * 2;
+  if (layout == RA_LAYOUT_STRIPED) {
+    dims[2] = static_cast<cuuint64_t>(N);
+    dims[3] = static_cast<cuuint64_t>(L);
+    strides[1] = tok;
+    strides[2] = tok * N;
+    box[2] = 1;
+    box[3] = kTile;
+  } else {
+    dims[2] = static_cast<cuuint64_t>(L);
+    dims[3] = static_cast<cuuint64_t>(N);
+    strides[1] = tok;
+    strides[2] = tok * L;
+    box[2] = kTile;
+    box[3] = 1;
+  }
+  dims[4] = static_cast<cuuint64_t>(b < 1 ? 1 : b);
+  strides[3] = tok * N * L;
+  box[0] = 64;
+  box[1] = 1;
+  box[4] = 1;
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(base), dims,
+                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(RA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return RA_OK;
+}
+
+ra_status launch_attention(const FwdParams &p, int d, const void *q, const void *k,
+                           const void *v, long long q_rows_per_shard, long long k_rows_per_shard,
+                           cudaStream_t stream) {
+  CUtensorMap qm, km, vm;
+  ra_status st;
+  if ((st = make_map(&qm, q, p.layout, p.b, p.N, static_cast<int>(q_rows_per_shard), p.h, d)) != RA_OK)
+    return st;
+  if ((st = make_map(&km, k, p.layout, p.b, p.N, static_cast<int>(k_rows_per_shard), p.n_kv, d)) != RA_OK)
+    return st;
+  if ((st = make_map(&vm, v, p.layout, p.b, p.N, static_cast<int>(k_rows_per_shard), p.n_kv, d)) != RA_OK)
+    return st;
+  const int nq = (p.g % 2 == 0) ? 2 : 1;
+  FwdParams pp = p;
+  pp.pairs = p.g / nq;
+  const long long n_units =
+      static_cast<long long>(p.b) * p.n_kv * pp.pairs * p.N * static_cast<long long>(p.n_qtiles);
+  if (n_units > 0x7fffffffLL) return fail(RA_ERR_UNSUPPORTED, "too many work units (%lld)", n_units);
+  cudaError_t e = counted(launch_fwd(pp, d, nq, qm, km, vm, n_units, stream));
+  if (e != cudaSuccess) return cuda_fail(e, "forward launch");
+  return RA_OK;
+}
+
+}  // namespace
+}  // namespace ra
+
+using namespace ra;
+
+extern "C" {
+
+int ra_version(void) { return 100; }
+
+uint64_t ra_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+const char *ra_last_error(void) { return g_last_error.c_str(); }
+
+ra_status ra_block_step(const uint16_t *q, const uint16_t *k, const uint16_t *v, float *m,
+                        float *l, float *o, const int32_t *q_pos, const int32_t *k_pos,
+                        int64_t Lq, int64_t Lk, ra_dims dims, int causal, float scale,
+                        void *stream) {
+  ra_status st;
+  if ((st = check_dims(dims)) != RA_OK) return st;
+  if (Lq < 0 || Lk < 0) return fail(RA_ERR_INVALID_ARG, "negative length Lq=%lld Lk=%lld",
+                                    (long long)Lq, (long long)Lk);
+  if (Lq >= (1LL << 31) || Lk >= (1LL << 31))
+    return fail(RA_ERR_UNSUPPORTED, "Lq/Lk must be below 2^31");
+  if (Lq == 0 || Lk == 0 || dims.b == 0) return RA_OK;
+  RA_CHECK_PTR(q);
+  RA_CHECK_PTR(k);
+  RA_CHECK_PTR(v);
+  RA_CHECK_PTR(m);
+  RA_CHECK_PTR(l);
+  RA_CHECK_PTR(o);
+  if (causal) {
+    if (!q_pos || !k_pos) return fail(RA_ERR_INVALID_ARG, "causal block step needs q_pos and k_pos");
+  }
+  float sc;
+  if ((st = resolve_scale(scale, dims.d, &sc)) != RA_OK) return st;
+  FwdParams p{};
+  p.b = dims.b;
+  p.h = dims.h;
+  p.n_kv = dims.n_kv;
+  p.g = dims.h / dims.n_kv;
+  p.N = 1;
+  p.L = static_cast<int>(Lq);
+  p.Lk = static_cast<int>(Lk);
+  p.S = static_cast<int>(Lq);
+  p.layout = RA_LAYOUT_CONTIGUOUS;
+  p.causal = causal ? 1 : 0;
+  p.scale_log2 = sc * kLog2e;
+  p.n_qtiles = static_cast<int>((Lq + kTile - 1) / kTile);
+  p.n_ktiles = static_cast<int>((Lk + kTile - 1) / kTile);
+  p.block_mode = 1;
+  p.q_pos = q_pos;
+  p.k_pos = k_pos;
+  p.st_m = m;
+  p.st_l = l;
+  p.st_o = o;
+  return launch_attention(p, dims.d, q, k, v, Lq, Lk, static_cast<cudaStream_t>(stream));
+}
+
+ra_status ra_finalize(float *o, const float *l, const float *m, float *lse, int64_t Lq,
+                      ra_dims dims, void *stream) {
+  ra_status st;
+  if ((st = check_dims(dims)) != RA_OK) return st;
+  if (Lq < 0) return fail(RA_ERR_INVALID_ARG, "negative Lq");
+  if (Lq == 0 || dims.b == 0) return RA_OK;
+  RA_CHECK_PTR(o);
+  RA_CHECK_PTR(l);
+  RA_CHECK_PTR(m);
+  RA_CHECK_PTR(lse);
+  cudaError_t e = counted(launch_finalize(o, l, m, lse, dims.b, Lq, dims.h, dims.d,
+                                  static_cast<cudaStream_t>(stream)));
+  return e == cudaSuccess ? RA_OK : cuda_fail(e, "finalize launch");
+}
+
+ra_status ra_merge(const float *o_a, const float *lse_a, const float *o_b, const float *lse_b,
+                   float *o, float *lse, int64_t Lq, ra_dims dims, void *stream) {
+  ra_status st;
+  if ((st = check_dims(dims)) != RA_OK) return st;
+  if (Lq < 0) return fail(RA_ERR_INVALID_ARG, "negative Lq");
+  if (Lq == 0 || dims.b == 0) return RA_OK;
+  RA_CHECK_PTR(o_a);
+  RA_CHECK_PTR(lse_a);
+  RA_CHECK_PTR(o_b);
+  RA_CHECK_PTR(lse_b);
+  RA_CHECK_PTR(o);
+  RA_CHECK_PTR(lse);
+  cudaError_t e = counted(launch_merge(o_a, lse_a, o_b, lse_b, o, lse, dims.b, Lq, dims.h, dims.d,
+                                       static_cast<cudaStream_t>(stream)));
+  return e == cudaSuccess ? RA_OK : cuda_fail(e, "merge launch");
+}
+
+ra_status ra_ring_attention(const uint16_t *q, const uint16_t *k, const uint16_t *v, float *out,
+                            float *lse, int64_t S, int n_shards, ra_layout layout, int causal,
+                            float scale, ra_dims dims, void *stream) {
+  ra_status st;
+  if ((st = check_dims(dims)) != RA_OK) return st;
+  if (layout != RA_LAYOUT_CONTIGUOUS && layout != RA_LAYOUT_STRIPED)
+    return fail(RA_ERR_INVALID_ARG, "unknown layout %d", (int)layout);
+  if (S < 0) return fail(RA_ERR_INVALID_ARG, "negative S");
+  if (n_shards < 1) return fail(RA_ERR_INVALID_ARG, "n_shards must be >= 1");
+  if (S >= (1LL << 31)) return fail(RA_ERR_UNSUPPORTED, "S must be below 2^31");
+  if (S % n_shards != 0)
+    return fail(RA_ERR_UNSUPPORTED, "S=%lld is not a multiple of n_shards=%d", (long long)S, n_shards);
+  if (S == 0 || dims.b == 0) return RA_OK;
+  RA_CHECK_PTR(q);
+  RA_CHECK_PTR(k);
+  RA_CHECK_PTR(v);
+  RA_CHECK_PTR(out);
+  RA_CHECK_PTR(lse);
+  float sc;
+  if ((st = resolve_scale(scale, dims.d, &sc)) != RA_OK) return st;
+  const long long L = S / n_shards;
+  FwdParams p{};
+  p.b = dims.b;
+  p.h = dims.h;
+  p.n_kv = dims.n_kv;
+  p.g = dims.h / dims.n_kv;
+  p.N = n_shards;
+  p.L = static_cast<int>(L);
+  p.Lk = static_cast<int>(L);
+  p.S = static_cast<int>(S);
+  p.layout = layout;
+  p.causal = causal ? 1 : 0;
+  p.scale_log2 = sc * kLog2e;
+  p.n_qtiles = static_cast<int>((L + kTile - 1) / kTile);
+  p.n_ktiles = p.n_qtiles;
+  p.block_mode = 0;
+  p.out = out;
+  p.lse = lse;
+  return launch_attention(p, dims.d, q, k, v, L, L, static_cast<cudaStream_t>(stream));
+}
+
+size_t ra_bwd_workspace_size(int64_t S, ra_dims dims) {
+  if (S <= 0 || dims.b <= 0 || dims.h <= 0) return 0;
+  // D = rowsum(dO * O) and the log2-domain LSE, one float each per (b, h, row).
+  return static_cast<size_t>(2) * dims.b * dims.h * static_cast<size_t>(S) * sizeof(float);
+}
+
+ra_status ra_ring_attention_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                                const float *out, const float *lse, const uint16_t *dout,
+                                float *dq, float *dk, float *dv, void *workspace,
+                                size_t workspace_bytes, int64_t S, int n_shards, ra_layout layout,
+                                int causal, float scale, ra_dims dims, void *stream) {
+  (void)q; (void)k; (void)v; (void)out; (void)lse; (void)dout; (void)dq; (void)dk; (void)dv;
+  (void)workspace; (void)workspace_bytes; (void)S; (void)n_shards; (void)layout; (void)causal;
+  (void)scale; (void)dims; (void)stream;
+  return fail(RA_ERR_UNSUPPORTED, "backward kernel not built in this version");
+}
+
+ra_status ra_position_map(ra_layout layout, int64_t S, int n_shards, int32_t *shard_of,
+                          int32_t *local_of, int32_t *token_of, void *stream) {
+  if (layout != RA_LAYOUT_CONTIGUOUS && layout != RA_LAYOUT_STRIPED)
+    return fail(RA_ERR_INVALID_ARG, "unknown layout %d", (int)layout);
+  if (S < 0 || n_shards < 1) return fail(RA_ERR_INVALID_ARG, "S >= 0 and n_shards >= 1 required");
+  if (S >= (1LL << 31)) return fail(RA_ERR_UNSUPPORTED, "S must be below 2^31");
+  if (S % n_shards != 0) return fail(RA_ERR_UNSUPPORTED, "S is not a multiple of n_shards");
+  if (S == 0) return RA_OK;
+  cudaError_t e = counted(launch_position_map(layout, static_cast<int>(S), n_shards, shard_of,
+                                              local_of, token_of, static_cast<cudaStream_t>(stream)));
+  return e == cudaSuccess ? RA_OK : cuda_fail(e, "position map launch");
+}
+
+ra_status ra_ring_order(int n_shards, int32_t *order, void *stream) {
+  if (n_shards < 1 || n_shards > 46340) return fail(RA_ERR_INVALID_ARG, "n_shards out of range");
+  if (!order) return fail(RA_ERR_INVALID_ARG, "order is NULL");
+  cudaError_t e = counted(launch_ring_order(n_shards, order, static_cast<cudaStream_t>(stream)));
+  return e == cudaSuccess ? RA_OK : cuda_fail(e, "ring order launch");
+}
+
+ra_status ra_stream_check(void *stream) {
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
+  unsigned int words[2] = {0u, 0u};
+  if ((e = read_error_word_fwd(&words[0])) != cudaSuccess) return cuda_fail(e, "error word read");
+  if ((e = read_error_word_small(&words[1])) != cudaSuccess) return cuda_fail(e, "error word read");
+  for (unsigned int w : words) {
+    if (w != 0u)
+      return fail(RA_ERR_DEVICE_TIMEOUT, "device wait ran out (code %u, site 0x%x)", w & 0xffu,
+                  w >> 8);
+  }
+  return RA_OK;
+}
+
+ra_status ra_selftest_wait_timeout(long long budget_cycles, void *stream) {
+  if (budget_cycles < 1 || budget_cycles > (1LL << 31))
+    return fail(RA_ERR_INVALID_ARG, "budget_cycles out of range");
+  cudaError_t e = counted(launch_wait_timeout_selftest(budget_cycles, static_cast<cudaStream_t>(stream)));
+  return e == cudaSuccess ? RA_OK : cuda_fail(e, "self-test launch");
+}
+
+}  // extern "C"

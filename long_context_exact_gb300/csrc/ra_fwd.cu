@@ -1,0 +1,638 @@
+// ra_fwd.cu -- forward blockwise ring-attention kernel for sm_103a.
+//
+// One CTA owns NQ query tiles of 128 rows (NQ = 2: two query heads of the
+// same GQA group at the same rows, so every K/V tile it loads serves both)
+// and walks the key/value tiles in ring order: shard (i - s) mod N for
+// s = 0..N-1 (the fourth page's "The Ring Communication Protocol"), skipping
+// tiles the causal rule masks completely.  Per tile and query tile it runs
+// the online-softmax update of the first page's "Blockwise Attention and
+// Online Softmax Formulations":
+//     S = Q K^T;  m' = max(m, rowmax S);  P = exp(S - m');
+//     l' = e^(m - m') l + rowsum P;  O' = e^(m - m') O + P V
+// with S, P and O held in tensor memory (TMEM) and the two GEMMs issued as
+// tcgen05.mma by one thread.  The epilogue either finalizes (O / l and
+// LSE = m + ln l, ring mode) or folds the block result into a caller-held
+// (m, l, O) state with the second page's rescale-merge (block-step mode).
+//
+// Warp roles (NQ = 2):
+//   warps 0-3  softmax + O rescale + epilogue for query tile 0 (thread = row)
+//   warps 4-7  the same for query tile 1
+//   warp 8     TMA producer: Q once, then K and V tiles into 2-deep rings
+//   warp 9     TMEM allocator and MMA issuer (lane 0)
+// TMEM columns: S_t/P_t at [128 t, 128 t + 128), O_t at [128 NQ + 128 t, ...).
+// P_t (bf16) overwrites the first 64 columns of S_t and feeds the PV MMA
+// straight from TMEM.
+//
+// Exponentials are base 2 with log2(e) folded into the scale.  The running
+// max used as the exponent shift is only raised when a row's max grows by
+// more than 8 (log2 units), so most tiles skip the O rescale; P stays
+// <= 2^8 and the result is unchanged because O and l share the same shift.
+// The exact running max is tracked alongside for the block-step state.
+#include <climits>
+#include <cmath>
+
+#include "ra_internal.cuh"
+#include "ra_ptx.cuh"
+
+namespace ra {
+
+namespace {
+
+constexpr float kRescaleThreshold = 8.0f;
+constexpr unsigned int kFull = 0xffffffffu;
+
+template <int D, int NQ>
+struct FwdCfg {
+  static constexpr int kHalves = D / 64;          // 64-column (128-byte) swizzle atoms per row
+  static constexpr int kHalfBytes = kTile * 128;  // 128 rows x 128 bytes
+  static constexpr int kTileBytes = kHalves * kHalfBytes;
+  static constexpr int kKSt = 2;
+  static constexpr int kVSt = 2;
+  static constexpr int kQOff = 0;
+  static constexpr int kKOff = kQOff + NQ * kTileBytes;
+  static constexpr int kVOff = kKOff + kKSt * kTileBytes;
+  static constexpr int kBarOff = kVOff + kVSt * kTileBytes;
+  static constexpr int bQFull = 0;
+  static constexpr int bKFull = 1;
+  static constexpr int bKEmpty = bKFull + kKSt;
+  static constexpr int bVFull = bKEmpty + kKSt;
+  static constexpr int bVEmpty = bVFull + kVSt;
+  static constexpr int bSFull = bVEmpty + kVSt;
+  static constexpr int bPReady = bSFull + NQ;
+  static constexpr int bODone = bPReady + NQ;
+  static constexpr int bDrain = bODone + NQ;
+  static constexpr int kNumBars = bDrain + 1;
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+  static constexpr int kSmemBytes = kMiscOff + 16;
+  static constexpr int kSmemAlloc = kSmemBytes + 1024;
+  static constexpr int kSoftmaxWarps = 4 * NQ;
+  static constexpr int kProducerWarp = kSoftmaxWarps;
+  static constexpr int kMmaWarp = kSoftmaxWarps + 1;
+  // NQ = 2: three full warpgroups (the last holds the producer, the MMA
+  // issuer and two idle warps) so registers can be re-split per warpgroup:
+  // 168 per thread at launch = 2 x 128 x 216 (softmax) + 128 x 72 (rest).
+  static constexpr bool kResplit = NQ == 2;
+  static constexpr int kThreads = kResplit ? 384 : (kSoftmaxWarps + 2) * 32;
+  static constexpr int kSoftmaxRegs = 216;
+  static constexpr int kOtherRegs = 72;
+  static constexpr uint32_t kTmemCols = NQ == 2 ? 512u : 256u;
+  static constexpr uint32_t kOCol0 = NQ * 128u;
+  static constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false, false);
+  static constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, false, true);
+};
+
+// Error sites recorded with a timeout (role * 16 + wait index).
+enum : unsigned int {
+  kSiteProdK = 0x11, kSiteProdV = 0x12,
+  kSiteMmaQ = 0x21, kSiteMmaK = 0x22, kSiteMmaV = 0x23, kSiteMmaP = 0x24,
+  kSiteSmS = 0x31, kSiteSmO = 0x32,
+};
+
+struct Unit {
+  int bb, kh, pr, i, a;
+  int qmin, qmax;  // token positions of the tile's first and last existing row
+};
+
+// Work-unit order: groups of (batch, kv head, query shard); inside a group the
+// query tiles run from the last (most key tiles under a causal mask) to the
+// first, so concurrently resident CTAs walk the same shards of the same KV
+// head (L2 reuse) and long units start first.
+__device__ __forceinline__ Unit decode_unit(const FwdParams &p, long long u) {
+  Unit x;
+  const long long per_group = static_cast<long long>(p.n_qtiles) * p.pairs;
+  const long long grp = u / per_group;
+  const int w = static_cast<int>(u % per_group);
+  x.a = p.n_qtiles - 1 - w / p.pairs;
+  x.pr = w % p.pairs;
+  x.i = static_cast<int>(grp % p.N);
+  const long long g2 = grp / p.N;
+  x.kh = static_cast<int>(g2 % p.n_kv);
+  x.bb = static_cast<int>(g2 / p.n_kv);
+  x.qmin = 0;
+  x.qmax = 0;
+  return x;
+}
+
+__device__ __forceinline__ int warp_min(int v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = min(v, __shfl_xor_sync(kFull, v, o));
+  return v;
+}
+__device__ __forceinline__ int warp_max(int v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(kFull, v, o));
+  return v;
+}
+
+// Token positions covered by the unit's query tile.  Warp-collective in
+// block mode (positions come from q_pos).
+__device__ __forceinline__ void unit_qrange(const FwdParams &p, Unit &x) {
+  const int r0 = x.a * kTile;
+  const int r1 = min(r0 + kTile, p.L) - 1;
+  if (!p.block_mode) {
+    x.qmin = token_at(p.layout, p.L, p.N, x.i, r0);
+    x.qmax = token_at(p.layout, p.L, p.N, x.i, r1);
+    return;
+  }
+  int lo = INT_MAX, hi = INT_MIN;
+  if (p.causal) {
+    for (int r = r0 + (threadIdx.x & 31); r <= r1; r += 32) {
+      const int v = p.q_pos[r];
+      lo = min(lo, v);
+      hi = max(hi, v);
+    }
+    lo = warp_min(lo);
+    hi = warp_max(hi);
+  }
+  x.qmin = lo;
+  x.qmax = hi;
+}
+
+struct KvIter {
+  int s = -1, j = 0, c = 0, c_end = 0, c_full = 0;
+};
+
+// Next key/value tile of the unit in ring order.  Returns false at the end.
+// `partial` marks tiles that need an element mask (causal diagonal or the
+// ragged last tile).  Warp-collective in block mode.
+__device__ __forceinline__ bool kv_next(const FwdParams &p, const Unit &x, KvIter &it, int &j,
+                                        int &c, bool &partial) {
+  const int n_complete = p.Lk / kTile;
+  if (!p.block_mode) {
+    while (it.c >= it.c_end) {
+      if (++it.s >= p.N) return false;
+      it.j = kv_shard_at(x.i, it.s, p.N);
+      it.c = 0;
+      if (!p.causal) {
+        it.c_end = p.n_ktiles;
+        it.c_full = n_complete;
+      } else {
+        // keys visible to the latest query form a prefix [0, lim] of the shard;
+        // keys visible to the earliest query form [0, limf].
+        const int lim = last_visible_row(p.layout, p.L, p.N, it.j, x.qmax);
+        const int limf = last_visible_row(p.layout, p.L, p.N, it.j, x.qmin);
+        it.c_end = lim < 0 ? 0 : min(p.n_ktiles, lim / kTile + 1);
+        it.c_full = limf < kTile - 1 ? 0 : min(n_complete, (limf - (kTile - 1)) / kTile + 1);
+        it.c_full = min(it.c_full, it.c_end);
+      }
+    }
+    j = it.j;
+    c = it.c;
+    partial = it.c >= it.c_full;
+    ++it.c;
+    return true;
+  }
+  while (it.c < p.n_ktiles) {
+    c = it.c++;
+    j = 0;
+    if (!p.causal) {
+      partial = c >= n_complete;
+      return true;
+    }
+    int lo = INT_MAX, hi = INT_MIN;
+    for (int e = threadIdx.x & 31; e < kTile; e += 32) {
+      const int kr = c * kTile + e;
+      if (kr < p.Lk) {
+        const int v = p.k_pos[kr];
+        lo = min(lo, v);
+        hi = max(hi, v);
+      }
+    }
+    lo = warp_min(lo);
+    hi = warp_max(hi);
+    if (lo > x.qmax) continue;  // every key after every query: skip
+    partial = (c >= n_complete) || (hi > x.qmin);
+    return true;
+  }
+  return false;
+}
+
+// (c2, c3) tensor-map coordinates of local row r of shard p: striped maps are
+// (.., shard, row, ..), contiguous ones (.., row, shard, ..).
+__device__ __forceinline__ void shard_coords(int layout, int p, int r, int &c2, int &c3) {
+  if (layout == RA_LAYOUT_STRIPED) {
+    c2 = p;
+    c3 = r;
+  } else {
+    c2 = r;
+    c3 = p;
+  }
+}
+
+template <int D>
+__device__ __forceinline__ void issue_s_mma(uint32_t tS, uint32_t q_saddr, uint32_t k_saddr,
+                                            uint32_t idesc) {
+  // S = Q K^T: A = Q (128 x D, K-major), B = K (128 keys x D, K-major).
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint32_t off = (kk >> 2) * (kTile * 128) + (kk & 3) * 32;
+    mma_ss(tS, smem_desc_sw128(q_saddr + off, 16, 1024), smem_desc_sw128(k_saddr + off, 16, 1024),
+           idesc, kk > 0 ? 1u : 0u);
+  }
+}
+
+template <int D>
+__device__ __forceinline__ void issue_pv_mma(uint32_t tO, uint32_t tP, uint32_t v_saddr,
+                                             uint32_t idesc, bool accumulate) {
+  // O (+)= P V: A = P from TMEM (128 x 128 bf16, 2 per column),
+  // B = V (128 keys x D, MN-major: 64-column atoms 16 KB apart, 8-key
+  // groups 1 KB apart; 16 keys per instruction).
+#pragma unroll
+  for (int kk = 0; kk < kTile / 16; ++kk) {
+    mma_ts(tO, tP + kk * 8, smem_desc_sw128(v_saddr + kk * 16 * 128, kTile * 128, 1024), idesc,
+           (accumulate || kk > 0) ? 1u : 0u);
+  }
+}
+
+template <int D, int NQ>
+__global__ void __launch_bounds__(FwdCfg<D, NQ>::kThreads, 1)
+    fwd_kernel(const __grid_constant__ FwdParams p, const __grid_constant__ CUtensorMap qmap,
+               const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap) {
+  using C = FwdCfg<D, NQ>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+  uint8_t *smem = smem_raw + pad;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kBarOff);
+  uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + C::kMiscOff);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kMiscOff + 4);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t sbase = smem_u32(smem);
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars[C::bQFull], 1);
+    for (int s = 0; s < C::kKSt; ++s) {
+      mbar_init(&bars[C::bKFull + s], 1);
+      mbar_init(&bars[C::bKEmpty + s], 1);
+    }
+    for (int s = 0; s < C::kVSt; ++s) {
+      mbar_init(&bars[C::bVFull + s], 1);
+      mbar_init(&bars[C::bVEmpty + s], 1);
+    }
+    for (int t = 0; t < NQ; ++t) {
+      mbar_init(&bars[C::bSFull + t], 1);
+      mbar_init(&bars[C::bPReady + t], 4);
+      mbar_init(&bars[C::bODone + t], 1);
+    }
+    mbar_init(&bars[C::bDrain], 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == C::kMmaWarp) {
+    tmem_alloc(tmem_holder, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+
+  Unit x = decode_unit(p, blockIdx.x);
+  unit_qrange(p, x);
+
+  if (warp >= C::kSoftmaxWarps) {
+    if constexpr (C::kResplit) regs_decrease<C::kOtherRegs>();
+  if (warp == C::kProducerWarp) {
+    // ------------------------------------------------------------ producer
+    int c2, c3;
+    if (lane == 0) {
+      prefetch_tmap(&qmap);
+      prefetch_tmap(&kmap);
+      prefetch_tmap(&vmap);
+      mbar_arrive_expect_tx(&bars[C::bQFull], NQ * C::kTileBytes);
+      shard_coords(p.layout, x.i, x.a * kTile, c2, c3);
+#pragma unroll
+      for (int t = 0; t < NQ; ++t) {
+        const int hq = x.kh * p.g + x.pr * NQ + t;
+#pragma unroll
+        for (int hf = 0; hf < C::kHalves; ++hf)
+          tma_load_5d(smem + C::kQOff + t * C::kTileBytes + hf * C::kHalfBytes, &qmap,
+                      &bars[C::bQFull], hf * 64, hq, c2, c3, x.bb);
+      }
+    }
+    int k_par[C::kKSt], v_par[C::kVSt];
+    for (int s = 0; s < C::kKSt; ++s) k_par[s] = -1;
+    for (int s = 0; s < C::kVSt; ++s) v_par[s] = -1;
+    KvIter it;
+    int j, c, n = 0;
+    bool partial;
+    while (kv_next(p, x, it, j, c, partial)) {
+      if (lane == 0) {
+        shard_coords(p.layout, j, c * kTile, c2, c3);
+        const int ks = n % C::kKSt;
+        const uint32_t kph = (n / C::kKSt) & 1;
+        if (mbar_wait(&bars[C::bKEmpty + ks], kph ^ 1, abort_flag, kSiteProdK)) {
+          mbar_arrive_expect_tx(&bars[C::bKFull + ks], C::kTileBytes);
+#pragma unroll
+          for (int hf = 0; hf < C::kHalves; ++hf)
+            tma_load_5d(smem + C::kKOff + ks * C::kTileBytes + hf * C::kHalfBytes, &kmap,
+                        &bars[C::bKFull + ks], hf * 64, x.kh, c2, c3, x.bb);
+          k_par[ks] = static_cast<int>(kph);
+          const int vs = n % C::kVSt;
+          const uint32_t vph = (n / C::kVSt) & 1;
+          if (mbar_wait(&bars[C::bVEmpty + vs], vph ^ 1, abort_flag, kSiteProdV)) {
+            mbar_arrive_expect_tx(&bars[C::bVFull + vs], C::kTileBytes);
+#pragma unroll
+            for (int hf = 0; hf < C::kHalves; ++hf)
+              tma_load_5d(smem + C::kVOff + vs * C::kTileBytes + hf * C::kHalfBytes, &vmap,
+                          &bars[C::bVFull + vs], hf * 64, x.kh, c2, c3, x.bb);
+            v_par[vs] = static_cast<int>(vph);
+          }
+        }
+      }
+      __syncwarp();
+      if (*abort_flag) break;
+      ++n;
+    }
+    if (lane == 0 && *abort_flag) {
+      // Let every copy this warp started land before the CTA unwinds.
+      mbar_wait_budget(&bars[C::bQFull], 0, kWaitBudgetCycles);
+      for (int s = 0; s < C::kKSt; ++s)
+        if (k_par[s] >= 0) mbar_wait_budget(&bars[C::bKFull + s], k_par[s], kWaitBudgetCycles);
+      for (int s = 0; s < C::kVSt; ++s)
+        if (v_par[s] >= 0) mbar_wait_budget(&bars[C::bVFull + s], v_par[s], kWaitBudgetCycles);
+    }
+  } else if (warp == C::kMmaWarp) {
+    // ------------------------------------------------------------ MMA issuer
+    bool ok = true;
+    if (lane == 0) ok = mbar_wait(&bars[C::bQFull], 0, abort_flag, kSiteMmaQ);
+    ok = __shfl_sync(kFull, ok ? 1 : 0, 0) != 0;
+    if (ok) {
+      tc_fence_after();
+      const uint32_t q_saddr = sbase + C::kQOff;
+      const uint32_t k_saddr = sbase + C::kKOff;
+      const uint32_t v_saddr = sbase + C::kVOff;
+      KvIter it;
+      int j, c, n = 0;
+      bool partial;
+      bool has = kv_next(p, x, it, j, c, partial);
+      if (has && lane == 0) {
+        if (mbar_wait(&bars[C::bKFull + 0], 0, abort_flag, kSiteMmaK)) {
+          tc_fence_after();
+#pragma unroll
+          for (int t = 0; t < NQ; ++t) {
+            issue_s_mma<D>(tmem + t * 128, q_saddr + t * C::kTileBytes, k_saddr, C::kIdescS);
+            mma_commit(&bars[C::bSFull + t]);
+          }
+          mma_commit(&bars[C::bKEmpty + 0]);
+        }
+      }
+      __syncwarp();
+      while (has && !*abort_flag) {
+        const bool has_next = kv_next(p, x, it, j, c, partial);
+        if (lane == 0) {
+          const int vs = n % C::kVSt;
+          const uint32_t vph = (n / C::kVSt) & 1;
+          const int ks = (n + 1) % C::kKSt;
+          const uint32_t kph = ((n + 1) / C::kKSt) & 1;
+          bool go = mbar_wait(&bars[C::bVFull + vs], vph, abort_flag, kSiteMmaV);
+          if (go) tc_fence_after();
+#pragma unroll
+          for (int t = 0; t < NQ; ++t) {
+            if (!go) break;
+            go = mbar_wait(&bars[C::bPReady + t], n & 1, abort_flag, kSiteMmaP);
+            if (!go) break;
+            tc_fence_after();
+            issue_pv_mma<D>(tmem + C::kOCol0 + t * 128, tmem + t * 128,
+                            v_saddr + vs * C::kTileBytes, C::kIdescPV, n > 0);
+            if (t == NQ - 1) mma_commit(&bars[C::bVEmpty + vs]);
+            if (has_next) {
+              if (t == 0) {
+                go = mbar_wait(&bars[C::bKFull + ks], kph, abort_flag, kSiteMmaK);
+                if (!go) break;
+                tc_fence_after();
+              }
+              issue_s_mma<D>(tmem + t * 128, q_saddr + t * C::kTileBytes,
+                             k_saddr + ks * C::kTileBytes, C::kIdescS);
+              mma_commit(&bars[C::bSFull + t]);
+              if (t == NQ - 1) mma_commit(&bars[C::bKEmpty + ks]);
+            } else {
+              mma_commit(&bars[C::bODone + t]);
+            }
+          }
+        }
+        __syncwarp();
+        ++n;
+        has = has_next;
+      }
+    }
+    if (lane == 0) {
+      // Every MMA this thread issued has finished before TMEM is released.
+      mma_commit(&bars[C::bDrain]);
+      mbar_wait_budget(&bars[C::bDrain], 0, kWaitBudgetCycles);
+    }
+    __syncwarp();
+  }
+  } else {
+    if constexpr (C::kResplit) regs_increase<C::kSoftmaxRegs>();
+    // ------------------------------------------------------------ softmax
+    const int t = warp >> 2;                // query tile of this warpgroup
+    const int row = (warp & 3) * 32 + lane;  // TMEM lane == tile row
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + lane_off + t * 128;
+    const uint32_t tO = tmem + lane_off + C::kOCol0 + t * 128;
+    const int hq = x.kh * p.g + x.pr * NQ + t;
+    const int r_abs = x.a * kTile + row;
+    const bool row_exists = r_abs < p.L;
+    const int r_cl = row_exists ? r_abs : p.L - 1;
+    const int qp = p.block_mode ? (p.causal ? p.q_pos[r_cl] : 0)
+                                : token_at(p.layout, p.L, p.N, x.i, r_cl);
+    const float sl2 = p.scale_log2;
+
+    float m_run = -INFINITY;  // exponent shift (log2 units of the scaled logits)
+    float m_max = -INFINITY;  // exact running row max (same units)
+    float l_sum = 0.f;
+    KvIter it;
+    int j, c, n = 0;
+    bool partial;
+    bool aborted = false;
+    while (kv_next(p, x, it, j, c, partial)) {
+      const bool got = mbar_wait(&bars[C::bSFull + t], n & 1, abort_flag, kSiteSmS);
+      if (!__all_sync(kFull, got)) {  // tcgen05.ld/st below are warp-collective
+        aborted = true;
+        break;
+      }
+      tc_fence_after();
+      float s[kTile];
+#pragma unroll
+      for (int ch = 0; ch < kTile / 32; ++ch) {
+        uint32_t r[32];
+        tmem_ld32(tS + ch * 32, r);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) s[ch * 32 + e] = __uint_as_float(r[e]);
+      }
+      if (partial) {
+        if (!p.block_mode) {
+          int lim = p.Lk - 1;
+          if (p.causal) lim = min(lim, last_visible_row(p.layout, p.L, p.N, j, qp));
+          const int climit = lim - c * kTile;
+#pragma unroll
+          for (int e = 0; e < kTile; ++e)
+            if (e > climit) s[e] = -INFINITY;
+        } else {
+#pragma unroll
+          for (int e = 0; e < kTile; ++e) {
+            const int kr = c * kTile + e;
+            const bool vis = kr < p.Lk && (!p.causal || __ldg(p.k_pos + kr) <= qp);
+            if (!vis) s[e] = -INFINITY;
+          }
+        }
+      }
+      float mx = s[0];
+#pragma unroll
+      for (int e = 1; e < kTile; ++e) mx = fmaxf(mx, s[e]);
+      const float mx2 = mx * sl2;
+      m_max = fmaxf(m_max, mx2);
+      const bool need = mx2 > m_run + kRescaleThreshold;
+      float alpha = 1.f;
+      if (need) {
+        alpha = ex2(m_run - mx2);  // 0 when m_run is still -inf
+        m_run = mx2;
+      }
+      if (n > 0 && __any_sync(kFull, need)) {
+        // O_t row *= alpha.  The previous PV into O_t is complete: it was
+        // issued before this tile's S MMA, whose commit we waited on.
+#pragma unroll
+        for (int ch = 0; ch < D / 32; ++ch) {
+          uint32_t r[32];
+          tmem_ld32(tO + ch * 32, r);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+          tmem_st32(tO + ch * 32, r);
+        }
+      }
+      l_sum *= alpha;
+      const float base = (m_run == -INFINITY) ? 0.f : m_run;
+      float rs = 0.f;
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const float p0 = ex2(fmaf(s[q4 * 32 + 2 * e], sl2, -base));
+          const float p1 = ex2(fmaf(s[q4 * 32 + 2 * e + 1], sl2, -base));
+          rs += p0 + p1;
+          pk[e] = pack_bf16x2(p0, p1);
+        }
+        tmem_st16(tS + q4 * 16, pk);
+      }
+      l_sum += rs;
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[C::bPReady + t]);
+      ++n;
+    }
+
+    // ------------------------------------------------------------ epilogue
+    bool have_o = n > 0 && !aborted;
+    if (have_o) {
+      if (!mbar_wait(&bars[C::bODone + t], 0, abort_flag, kSiteSmO)) have_o = false;
+      tc_fence_after();
+    }
+    have_o = __all_sync(kFull, have_o && *abort_flag == 0);
+    if (!p.block_mode) {
+      const int tok = token_at(p.layout, p.L, p.N, x.i, r_cl);
+      const size_t orow = ((static_cast<size_t>(x.bb) * p.S + tok) * p.h + hq) * D;
+      const bool live = have_o && l_sum > 0.f;
+      const float inv_l = live ? 1.f / l_sum : 0.f;
+      if (row_exists && !*abort_flag)
+        p.lse[(static_cast<size_t>(x.bb) * p.h + hq) * p.S + tok] =
+            live ? (m_run + log2f(l_sum)) * kLn2 : -INFINITY;
+#pragma unroll
+      for (int ch = 0; ch < D / 32; ++ch) {
+        uint32_t r[32];
+        if (have_o) tmem_ld32(tO + ch * 32, r);
+        if (row_exists && !*abort_flag) {
+          float4 *dst = reinterpret_cast<float4 *>(p.out + orow + ch * 32);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            float4 v4;
+            v4.x = live ? __uint_as_float(r[4 * e + 0]) * inv_l : 0.f;
+            v4.y = live ? __uint_as_float(r[4 * e + 1]) * inv_l : 0.f;
+            v4.z = live ? __uint_as_float(r[4 * e + 2]) * inv_l : 0.f;
+            v4.w = live ? __uint_as_float(r[4 * e + 3]) * inv_l : 0.f;
+            dst[e] = v4;
+          }
+        }
+      }
+    } else {
+      // Fold the block result (shift m_run, sum l_sum, numerator in TMEM)
+      // into the caller's state, re-referenced to the exact running max.
+      const size_t si = (static_cast<size_t>(x.bb) * p.h + hq) * p.L + r_cl;
+      const size_t oi = ((static_cast<size_t>(x.bb) * p.L + r_cl) * p.h + hq) * D;
+      const float m_old2 = row_exists ? p.st_m[si] * kLog2e : -INFINITY;
+      const float M = fmaxf(m_old2, have_o ? m_max : -INFINITY);
+      const bool write = row_exists && !*abort_flag && have_o && M != -INFINITY;
+      const float a_old = (m_old2 == -INFINITY) ? 0.f : ex2(m_old2 - M);
+      const float a_blk = (!have_o || m_run == -INFINITY) ? 0.f : ex2(m_run - M);
+      if (write) {
+        p.st_l[si] = p.st_l[si] * a_old + l_sum * a_blk;
+        p.st_m[si] = M * kLn2;
+      }
+#pragma unroll
+      for (int ch = 0; ch < D / 32; ++ch) {
+        uint32_t r[32];
+        if (have_o) tmem_ld32(tO + ch * 32, r);
+        if (write) {
+          float4 *dst = reinterpret_cast<float4 *>(p.st_o + oi + ch * 32);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            float4 v4 = dst[e];
+            v4.x = v4.x * a_old + __uint_as_float(r[4 * e + 0]) * a_blk;
+            v4.y = v4.y * a_old + __uint_as_float(r[4 * e + 1]) * a_blk;
+            v4.z = v4.z * a_old + __uint_as_float(r[4 * e + 2]) * a_blk;
+            v4.w = v4.w * a_old + __uint_as_float(r[4 * e + 3]) * a_blk;
+            dst[e] = v4;
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == C::kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+template <int D, int NQ>
+cudaError_t launch_fwd_t(const FwdParams &p, const CUtensorMap &qmap, const CUtensorMap &kmap,
+                         const CUtensorMap &vmap, long long n_units, cudaStream_t stream) {
+  using C = FwdCfg<D, NQ>;
+  auto kern = fwd_kernel<D, NQ>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemAlloc);
+  if (e != cudaSuccess) return e;
+  if constexpr (C::kResplit) {
+    // The register increase in the kernel waits until the pool covers it.
+    cudaFuncAttributes attr;
+    e = cudaFuncGetAttributes(&attr, kern);
+    if (e != cudaSuccess) return e;
+    const long long pool = static_cast<long long>(attr.numRegs) * C::kThreads;
+    const long long want = 2LL * 128 * C::kSoftmaxRegs + 128LL * C::kOtherRegs;
+    if (pool < want) return cudaErrorInvalidConfiguration;
+  }
+  kern<<<dim3(static_cast<unsigned int>(n_units)), dim3(C::kThreads), C::kSmemAlloc, stream>>>(
+      p, qmap, kmap, vmap);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd(const FwdParams &p, int d, int nq, const CUtensorMap &qmap,
+                       const CUtensorMap &kmap, const CUtensorMap &vmap, long long n_units,
+                       cudaStream_t stream) {
+  if (n_units <= 0) return cudaSuccess;
+  if (d == 128 && nq == 2) return launch_fwd_t<128, 2>(p, qmap, kmap, vmap, n_units, stream);
+  if (d == 128 && nq == 1) return launch_fwd_t<128, 1>(p, qmap, kmap, vmap, n_units, stream);
+  if (d == 64 && nq == 2) return launch_fwd_t<64, 2>(p, qmap, kmap, vmap, n_units, stream);
+  if (d == 64 && nq == 1) return launch_fwd_t<64, 1>(p, qmap, kmap, vmap, n_units, stream);
+  return cudaErrorInvalidValue;
+}
+
+RA_DEFINE_ERROR_WORD_READER(read_error_word_fwd)
+
+}  // namespace ra

@@ -1,0 +1,177 @@
+// ra_small.cu -- the HBM-bound and bookkeeping kernels: finalize, the
+// two-sided rescale-merge, the token-placement and ring-order maps, and the
+// bounded-wait self test.  Also home of the device error word.
+#include <cmath>
+
+#include "ra_internal.cuh"
+#include "ra_ptx.cuh"
+
+namespace ra {
+
+namespace {
+
+constexpr int kEwThreads = 256;
+
+// Grid size for a grid-stride loop over `work` items: enough CTAs to fill
+// every SM several times, never more than the work needs.
+inline unsigned int ew_grid(long long work) {
+  static int n_sm = 0;
+  if (n_sm == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        n_sm <= 0)
+      n_sm = 152;
+  }
+  const long long want = (work + kEwThreads - 1) / kEwThreads;
+  const long long cap = static_cast<long long>(n_sm) * 8;
+  return static_cast<unsigned int>(want < 1 ? 1 : (want < cap ? want : cap));
+}
+
+// One warp per (batch, head, row); lanes stride the d columns with float4.
+// o <- o / l, lse = m + ln l; rows with l == 0 get 0 and -inf.
+__global__ void finalize_kernel(float *o, const float *l, const float *m, float *lse, int b,
+                                long long Lq, int h, int d) {
+  const long long rows = static_cast<long long>(b) * h * Lq;
+  const int lane = threadIdx.x & 31;
+  const long long warps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
+  for (long long w = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; w < rows;
+       w += warps) {
+    const long long r = w % Lq;
+    const long long bh = w / Lq;
+    const int hq = static_cast<int>(bh % h);
+    const long long bb = bh / h;
+    const float lr = l[w];
+    const bool live = lr > 0.f;
+    const float inv = live ? 1.f / lr : 0.f;
+    if (lane == 0) lse[w] = live ? m[w] + logf(lr) : -INFINITY;
+    float4 *row = reinterpret_cast<float4 *>(o + ((bb * Lq + r) * h + hq) * d);
+    for (int e = lane; e < d / 4; e += 32) {
+      float4 v = row[e];
+      v.x *= inv;
+      v.y *= inv;
+      v.z *= inv;
+      v.w *= inv;
+      row[e] = v;
+    }
+  }
+}
+
+// Rescale-merge of two normalised partial results over disjoint keys.
+__global__ void merge_kernel(const float *o_a, const float *lse_a, const float *o_b,
+                             const float *lse_b, float *o, float *lse, int b, long long Lq, int h,
+                             int d) {
+  const long long rows = static_cast<long long>(b) * h * Lq;
+  const int lane = threadIdx.x & 31;
+  const long long warps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
+  for (long long w = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; w < rows;
+       w += warps) {
+    const long long r = w % Lq;
+    const long long bh = w / Lq;
+    const int hq = static_cast<int>(bh % h);
+    const long long bb = bh / h;
+    const float la = lse_a[w], lb = lse_b[w];
+    const float mx = fmaxf(la, lb);
+    float wa = 0.f, wb = 0.f, out_lse = -INFINITY;
+    if (mx != -INFINITY) {
+      wa = (la == -INFINITY) ? 0.f : expf(la - mx);
+      wb = (lb == -INFINITY) ? 0.f : expf(lb - mx);
+      const float den = wa + wb;
+      out_lse = mx + logf(den);
+      wa /= den;
+      wb /= den;
+    }
+    const size_t off = ((bb * Lq + r) * h + hq) * d;
+    const float4 *ra4 = reinterpret_cast<const float4 *>(o_a + off);
+    const float4 *rb4 = reinterpret_cast<const float4 *>(o_b + off);
+    float4 *ro4 = reinterpret_cast<float4 *>(o + off);
+    for (int e = lane; e < d / 4; e += 32) {
+      const float4 a = ra4[e], c = rb4[e];
+      float4 v;
+      v.x = (wa == 0.f ? 0.f : wa * a.x) + (wb == 0.f ? 0.f : wb * c.x);
+      v.y = (wa == 0.f ? 0.f : wa * a.y) + (wb == 0.f ? 0.f : wb * c.y);
+      v.z = (wa == 0.f ? 0.f : wa * a.z) + (wb == 0.f ? 0.f : wb * c.z);
+      v.w = (wa == 0.f ? 0.f : wa * a.w) + (wb == 0.f ? 0.f : wb * c.w);
+      ro4[e] = v;
+    }
+    __syncwarp();
+    if (lane == 0) lse[w] = out_lse;
+  }
+}
+
+__global__ void position_map_kernel(int layout, int S, int N, int32_t *shard_of,
+                                    int32_t *local_of, int32_t *token_of) {
+  const int L = S / N;
+  for (long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; idx < S;
+       idx += static_cast<long long>(gridDim.x) * blockDim.x) {
+    // idx enumerates (shard p, local row r); the token is where it lands.
+    const int p = static_cast<int>(idx / L);
+    const int r = static_cast<int>(idx % L);
+    const int t = token_at(layout, L, N, p, r);
+    if (shard_of) shard_of[t] = p;
+    if (local_of) local_of[t] = r;
+    if (token_of) token_of[idx] = t;
+  }
+}
+
+__global__ void ring_order_kernel(int N, int32_t *order) {
+  const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx < N * N) order[idx] = kv_shard_at(idx / N, idx % N, N);
+}
+
+// One CTA waits on an mbarrier that nothing arrives on; the bounded wait
+// runs out and the timeout is recorded in the error word.
+__global__ void wait_timeout_selftest_kernel(long long budget) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    if (!mbar_wait_budget(&bar, 0, budget)) raise_error(kErrTimeout, 0xF0);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_finalize(float *o, const float *l, const float *m, float *lse, int b,
+                            long long Lq, int h, int d, cudaStream_t stream) {
+  const long long rows = static_cast<long long>(b) * h * Lq;
+  if (rows == 0) return cudaSuccess;
+  finalize_kernel<<<ew_grid(rows * 32), kEwThreads, 0, stream>>>(o, l, m, lse, b, Lq, h, d);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_merge(const float *o_a, const float *lse_a, const float *o_b,
+                         const float *lse_b, float *o, float *lse, int b, long long Lq, int h,
+                         int d, cudaStream_t stream) {
+  const long long rows = static_cast<long long>(b) * h * Lq;
+  if (rows == 0) return cudaSuccess;
+  merge_kernel<<<ew_grid(rows * 32), kEwThreads, 0, stream>>>(o_a, lse_a, o_b, lse_b, o, lse, b,
+                                                              Lq, h, d);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_position_map(int layout, int S, int N, int32_t *shard_of, int32_t *local_of,
+                                int32_t *token_of, cudaStream_t stream) {
+  if (S == 0) return cudaSuccess;
+  position_map_kernel<<<ew_grid(S), kEwThreads, 0, stream>>>(layout, S, N, shard_of, local_of,
+                                                             token_of);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_ring_order(int N, int32_t *order, cudaStream_t stream) {
+  const int n = N * N;
+  ring_order_kernel<<<(n + kEwThreads - 1) / kEwThreads, kEwThreads, 0, stream>>>(N, order);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_wait_timeout_selftest(long long budget, cudaStream_t stream) {
+  wait_timeout_selftest_kernel<<<1, 32, 0, stream>>>(budget);
+  return cudaGetLastError();
+}
+
+RA_DEFINE_ERROR_WORD_READER(read_error_word_small)
+
+}  // namespace ra

@@ -1,0 +1,123 @@
+"""Host-side checks of the C ABI that need no GPU: the library builds and
+loads, exports every entry point ``include/ra.h`` declares, and rejects bad
+arguments on the host before touching CUDA."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from long_context_exact_gb300 import binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ra.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from long_context_exact_gb300 import build as b
+    b.build()
+    return binding.load()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ra_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    for required in ("ra_block_step", "ra_finalize", "ra_merge", "ra_ring_attention",
+                     "ra_ring_attention_bwd", "ra_bwd_workspace_size", "ra_position_map",
+                     "ra_ring_order", "ra_stream_check", "ra_last_error"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_version(lib):
+    assert lib.ra_version() >= 100
+
+
+def _dims(b=1, h=4, n_kv=2, d=128):
+    return binding.Dims(b, h, n_kv, d)
+
+
+FAKE = ctypes.c_void_p(0x10000)      # aligned, never dereferenced: calls fail earlier
+MISALIGNED = ctypes.c_void_p(0x10008)
+
+
+@pytest.mark.parametrize("dims,status", [
+    (dict(d=96), binding.RA_ERR_UNSUPPORTED),
+    (dict(h=6, n_kv=4), binding.RA_ERR_UNSUPPORTED),
+    (dict(h=0), binding.RA_ERR_INVALID_ARG),
+    (dict(b=-1), binding.RA_ERR_INVALID_ARG),
+])
+def test_ring_attention_rejects_bad_dims(lib, dims, status):
+    st = lib.ra_ring_attention(FAKE, FAKE, FAKE, FAKE, FAKE, 1024, 4, 1, 1, 0.0, _dims(**dims), None)
+    assert st == status
+    assert lib.ra_last_error()
+
+
+def test_ring_attention_rejects_bad_sizes_and_pointers(lib):
+    d = _dims()
+    assert lib.ra_ring_attention(FAKE, FAKE, FAKE, FAKE, FAKE, 1000, 3, 1, 1, 0.0, d, None) == \
+        binding.RA_ERR_UNSUPPORTED                      # S % N != 0
+    assert lib.ra_ring_attention(FAKE, FAKE, FAKE, FAKE, FAKE, 1024, 0, 1, 1, 0.0, d, None) == \
+        binding.RA_ERR_INVALID_ARG                      # N < 1
+    assert lib.ra_ring_attention(FAKE, FAKE, FAKE, FAKE, FAKE, 1024, 4, 7, 1, 0.0, d, None) == \
+        binding.RA_ERR_INVALID_ARG                      # layout
+    assert lib.ra_ring_attention(None, FAKE, FAKE, FAKE, FAKE, 1024, 4, 1, 1, 0.0, d, None) == \
+        binding.RA_ERR_INVALID_ARG                      # null q
+    assert "q" in lib.ra_last_error().decode()
+    assert lib.ra_ring_attention(FAKE, MISALIGNED, FAKE, FAKE, FAKE, 1024, 4, 1, 1, 0.0, d, None) == \
+        binding.RA_ERR_INVALID_ARG                      # misaligned k
+    assert lib.ra_ring_attention(FAKE, FAKE, FAKE, FAKE, FAKE, 1024, 4, 1, 1, float("nan"), d,
+                                 None) == binding.RA_ERR_INVALID_ARG
+    assert lib.ra_ring_attention(FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 31, 1, 1, 1, 0.0, d, None) == \
+        binding.RA_ERR_UNSUPPORTED
+
+
+def test_empty_inputs_are_a_no_op(lib):
+    d = _dims()
+    assert lib.ra_ring_attention(None, None, None, None, None, 0, 4, 1, 1, 0.0, d, None) == binding.RA_OK
+    assert lib.ra_ring_attention(None, None, None, None, None, 512, 4, 1, 1, 0.0, _dims(b=0),
+                                 None) == binding.RA_OK
+    assert lib.ra_block_step(None, None, None, None, None, None, None, None, 0, 128, d, 1, 0.0,
+                             None) == binding.RA_OK
+    assert lib.ra_finalize(None, None, None, None, 0, d, None) == binding.RA_OK
+    assert lib.ra_merge(None, None, None, None, None, None, 0, d, None) == binding.RA_OK
+
+
+def test_block_step_validation(lib):
+    d = _dims()
+    assert lib.ra_block_step(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, 128, 128, d, 1, 0.0,
+                             None) == binding.RA_ERR_INVALID_ARG   # causal without positions
+    assert lib.ra_block_step(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, -1, 128, d, 0, 0.0,
+                             None) == binding.RA_ERR_INVALID_ARG
+
+
+def test_map_and_order_validation(lib):
+    assert lib.ra_position_map(1, 1000, 3, FAKE, FAKE, FAKE, None) == binding.RA_ERR_UNSUPPORTED
+    assert lib.ra_position_map(5, 1024, 4, FAKE, FAKE, FAKE, None) == binding.RA_ERR_INVALID_ARG
+    assert lib.ra_ring_order(0, FAKE, None) == binding.RA_ERR_INVALID_ARG
+    assert lib.ra_ring_order(4, None, None) == binding.RA_ERR_INVALID_ARG
+    assert lib.ra_selftest_wait_timeout(0, None) == binding.RA_ERR_INVALID_ARG
+
+
+def test_workspace_size(lib):
+    n = lib.ra_bwd_workspace_size(65536, _dims(b=2, h=32, n_kv=8))
+    assert n >= 2 * 32 * 65536 * 4
+    assert lib.ra_bwd_workspace_size(0, _dims()) == 0
+
+
+def test_binding_refuses_cpu_tensors(lib):
+    import torch
+    q = torch.zeros((1, 128, 2, 64), dtype=torch.bfloat16)
+    with pytest.raises(binding.RAError):
+        binding.ring_attention(q, q, q, 1)

@@ -1,0 +1,251 @@
+"""GPU parity of the forward path against the fp64 oracle, through the C ABI.
+
+Tolerances: max-abs 1e-2 on O and 1e-3 on LSE (bf16 inputs, fp32
+accumulation); integer maps bit-exact.  Small cases compare every element;
+the long workloads compare sampled query rows the oracle computes one by one.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from long_context_exact_gb300 import binding as ra
+from long_context_exact_gb300.inputs import (CONTIGUOUS, STRIPED, WORKLOADS, make_inputs,
+                                             sample_rows, workload_inputs)
+
+pytestmark = pytest.mark.gpu
+
+O_TOL = 1e-2
+LSE_TOL = 1e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from long_context_exact_gb300 import build as b
+    b.build()
+    ra.load()
+
+
+def _dev(*ts):
+    return [t.cuda() for t in ts]
+
+
+def _cmp(out, lse, ref_out, ref_lse, rows=None):
+    o = out.double().cpu().numpy()
+    l = lse.double().cpu().numpy()
+    if rows is not None:
+        o = o[:, rows]
+        l = l[:, :, rows]
+    err_o = np.abs(o - ref_out).max()
+    fin = np.isfinite(ref_lse)
+    assert np.array_equal(np.isfinite(l), fin)
+    err_l = np.abs(l[fin] - ref_lse[fin]).max() if fin.any() else 0.0
+    assert err_o <= O_TOL, f"O max-abs {err_o}"
+    assert err_l <= LSE_TOL, f"LSE max-abs {err_l}"
+    return err_o, err_l
+
+
+# ------------------------------------------------------------------ maps
+@pytest.mark.parametrize("layout", [CONTIGUOUS, STRIPED])
+@pytest.mark.parametrize("S,N", [(8, 4), (1024, 4), (65536, 8), (65536, 16), (3 * 200, 3)])
+def test_position_map_bit_exact(orc, layout, S, N):
+    shard, local, tok = ra.position_map(layout, S, N)
+    r_shard, r_local, r_tok = orc.position_map(layout, S, N)
+    assert np.array_equal(shard.cpu().numpy(), r_shard)
+    assert np.array_equal(local.cpu().numpy(), r_local)
+    assert np.array_equal(tok.cpu().numpy(), r_tok)
+
+
+@pytest.mark.parametrize("N", [1, 2, 4, 8, 16, 37])
+def test_ring_order_bit_exact(orc, N):
+    assert np.array_equal(ra.ring_order(N).cpu().numpy(), orc.ring_order(N))
+
+
+# ------------------------------------------------------------------ ring attention
+SMALL = [
+    # b, S, h, n_kv, d, N, layout, causal
+    (1, 1024, 2, 2, 64, 4, CONTIGUOUS, False),     # the tiny workload (g = 1, d = 64)
+    (1, 1024, 8, 2, 128, 4, CONTIGUOUS, False),
+    (1, 1024, 8, 2, 128, 4, CONTIGUOUS, True),
+    (1, 1024, 8, 2, 128, 4, STRIPED, True),
+    (2, 2048, 8, 2, 128, 8, STRIPED, True),
+    (1, 768, 4, 4, 64, 2, STRIPED, True),          # g = 1 causal
+    (1, 600, 8, 2, 128, 3, CONTIGUOUS, True),      # ragged: L = 200
+    (1, 600, 8, 2, 128, 3, STRIPED, True),
+    (1, 600, 6, 2, 64, 3, STRIPED, False),         # g = 3 (odd), ragged, non-causal
+    (1, 300, 4, 1, 128, 1, CONTIGUOUS, True),      # N = 1, ragged single shard
+    (1, 64, 8, 2, 128, 1, STRIPED, True),          # shorter than one tile
+    (1, 1, 2, 1, 64, 1, CONTIGUOUS, True),         # a single token
+]
+
+
+@pytest.mark.parametrize("b,S,h,n_kv,d,N,layout,causal", SMALL)
+def test_ring_attention_matches_oracle(orc, b, S, h, n_kv, d, N, layout, causal):
+    q, k, v = make_inputs(b, S, h, n_kv, d, seed=S + h + d + N)
+    ref_o, ref_l = orc.attn_fwd_rows(q, k, v, causal)
+    out, lse = ra.ring_attention(*_dev(q, k, v), N, layout, causal)
+    ra.stream_check()
+    _cmp(out, lse, ref_o, ref_l)
+
+
+def test_layouts_agree_and_results_are_deterministic():
+    q, k, v = _dev(*make_inputs(1, 4096, 8, 2, 128, seed=5))
+    oc, lc = ra.ring_attention(q, k, v, 8, CONTIGUOUS, True)
+    os_, ls_ = ra.ring_attention(q, k, v, 8, STRIPED, True)
+    ra.stream_check()
+    assert (oc - os_).abs().max().item() < 2e-3
+    assert (lc - ls_).abs().max().item() < 1e-4
+    o2, l2 = ra.ring_attention(q, k, v, 8, STRIPED, True)
+    assert torch.equal(o2, os_) and torch.equal(l2, ls_)
+
+
+def test_custom_scale(orc):
+    q, k, v = make_inputs(1, 512, 4, 2, 128, seed=77)
+    ref_o, ref_l = orc.attn_fwd_rows(q, k, v, True, scale=0.05)
+    out, lse = ra.ring_attention(*_dev(q, k, v), 4, STRIPED, True, scale=0.05)
+    _cmp(out, lse, ref_o, ref_l)
+
+
+# ------------------------------------------------------------------ block step
+@pytest.mark.parametrize("Lq,Lk,causal,g,d", [
+    (256, 256, False, 4, 128), (200, 333, True, 4, 128), (128, 512, True, 1, 64),
+    (384, 130, True, 2, 128), (64, 1000, False, 3, 64),
+])
+def test_block_step_matches_oracle_update(orc, Lq, Lk, causal, g, d):
+    n_kv = 2
+    h = g * n_kv
+    q, _, _ = make_inputs(1, Lq, h, n_kv, d, seed=Lq)
+    _, k, v = make_inputs(1, Lk, h, n_kv, d, seed=Lk + 1)
+    rng = np.random.default_rng(Lq + Lk)
+    q_pos = np.sort(rng.choice(4 * (Lq + Lk), Lq, replace=False)).astype(np.int32)
+    k_pos = np.sort(rng.choice(4 * (Lq + Lk), Lk, replace=False)).astype(np.int32)
+    scale = 1.0 / np.sqrt(d)
+    # a non-trivial starting state from a first block
+    q0, k0, v0 = make_inputs(1, 192, h, n_kv, d, seed=3)
+    k0 = k0[:, :192]
+    v0 = v0[:, :192]
+    k0_pos = np.sort(rng.choice(4 * (Lq + Lk), 192, replace=False)).astype(np.int32)
+    st_ref = orc.new_state(1, Lq, h, d)
+    orc.block_update(q, k0, v0, q_pos, k0_pos, causal, scale, st_ref)
+    orc.block_update(q, k, v, q_pos, k_pos, causal, scale, st_ref)
+
+    qd, kd, vd, k0d, v0d = _dev(q, k, v, k0.contiguous(), v0.contiguous())
+    qp, kp, k0p = (torch.from_numpy(a).cuda() for a in (q_pos, k_pos, k0_pos))
+    st = ra.new_state(1, Lq, h, d, "cuda")
+    ra.block_step(qd, k0d, v0d, st, qp, k0p, causal)
+    ra.block_step(qd, kd, vd, st, qp, kp, causal)
+    ra.stream_check()
+    m, l, o = (t.double().cpu().numpy() for t in st)
+    rm, rl, ro = st_ref
+    fin = np.isfinite(rm)
+    assert np.array_equal(np.isfinite(m), fin)
+    # the state itself: m is the exact running max, l and O relative to it
+    assert np.abs(m[fin] - rm[fin]).max() <= 1e-4
+    rel_l = np.abs(l[fin] - rl[fin]) / rl[fin]
+    assert rel_l.max() <= 1e-3
+    # normalised results
+    out, lse = ra.finalize(st)
+    r_out, r_lse = orc.finalize(st_ref)
+    _cmp(out, lse, r_out, r_lse)
+
+
+def test_block_steps_over_ring_reproduce_full_attention(orc):
+    """ra_block_step over the N shards in ring order, then ra_finalize,
+    equals the direct definition (the pages' exactness claim)."""
+    b, S, h, n_kv, d, N = 1, 1024, 8, 2, 128, 4
+    q, k, v = make_inputs(b, S, h, n_kv, d, seed=99)
+    ref_o, ref_l = orc.attn_fwd_rows(q, k, v, True)
+    _, _, tok = orc.position_map(STRIPED, S, N)
+    order = orc.ring_order(N)
+    out = torch.empty((b, S, h, d), dtype=torch.float32)
+    lse = torch.empty((b, h, S), dtype=torch.float32)
+    qd, kd, vd = _dev(q, k, v)
+    for i in range(N):
+        qt = torch.from_numpy(tok[i].astype(np.int64)).cuda()
+        qi = qd[:, qt].contiguous()
+        st = ra.new_state(b, qi.shape[1], h, d, "cuda")
+        for s in range(N):
+            kt = torch.from_numpy(tok[order[i, s]].astype(np.int64)).cuda()
+            ra.block_step(qi, kd[:, kt].contiguous(), vd[:, kt].contiguous(), st,
+                          qt.int(), kt.int(), True)
+        o_i, l_i = ra.finalize(st)
+        out[:, qt.cpu()] = o_i.cpu()
+        lse[:, :, qt.cpu()] = l_i.cpu()
+    ra.stream_check()
+    _cmp(out, lse, ref_o, ref_l)
+
+
+def test_merge_matches_oracle(orc):
+    b, S, h, n_kv, d = 1, 512, 4, 2, 128
+    q, k, v = make_inputs(b, S, h, n_kv, d, seed=12)
+    pos = np.arange(S, dtype=np.int32)
+    sel = np.random.default_rng(0).permutation(S)
+    parts_ref, parts_gpu = [], []
+    qd, kd, vd = _dev(q, k, v)
+    for idx in (np.sort(sel[:200]), np.sort(sel[200:])):
+        st = orc.new_state(b, S, h, d)
+        ti = torch.from_numpy(idx)
+        orc.block_update(q, k[:, ti], v[:, ti], pos, pos[idx], True, 1 / np.sqrt(d), st)
+        parts_ref.append(orc.finalize(st))
+        sg = ra.new_state(b, S, h, d, "cuda")
+        tid = ti.cuda()
+        ra.block_step(qd, kd[:, tid].contiguous(), vd[:, tid].contiguous(), sg,
+                      torch.from_numpy(pos).cuda(), torch.from_numpy(pos[idx]).cuda(), True)
+        parts_gpu.append(ra.finalize(sg))
+    o, lse = ra.merge(parts_gpu[0][0], parts_gpu[0][1], parts_gpu[1][0], parts_gpu[1][1])
+    ro, rl = orc.merge(parts_ref[0][0], parts_ref[0][1], parts_ref[1][0], parts_ref[1][1])
+    ra.stream_check()
+    _cmp(o, lse, ro, rl)
+    # a side with no keys leaves the other untouched
+    empty_o = torch.zeros_like(o)
+    empty_l = torch.full_like(lse, float("-inf"))
+    o2, l2 = ra.merge(o, lse, empty_o, empty_l)
+    assert torch.allclose(o2, o, atol=1e-6) and torch.allclose(l2, lse, atol=1e-6)
+
+
+# ------------------------------------------------------------------ failure detection
+def test_bounded_wait_reports_timeout():
+    """A wait on a barrier nothing arrives on runs out and is reported; the
+    context stays usable."""
+    ra.selftest_wait_timeout(200000)
+    with pytest.raises(ra.RAError) as ei:
+        ra.stream_check()
+    assert ei.value.status == ra.RA_ERR_DEVICE_TIMEOUT
+    ra.stream_check()   # cleared
+    q, k, v = _dev(*make_inputs(1, 256, 2, 1, 64, seed=1))
+    ra.ring_attention(q, k, v, 2, STRIPED, True)
+    ra.stream_check()
+
+
+# ------------------------------------------------------------------ full-size workloads
+def _workload_parity(orc, name, layouts=None):
+    w = WORKLOADS[name]
+    q, k, v = workload_inputs(w)[:3]
+    rows = sample_rows(w.S, w.n_shards, w.rows_per_head, w.seed)
+    ref_o, ref_l = orc.attn_fwd_rows(q, k, v, w.causal, rows=rows)
+    qd, kd, vd = _dev(q, k, v)
+    errs = {}
+    for layout in (layouts or w.layouts):
+        out, lse = ra.ring_attention(qd, kd, vd, w.n_shards, layout, w.causal)
+        ra.stream_check()
+        errs[layout] = _cmp(out, lse, ref_o, ref_l, rows)
+        del out, lse
+    return errs
+
+
+def test_workload_tiny_all_rows(orc):
+    _workload_parity(orc, "tiny")
+
+
+def test_workload_noncausal_32k(orc):
+    _workload_parity(orc, "noncausal32k")
+
+
+def test_workload_causal_64k_both_layouts(orc):
+    _workload_parity(orc, "causal64k")
+
+
+def test_workload_causal_256k_striped(orc):
+    _workload_parity(orc, "causal256k")
