@@ -214,7 +214,7 @@ def run_ours(a, rank, world, local_rank):
     dq = torch.empty_like(out)
     dk = torch.empty((w.b, w.S, w.n_kv, w.d), dtype=torch.float32, device=dev)
     dv = torch.empty_like(dk)
-    ws = torch.empty(max(ra.bwd_workspace_size(w.S, w.b, w.h, w.n_kv, w.d), 16),
+    ws = torch.empty(max(ra.bwd_workspace_size(w.S, w.n_shards, w.b, w.h, w.n_kv, w.d), 16),
                      dtype=torch.uint8, device=dev)
 
     have_bwd = True

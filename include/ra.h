@@ -127,9 +127,11 @@ ra_status ra_ring_attention(const uint16_t *q, const uint16_t *k, const uint16_t
                             float *lse, int64_t S, int n_shards, ra_layout layout, int causal,
                             float scale, ra_dims dims, void *stream);
 
-/* Bytes of device workspace ra_ring_attention_bwd needs (per-row
- * D = rowsum(dO * O) and the log2-domain LSE). */
-size_t ra_bwd_workspace_size(int64_t S, ra_dims dims);
+/* Bytes of device workspace ra_ring_attention_bwd needs: per query row,
+ * D = rowsum(dO * O) and the log2-domain LSE, both float, stored per shard
+ * with each shard's rows padded to a multiple of 128.  0 if the arguments
+ * are invalid or the problem is empty. */
+size_t ra_bwd_workspace_size(int64_t S, int n_shards, ra_dims dims);
 
 /* Blockwise backward with recomputation ("The Backward Pass and Gradient
  * Exchange"; "The Backward Pass: Symmetric Ring Operation"):
@@ -147,6 +149,8 @@ ra_status ra_ring_attention_bwd(const uint16_t *q, const uint16_t *k, const uint
                                 float *dq, float *dk, float *dv, void *workspace,
                                 size_t workspace_bytes, int64_t S, int n_shards, ra_layout layout,
                                 int causal, float scale, ra_dims dims, void *stream);
+/* (dq is zeroed on the stream and then accumulated; the workspace contents
+ * need no initialisation and are scratch after the call.) */
 
 /* Token placement maps (the third page's section 6 example; "Striped
  * Attention" on the first page), computed on the device by the same functions

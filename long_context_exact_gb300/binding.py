@@ -71,7 +71,7 @@ def load(path: str | None = None):
             fn = getattr(lib, name)
             fn.argtypes = args
             fn.restype = I
-        lib.ra_bwd_workspace_size.argtypes = [I64, Dims]
+        lib.ra_bwd_workspace_size.argtypes = [I64, I, Dims]
         lib.ra_bwd_workspace_size.restype = ctypes.c_size_t
         lib.ra_last_error.argtypes = []
         lib.ra_last_error.restype = ctypes.c_char_p
@@ -195,8 +195,8 @@ def merge(o_a, lse_a, o_b, lse_b, o=None, lse=None, stream=None):
 
 
 # ---------------------------------------------------------------- backward
-def bwd_workspace_size(S: int, b: int, h: int, n_kv: int, d: int) -> int:
-    return int(load().ra_bwd_workspace_size(S, _dims(b, h, n_kv, d)))
+def bwd_workspace_size(S: int, n_shards: int, b: int, h: int, n_kv: int, d: int) -> int:
+    return int(load().ra_bwd_workspace_size(S, int(n_shards), _dims(b, h, n_kv, d)))
 
 
 def ring_attention_bwd(q, k, v, out, lse, dout, n_shards: int, layout: int = STRIPED,
@@ -204,12 +204,16 @@ def ring_attention_bwd(q, k, v, out, lse, dout, n_shards: int, layout: int = STR
                        workspace=None, stream=None):
     """Gradients (dq, dk, dv) as float32, recomputing P from the saved LSE."""
     lib = load()
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (dout, "dout")):
+        _need(t, torch.bfloat16, n)
+    for t, n in ((out, "out"), (lse, "lse")):
+        _need(t, torch.float32, n)
     b, S, h, d = q.shape
     n_kv = k.shape[2]
     dq = torch.empty((b, S, h, d), dtype=torch.float32, device=q.device) if dq is None else dq
     dk = torch.empty((b, S, n_kv, d), dtype=torch.float32, device=q.device) if dk is None else dk
     dv = torch.empty((b, S, n_kv, d), dtype=torch.float32, device=q.device) if dv is None else dv
-    ws_bytes = bwd_workspace_size(S, b, h, n_kv, d)
+    ws_bytes = bwd_workspace_size(S, n_shards, b, h, n_kv, d)
     if workspace is None:
         workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=q.device)
     _check(lib.ra_ring_attention_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout),

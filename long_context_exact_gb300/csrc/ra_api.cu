@@ -39,6 +39,17 @@ ra_status cuda_fail(cudaError_t e, const char *what) {
   return fail(RA_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
 }
 
+int sm_count() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 152;
+  }
+  return n;
+}
+
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Pointers must be non-null and 16-byte aligned (TMA and float4 access).
@@ -281,10 +292,12 @@ ra_status ra_ring_attention(const uint16_t *q, const uint16_t *k, const uint16_t
   return launch_attention(p, dims.d, q, k, v, L, L, static_cast<cudaStream_t>(stream));
 }
 
-size_t ra_bwd_workspace_size(int64_t S, ra_dims dims) {
-  if (S <= 0 || dims.b <= 0 || dims.h <= 0) return 0;
-  // D = rowsum(dO * O) and the log2-domain LSE, one float each per (b, h, row).
-  return static_cast<size_t>(2) * dims.b * dims.h * static_cast<size_t>(S) * sizeof(float);
+size_t ra_bwd_workspace_size(int64_t S, int n_shards, ra_dims dims) {
+  if (S <= 0 || n_shards < 1 || S % n_shards != 0 || dims.b <= 0 || dims.h <= 0) return 0;
+  const int64_t L = S / n_shards;
+  const int64_t Lpad = (L + kTile - 1) / kTile * kTile;
+  return static_cast<size_t>(2) * dims.b * dims.h * static_cast<size_t>(n_shards) *
+         static_cast<size_t>(Lpad) * sizeof(float);
 }
 
 ra_status ra_ring_attention_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
@@ -292,10 +305,66 @@ ra_status ra_ring_attention_bwd(const uint16_t *q, const uint16_t *k, const uint
                                 float *dq, float *dk, float *dv, void *workspace,
                                 size_t workspace_bytes, int64_t S, int n_shards, ra_layout layout,
                                 int causal, float scale, ra_dims dims, void *stream) {
-  (void)q; (void)k; (void)v; (void)out; (void)lse; (void)dout; (void)dq; (void)dk; (void)dv;
-  (void)workspace; (void)workspace_bytes; (void)S; (void)n_shards; (void)layout; (void)causal;
-  (void)scale; (void)dims; (void)stream;
-  return fail(RA_ERR_UNSUPPORTED, "backward kernel not built in this version");
+  ra_status st;
+  if ((st = check_dims(dims)) != RA_OK) return st;
+  if (layout != RA_LAYOUT_CONTIGUOUS && layout != RA_LAYOUT_STRIPED)
+    return fail(RA_ERR_INVALID_ARG, "unknown layout %d", (int)layout);
+  if (S < 0) return fail(RA_ERR_INVALID_ARG, "negative S");
+  if (n_shards < 1) return fail(RA_ERR_INVALID_ARG, "n_shards must be >= 1");
+  if (S >= (1LL << 31)) return fail(RA_ERR_UNSUPPORTED, "S must be below 2^31");
+  if (S % n_shards != 0)
+    return fail(RA_ERR_UNSUPPORTED, "S=%lld is not a multiple of n_shards=%d", (long long)S, n_shards);
+  if (S == 0 || dims.b == 0) return RA_OK;
+  RA_CHECK_PTR(q);
+  RA_CHECK_PTR(k);
+  RA_CHECK_PTR(v);
+  RA_CHECK_PTR(out);
+  RA_CHECK_PTR(lse);
+  RA_CHECK_PTR(dout);
+  RA_CHECK_PTR(dq);
+  RA_CHECK_PTR(dk);
+  RA_CHECK_PTR(dv);
+  const size_t need = ra_bwd_workspace_size(S, n_shards, dims);
+  if (workspace == nullptr || workspace_bytes < need)
+    return fail(RA_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need,
+                workspace == nullptr ? (size_t)0 : workspace_bytes);
+  if (!aligned16(workspace)) return fail(RA_ERR_INVALID_ARG, "workspace is not 16-byte aligned");
+  float sc;
+  if ((st = resolve_scale(scale, dims.d, &sc)) != RA_OK) return st;
+  const int64_t L = S / n_shards;
+  BwdParams p{};
+  p.b = dims.b;
+  p.h = dims.h;
+  p.n_kv = dims.n_kv;
+  p.g = dims.h / dims.n_kv;
+  p.N = n_shards;
+  p.L = static_cast<int>(L);
+  p.S = static_cast<int>(S);
+  p.layout = layout;
+  p.causal = causal ? 1 : 0;
+  p.scale = sc;
+  p.scale_log2 = sc * kLog2e;
+  p.n_qtiles = static_cast<int>((L + kTile - 1) / kTile);
+  p.n_ktiles = p.n_qtiles;
+  p.Lpad = p.n_qtiles * kTile;
+  const size_t rows = static_cast<size_t>(dims.b) * dims.h * n_shards * p.Lpad;
+  p.dvec = static_cast<float *>(workspace);
+  p.lse2 = p.dvec + rows;
+  p.dq = dq;
+  p.dk = dk;
+  p.dv = dv;
+  CUtensorMap qm, km, vm, dom;
+  if ((st = make_map(&qm, q, layout, dims.b, n_shards, p.L, dims.h, dims.d)) != RA_OK) return st;
+  if ((st = make_map(&km, k, layout, dims.b, n_shards, p.L, dims.n_kv, dims.d)) != RA_OK) return st;
+  if ((st = make_map(&vm, v, layout, dims.b, n_shards, p.L, dims.n_kv, dims.d)) != RA_OK) return st;
+  if ((st = make_map(&dom, dout, layout, dims.b, n_shards, p.L, dims.h, dims.d)) != RA_OK) return st;
+  const long long n_units = static_cast<long long>(dims.b) * dims.n_kv * n_shards * p.n_ktiles;
+  if (n_units > 0x7fffffffLL) return fail(RA_ERR_UNSUPPORTED, "too many work units (%lld)", n_units);
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemsetAsync(dq, 0, static_cast<size_t>(dims.b) * S * dims.h * dims.d * 4, cs);
+  if (e != cudaSuccess) return cuda_fail(e, "dq clear");
+  e = counted(launch_bwd(p, dims.d, out, lse, dout, qm, km, vm, dom, n_units, sm_count(), cs), 2);
+  return e == cudaSuccess ? RA_OK : cuda_fail(e, "backward launch");
 }
 
 ra_status ra_position_map(ra_layout layout, int64_t S, int n_shards, int32_t *shard_of,
@@ -321,9 +390,10 @@ ra_status ra_ring_order(int n_shards, int32_t *order, void *stream) {
 ra_status ra_stream_check(void *stream) {
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
-  unsigned int words[2] = {0u, 0u};
+  unsigned int words[3] = {0u, 0u, 0u};
   if ((e = read_error_word_fwd(&words[0])) != cudaSuccess) return cuda_fail(e, "error word read");
   if ((e = read_error_word_small(&words[1])) != cudaSuccess) return cuda_fail(e, "error word read");
+  if ((e = read_error_word_bwd(&words[2])) != cudaSuccess) return cuda_fail(e, "error word read");
   for (unsigned int w : words) {
     if (w != 0u)
       return fail(RA_ERR_DEVICE_TIMEOUT, "device wait ran out (code %u, site 0x%x)", w & 0xffu,

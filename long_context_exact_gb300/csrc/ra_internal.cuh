@@ -64,12 +64,32 @@ struct FwdParams {
   float *st_o;              // block: [b, Lq, h, d]
 };
 
+struct BwdParams {
+  int b, h, n_kv, g;
+  int N, L, S;              // shards, rows per shard, tokens per sequence
+  int layout, causal;
+  float scale;              // dQ, dK multiplier
+  float scale_log2;         // scale * log2(e)
+  int n_qtiles, n_ktiles;   // ceil(L / 128)
+  int Lpad;                 // n_qtiles * 128
+  float *dvec;              // [b, h, N, Lpad] rowsum(dO * O), shard-local order
+  float *lse2;              // [b, h, N, Lpad] LSE * log2(e), +inf on padding rows
+  float *dq;                // [b, S, h, d], accumulated (zeroed before the launch)
+  float *dk, *dv;           // [b, S, n_kv, d]
+};
+
 // Forward launch (ra_fwd.cu).  Tensor maps view Q/K/V as 5-D tensors whose
 // coordinates are (x, head, shard-or-row, row-or-shard, batch); see
 // make_qkv_maps() in ra_api.cu.
 cudaError_t launch_fwd(const FwdParams &p, int d, int nq, const CUtensorMap &qmap,
                        const CUtensorMap &kmap, const CUtensorMap &vmap, long long n_units,
                        cudaStream_t stream);
+
+// Backward launch (ra_bwd.cu): the D / LSE2 pre-pass, then the main kernel.
+cudaError_t launch_bwd(const BwdParams &p, int d, const float *out, const float *lse,
+                       const uint16_t *dout, const CUtensorMap &qmap, const CUtensorMap &kmap,
+                       const CUtensorMap &vmap, const CUtensorMap &domap, long long n_units,
+                       int n_sm, cudaStream_t stream);
 
 // Element-wise kernels (ra_small.cu).
 cudaError_t launch_finalize(float *o, const float *l, const float *m, float *lse, int b,
@@ -84,5 +104,6 @@ cudaError_t launch_wait_timeout_selftest(long long budget, cudaStream_t stream);
 // Read-and-clear of each translation unit's device error word.
 cudaError_t read_error_word_fwd(unsigned int *word);
 cudaError_t read_error_word_small(unsigned int *word);
+cudaError_t read_error_word_bwd(unsigned int *word);
 
 }  // namespace ra

@@ -111,9 +111,28 @@ def test_map_and_order_validation(lib):
 
 
 def test_workspace_size(lib):
-    n = lib.ra_bwd_workspace_size(65536, _dims(b=2, h=32, n_kv=8))
-    assert n >= 2 * 32 * 65536 * 4
-    assert lib.ra_bwd_workspace_size(0, _dims()) == 0
+    lib.ra_bwd_workspace_size.argtypes = [ctypes.c_int64, ctypes.c_int, binding.Dims]
+    n = lib.ra_bwd_workspace_size(65536, 16, _dims(b=2, h=32, n_kv=8))
+    assert n == 2 * 2 * 32 * 65536 * 4
+    # rows of each shard are padded to a multiple of 128
+    assert lib.ra_bwd_workspace_size(600, 3, _dims(b=1, h=4)) == 2 * 4 * 3 * 256 * 4
+    assert lib.ra_bwd_workspace_size(0, 4, _dims()) == 0
+    assert lib.ra_bwd_workspace_size(1000, 3, _dims()) == 0
+
+
+def test_bwd_validation(lib):
+    d = _dims()
+    args = [FAKE] * 9
+    assert lib.ra_ring_attention_bwd(*args, None, 0, 1024, 4, 1, 1, 0.0, d, None) == \
+        binding.RA_ERR_WORKSPACE
+    assert lib.ra_ring_attention_bwd(*args, FAKE, 16, 1024, 4, 1, 1, 0.0, d, None) == \
+        binding.RA_ERR_WORKSPACE
+    assert lib.ra_ring_attention_bwd(*args, FAKE, 1 << 30, 1024, 4, 1, 1, 0.0, _dims(d=80),
+                                     None) == binding.RA_ERR_UNSUPPORTED
+    bad = list(args)
+    bad[5] = None
+    assert lib.ra_ring_attention_bwd(*bad, FAKE, 1 << 30, 1024, 4, 1, 1, 0.0, d, None) == \
+        binding.RA_ERR_INVALID_ARG
 
 
 def test_binding_refuses_cpu_tensors(lib):

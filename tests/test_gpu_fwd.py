@@ -95,7 +95,9 @@ def test_layouts_agree_and_results_are_deterministic():
     oc, lc = ra.ring_attention(q, k, v, 8, CONTIGUOUS, True)
     os_, ls_ = ra.ring_attention(q, k, v, 8, STRIPED, True)
     ra.stream_check()
-    assert (oc - os_).abs().max().item() < 2e-3
+    # each path is within O_TOL of the exact result; P is rounded to bf16 on
+    # both, in different accumulation orders
+    assert (oc - os_).abs().max().item() < O_TOL
     assert (lc - ls_).abs().max().item() < 1e-4
     o2, l2 = ra.ring_attention(q, k, v, 8, STRIPED, True)
     assert torch.equal(o2, os_) and torch.equal(l2, ls_)
