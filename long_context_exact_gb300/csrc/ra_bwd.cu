@@ -14,15 +14,26 @@
 // query heads of its GQA group.  dQ partial tiles are added into the fp32 dq
 // output with vector reductions.
 //
+// Precision: bf16 operands with fp32 accumulation lose up to 2^-9 of each
+// product term, which on query rows with few visible keys (large weights)
+// reaches the 1e-2 parity budget.  dS is always formed from the fp32 P; on
+// steps whose query tile has a row seeing fewer than kSplitKeys keys, P and
+// dS also go to the tensor cores as a bf16 pair hi + lo (lo = the rounding
+// residual): dV += P_hi^T dO + P_lo^T dO, dK += dS_hi^T Q + dS_lo^T Q,
+// dQ = dS_hi K + dS_lo K.
+//
 // Warp roles (12 warps):
 //   warps 0-3  "softmax": thread = key row; P^T = exp2(S^T - LSE2), written to
-//              TMEM as bf16; dS^T = P^T (dP^T - D), written to shared memory
+//              TMEM as bf16 (and its residual on split steps); dS^T =
+//              P^T (dP^T - D) to shared memory (residual over the step's dO
+//              tile once dV is done with it, on split steps)
 //   warps 4-7  dQ drain: TMEM -> registers -> red.global.add.v4.f32; at the
 //              end the dK / dV epilogue
 //   warp 8     TMA producer: K, V once; Q and dO tiles into a 2-deep ring
 //   warp 9     TMEM allocator and MMA issuer (lane 0)
 //   warps 10-11 idle
-// TMEM columns: S^T/P^T [0,128), dP^T then dQ [128,256), dV [256,..), dK [384,..).
+// TMEM columns: S^T then P_hi^T [0,64) + P_lo^T [64,128); dP^T then dQ
+// [128,256); dV [256,..); dK [384,..).
 // MMAs per step: S^T = K Q^T, dP^T = V dO^T (SS, both K-major);
 // dV += P^T dO (A from TMEM, dO MN-major); dK += dS^T Q (dS^T K-major, Q
 // MN-major); dQ = dS K (dS^T read MN-major, K MN-major).
@@ -50,7 +61,11 @@ struct BwdCfg {
   static constexpr int kQOff = kVOff + kTileBytes;
   static constexpr int kDoOff = kQOff + kQSt * kTileBytes;
   static constexpr int kDsOff = kDoOff + kQSt * kTileBytes;
-  static constexpr int kBarOff = kDsOff + kDsBytes;
+  // dS_lo^T (split steps): over the step's dO tile when that is as large as
+  // a dS tile (D = 128), else a buffer of its own.
+  static constexpr bool kDsLoInDo = kTileBytes >= kDsBytes;
+  static constexpr int kDsLoOff = kDsOff + kDsBytes;
+  static constexpr int kBarOff = kDsLoOff + (kDsLoInDo ? 0 : kDsBytes);
   static constexpr int bKV = 0;
   static constexpr int bQFull = 1;
   static constexpr int bQEmpty = bQFull + kQSt;
@@ -61,13 +76,22 @@ struct BwdCfg {
   static constexpr int bDsEmpty = bDsReady + 1;
   static constexpr int bDqFull = bDsEmpty + 1;
   static constexpr int bDqEmpty = bDqFull + 1;
-  static constexpr int bDone = bDqEmpty + 1;
+  static constexpr int bDvDone = bDqEmpty + 1;
+  static constexpr int bDone = bDvDone + 1;
   static constexpr int bDrain = bDone + 1;
   static constexpr int kNumBars = bDrain + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kSmemBytes = kMiscOff + 16;
   static constexpr int kSmemAlloc = kSmemBytes + 1024;
   static constexpr int kThreads = 384;
+  // 168 registers per thread at launch = 128 x (232 softmax + 160 dQ drain
+  // + 112 producer / MMA) re-split per warpgroup.
+  static constexpr int kLaunchRegs = 168;
+  static constexpr int kSoftmaxRegs = 232;
+  static constexpr int kDrainRegs = 160;
+  static constexpr int kOtherRegs = 112;
+  static_assert(128 * (kSoftmaxRegs + kDrainRegs + kOtherRegs) == kThreads * kLaunchRegs,
+                "register re-split must use exactly the launch pool");
   static constexpr int kProducerWarp = 8;
   static constexpr int kMmaWarp = 9;
   static constexpr uint32_t kTmemCols = 512;
@@ -80,7 +104,7 @@ struct BwdCfg {
 enum : unsigned int {
   kSiteBProdKV = 0x51, kSiteBProdQ = 0x52,
   kSiteBMmaKV = 0x61, kSiteBMmaQ = 0x62, kSiteBMmaP = 0x63, kSiteBMmaDs = 0x64, kSiteBMmaDq = 0x65,
-  kSiteBSmS = 0x71, kSiteBSmDp = 0x72, kSiteBSmDs = 0x73,
+  kSiteBSmS = 0x71, kSiteBSmDp = 0x72, kSiteBSmDs = 0x73, kSiteBSmDv = 0x74,
   kSiteBDq = 0x81, kSiteBDone = 0x82,
 };
 
@@ -121,7 +145,7 @@ struct QIter {
 // tile, in ring order.  `partial` marks steps that need the causal element
 // mask.
 __device__ __forceinline__ bool q_next(const BwdParams &p, const KvUnit &x, QIter &it, int &i,
-                                       int &a, int &hq, bool &partial) {
+                                       int &a, int &hq, bool &partial, bool &split) {
   bool have = false;
   if (it.s >= 0) {
     if (++it.hh < p.g) {
@@ -152,6 +176,8 @@ __device__ __forceinline__ bool q_next(const BwdParams &p, const KvUnit &x, QIte
   a = it.a;
   hq = x.kh * p.g + it.hh;
   partial = it.a < it.a_full;
+  split = p.causal ? (token_at(p.layout, p.L, p.N, it.i, it.a * kTile) + 1 < kSplitKeys)
+                   : (p.S < kSplitKeys);
   return true;
 }
 
@@ -174,6 +200,27 @@ __device__ __forceinline__ void mma_kk(uint32_t d_tmem, uint32_t a_saddr, uint32
     const uint32_t off = (kk >> 2) * (kTile * 128) + (kk & 3) * 32;
     mma_ss(d_tmem, smem_desc_sw128(a_saddr + off, 16, 1024),
            smem_desc_sw128(b_saddr + off, 16, 1024), idesc, kk > 0 ? 1u : 0u);
+  }
+}
+
+// P^T row (fp32) to TMEM as bf16 pairs in columns [0,64); with kSplit the
+// rounding residual too, in columns [64,128).
+template <bool kSplit>
+__device__ __forceinline__ void store_p_pair(const float (&pf)[kTile], uint32_t tS) {
+#pragma unroll
+  for (int q4 = 0; q4 < 4; ++q4) {
+    uint32_t hi[16];
+    uint32_t lo[kSplit ? 16 : 1];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      const int c = q4 * 32 + 2 * e;
+      hi[e] = pack_bf16x2(pf[c], pf[c + 1]);
+      if constexpr (kSplit)
+        lo[e] = pack_bf16x2(pf[c] - __uint_as_float(hi[e] << 16),
+                            pf[c + 1] - __uint_as_float(hi[e] & 0xffff0000u));
+    }
+    tmem_st16(tS + q4 * 16, hi);
+    if constexpr (kSplit) tmem_st16(tS + 64 + q4 * 16, lo);
   }
 }
 
@@ -206,6 +253,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     mbar_init(&bars[C::bDsEmpty], 1);
     mbar_init(&bars[C::bDqFull], 1);
     mbar_init(&bars[C::bDqEmpty], 4);
+    mbar_init(&bars[C::bDvDone], 1);
     mbar_init(&bars[C::bDone], 1);
     mbar_init(&bars[C::bDrain], 1);
     *abort_flag = 0;
@@ -221,6 +269,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
   const uint32_t tmem = *tmem_holder;
   const KvUnit x = decode_kv_unit(p, blockIdx.x);
 
+  if (warp >= 8) {
+    regs_set<C::kOtherRegs, C::kLaunchRegs>();
   if (warp == C::kProducerWarp) {
     // ------------------------------------------------------------ producer
     int q_par[C::kQSt] = {-1, -1};
@@ -242,8 +292,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     }
     QIter it;
     int i, a, hq, n = 0;
-    bool partial;
-    while (q_next(p, x, it, i, a, hq, partial)) {
+    bool partial, split;
+    while (q_next(p, x, it, i, a, hq, partial, split)) {
       if (lane == 0) {
         const int st = n % C::kQSt;
         const uint32_t ph = (n / C::kQSt) & 1;
@@ -282,8 +332,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       const uint32_t ds_s = sbase + C::kDsOff;
       QIter it;
       int i, a, hq, n = 0;
-      bool partial;
-      bool has = q_next(p, x, it, i, a, hq, partial);
+      bool partial, split;
+      bool has = q_next(p, x, it, i, a, hq, partial, split);
       if (has && lane == 0) {
         if (mbar_wait(&bars[C::bQFull + 0], 0, abort_flag, kSiteBMmaQ)) {
           tc_fence_after();
@@ -293,11 +343,13 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       }
       __syncwarp();
       while (has && !*abort_flag) {
-        const bool has_next = q_next(p, x, it, i, a, hq, partial);
+        const bool cur_split = split;
+        const bool has_next = q_next(p, x, it, i, a, hq, partial, split);
         if (lane == 0) {
           const int st = n % C::kQSt;
           const uint32_t q_s = sbase + C::kQOff + st * C::kTileBytes;
           const uint32_t do_s = sbase + C::kDoOff + st * C::kTileBytes;
+          const uint32_t dslo_s = C::kDsLoInDo ? do_s : sbase + C::kDsLoOff;
           bool go = true;
           if (n > 0) go = mbar_wait(&bars[C::bDqEmpty], (n - 1) & 1, abort_flag, kSiteBMmaDq);
           if (go) {
@@ -309,12 +361,19 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
           }
           if (go) {
             tc_fence_after();
-            // dV += P^T dO: A = P^T (TMEM, bf16 pairs), B = dO MN-major
+            // dV += P_hi^T dO + P_lo^T dO: A from TMEM (bf16 pairs), B = dO MN-major
 #pragma unroll
             for (int kk = 0; kk < kTile / 16; ++kk)
               mma_ts(tmem + C::kColDv, tmem + C::kColS + kk * 8,
                      smem_desc_sw128(do_s + kk * 16 * 128, kTile * 128, 1024), C::kIdescDv,
                      (n > 0 || kk > 0) ? 1u : 0u);
+            if (cur_split)
+#pragma unroll
+              for (int kk = 0; kk < kTile / 16; ++kk)
+                mma_ts(tmem + C::kColDv, tmem + C::kColS + 64 + kk * 8,
+                       smem_desc_sw128(do_s + kk * 16 * 128, kTile * 128, 1024), C::kIdescDv,
+                       1u);
+            mma_commit(&bars[C::bDvDone]);
             if (has_next) {
               const int st1 = (n + 1) % C::kQSt;
               go = mbar_wait(&bars[C::bQFull + st1], ((n + 1) / C::kQSt) & 1, abort_flag,
@@ -337,12 +396,25 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                      smem_desc_sw128(ds_s + (kk >> 2) * (kTile * 128) + (kk & 3) * 32, 16, 1024),
                      smem_desc_sw128(q_s + kk * 16 * 128, kTile * 128, 1024), C::kIdescDv,
                      (n > 0 || kk > 0) ? 1u : 0u);
+            if (cur_split)  // dK += dS_lo^T Q
+#pragma unroll
+              for (int kk = 0; kk < kTile / 16; ++kk)
+                mma_ss(tmem + C::kColDk,
+                       smem_desc_sw128(dslo_s + (kk >> 2) * (kTile * 128) + (kk & 3) * 32, 16,
+                                       1024),
+                       smem_desc_sw128(q_s + kk * 16 * 128, kTile * 128, 1024), C::kIdescDv, 1u);
             // dQ = dS K: A = dS (queries x keys) read from dS^T MN-major, B = K MN-major
 #pragma unroll
             for (int kk = 0; kk < kTile / 16; ++kk)
               mma_ss(tmem + C::kColDp, smem_desc_sw128(ds_s + kk * 16 * 128, kTile * 128, 1024),
                      smem_desc_sw128(k_s + kk * 16 * 128, kTile * 128, 1024), C::kIdescDq,
                      kk > 0 ? 1u : 0u);
+            if (cur_split)  // dQ += dS_lo K
+#pragma unroll
+              for (int kk = 0; kk < kTile / 16; ++kk)
+                mma_ss(tmem + C::kColDp,
+                       smem_desc_sw128(dslo_s + kk * 16 * 128, kTile * 128, 1024),
+                       smem_desc_sw128(k_s + kk * 16 * 128, kTile * 128, 1024), C::kIdescDq, 1u);
             mma_commit(&bars[C::bDqFull]);
             mma_commit(&bars[C::bDsEmpty]);
             mma_commit(&bars[C::bQEmpty + st]);
@@ -359,7 +431,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       mbar_wait_budget(&bars[C::bDrain], 0, kWaitBudgetCycles);
     }
     __syncwarp();
+  }
   } else if (warp < 4) {
+    regs_set<C::kSoftmaxRegs, C::kLaunchRegs>();
     // ------------------------------------------------------------ softmax (thread = key)
     const int row = warp * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
@@ -372,8 +446,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     uint8_t *ds_row = smem + C::kDsOff + row * 128;
     QIter it;
     int i, a, hq, n = 0;
-    bool partial;
-    while (q_next(p, x, it, i, a, hq, partial)) {
+    bool partial, split;
+    while (q_next(p, x, it, i, a, hq, partial, split)) {
       const size_t qrow0 = ((static_cast<size_t>(x.bb) * p.h + hq) * p.N + i) * p.Lpad + a * kTile;
       const float4 *lse4 = reinterpret_cast<const float4 *>(p.lse2 + qrow0);
       const float4 *d4 = reinterpret_cast<const float4 *>(p.dvec + qrow0);
@@ -383,34 +457,28 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       if (!key_exists) c0 = kTile;
       if (!__all_sync(kFull, mbar_wait(&bars[C::bSFull], n & 1, abort_flag, kSiteBSmS))) break;
       tc_fence_after();
-      uint32_t pk[64];
+      float pf[kTile];  // P^T row of this key, fp32
+      {
+        uint32_t sr[kTile];
+        tmem_ld128(tS, sr);
 #pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
-        uint32_t r[32];
-        tmem_ld32(tS + ch * 32, r);
-#pragma unroll
-        for (int e4 = 0; e4 < 8; ++e4) {
-          const float4 l4 = __ldg(lse4 + ch * 8 + e4);
-          const int c = ch * 32 + e4 * 4;
-          float pv[4];
-          pv[0] = ex2(fmaf(__uint_as_float(r[e4 * 4 + 0]), sl2, -l4.x));
-          pv[1] = ex2(fmaf(__uint_as_float(r[e4 * 4 + 1]), sl2, -l4.y));
-          pv[2] = ex2(fmaf(__uint_as_float(r[e4 * 4 + 2]), sl2, -l4.z));
-          pv[3] = ex2(fmaf(__uint_as_float(r[e4 * 4 + 3]), sl2, -l4.w));
+        for (int e4 = 0; e4 < kTile / 4; ++e4) {
+          const float4 l4 = __ldg(lse4 + e4);
+          const int c = e4 * 4;
+          pf[c + 0] = ex2(fmaf(__uint_as_float(sr[c + 0]), sl2, -l4.x));
+          pf[c + 1] = ex2(fmaf(__uint_as_float(sr[c + 1]), sl2, -l4.y));
+          pf[c + 2] = ex2(fmaf(__uint_as_float(sr[c + 2]), sl2, -l4.z));
+          pf[c + 3] = ex2(fmaf(__uint_as_float(sr[c + 3]), sl2, -l4.w));
 #pragma unroll
           for (int u = 0; u < 4; ++u)
-            if (c + u < c0) pv[u] = 0.f;
-          pk[ch * 16 + e4 * 2 + 0] = pack_bf16x2(pv[0], pv[1]);
-          pk[ch * 16 + e4 * 2 + 1] = pack_bf16x2(pv[2], pv[3]);
+            if (c + u < c0) pf[c + u] = 0.f;
         }
       }
-#pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        uint32_t w16[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) w16[e] = pk[q4 * 16 + e];
-        tmem_st16(tS + q4 * 16, w16);
-      }
+      // P_hi^T to columns [0,64) (and P_lo^T to [64,128) on split steps)
+      if (split)
+        store_p_pair<true>(pf, tS);
+      else
+        store_p_pair<false>(pf, tS);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
@@ -418,34 +486,52 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
 
       bool go = mbar_wait(&bars[C::bDpFull], n & 1, abort_flag, kSiteBSmDp);
       if (go) go = mbar_wait(&bars[C::bDsEmpty], (n & 1) ^ 1, abort_flag, kSiteBSmDs);
+      // the residual goes over this step's dO tile once dV has read it
+      if (go && split && C::kDsLoInDo)
+        go = mbar_wait(&bars[C::bDvDone], n & 1, abort_flag, kSiteBSmDv);
       if (!__all_sync(kFull, go)) break;
       tc_fence_after();
+      uint8_t *dslo_row = (C::kDsLoInDo ? smem + C::kDoOff + (n % C::kQSt) * C::kTileBytes
+                                        : smem + C::kDsLoOff) +
+                          row * 128;
 #pragma unroll
       for (int ch = 0; ch < 4; ++ch) {
         uint32_t r[32];
         tmem_ld32(tDp + ch * 32, r);
-        uint32_t w[16];
+        uint32_t whi[16], wlo[16];
 #pragma unroll
         for (int e4 = 0; e4 < 8; ++e4) {
           const float4 dd = __ldg(d4 + ch * 8 + e4);
-          const uint32_t pa = pk[ch * 16 + e4 * 2 + 0];
-          const uint32_t pb = pk[ch * 16 + e4 * 2 + 1];
-          const float p0 = __uint_as_float(pa << 16), p1 = __uint_as_float(pa & 0xffff0000u);
-          const float p2 = __uint_as_float(pb << 16), p3 = __uint_as_float(pb & 0xffff0000u);
-          const float s0 = p0 * (__uint_as_float(r[e4 * 4 + 0]) - dd.x);
-          const float s1 = p1 * (__uint_as_float(r[e4 * 4 + 1]) - dd.y);
-          const float s2 = p2 * (__uint_as_float(r[e4 * 4 + 2]) - dd.z);
-          const float s3 = p3 * (__uint_as_float(r[e4 * 4 + 3]) - dd.w);
-          w[e4 * 2 + 0] = pack_bf16x2(s0, s1);
-          w[e4 * 2 + 1] = pack_bf16x2(s2, s3);
+          const int c = ch * 32 + e4 * 4;
+          const float s0 = pf[c + 0] * (__uint_as_float(r[e4 * 4 + 0]) - dd.x);
+          const float s1 = pf[c + 1] * (__uint_as_float(r[e4 * 4 + 1]) - dd.y);
+          const float s2 = pf[c + 2] * (__uint_as_float(r[e4 * 4 + 2]) - dd.z);
+          const float s3 = pf[c + 3] * (__uint_as_float(r[e4 * 4 + 3]) - dd.w);
+          const uint32_t h01 = pack_bf16x2(s0, s1);
+          const uint32_t h23 = pack_bf16x2(s2, s3);
+          whi[e4 * 2 + 0] = h01;
+          whi[e4 * 2 + 1] = h23;
+          wlo[e4 * 2 + 0] = pack_bf16x2(s0 - __uint_as_float(h01 << 16),
+                                        s1 - __uint_as_float(h01 & 0xffff0000u));
+          wlo[e4 * 2 + 1] = pack_bf16x2(s2 - __uint_as_float(h23 << 16),
+                                        s3 - __uint_as_float(h23 & 0xffff0000u));
         }
-        // 32 queries = four 16-byte chunks of this key's row, 128-byte swizzled
+        // dS_hi^T: 32 queries = four 16-byte chunks of this key's row, 128-byte swizzled
         uint8_t *half = ds_row + (ch >> 1) * (kTile * 128);
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           const int chunk = ((ch & 1) * 4 + u) ^ (row & 7);
           *reinterpret_cast<uint4 *>(half + chunk * 16) =
-              make_uint4(w[u * 4 + 0], w[u * 4 + 1], w[u * 4 + 2], w[u * 4 + 3]);
+              make_uint4(whi[u * 4 + 0], whi[u * 4 + 1], whi[u * 4 + 2], whi[u * 4 + 3]);
+        }
+        if (split) {
+          uint8_t *half_lo = dslo_row + (ch >> 1) * (kTile * 128);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int chunk = ((ch & 1) * 4 + u) ^ (row & 7);
+            *reinterpret_cast<uint4 *>(half_lo + chunk * 16) =
+                make_uint4(wlo[u * 4 + 0], wlo[u * 4 + 1], wlo[u * 4 + 2], wlo[u * 4 + 3]);
+          }
         }
       }
       fence_proxy_async_smem();
@@ -455,15 +541,16 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       ++n;
     }
   } else if (warp < 8) {
+    regs_set<C::kDrainRegs, C::kLaunchRegs>();
     // ------------------------------------------------------------ dQ drain, then dK/dV
     const int row = (warp & 3) * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tDq = tmem + lane_off + C::kColDp;
     QIter it;
     int i, a, hq, n = 0;
-    bool partial;
+    bool partial, split;
     bool aborted = false;
-    while (q_next(p, x, it, i, a, hq, partial)) {
+    while (q_next(p, x, it, i, a, hq, partial, split)) {
       if (!__all_sync(kFull, mbar_wait(&bars[C::bDqFull], n & 1, abort_flag, kSiteBDq))) {
         aborted = true;
         break;
@@ -599,6 +686,14 @@ cudaError_t launch_bwd_t(const BwdParams &p, const float *out, const float *lse,
   auto kern = bwd_kernel<D>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemAlloc);
   if (e != cudaSuccess) return e;
+  {
+    // The register increases in the kernel wait until the pool covers them.
+    cudaFuncAttributes attr;
+    e = cudaFuncGetAttributes(&attr, kern);
+    if (e != cudaSuccess) return e;
+    // The re-split assumes each warpgroup starts from exactly kLaunchRegs.
+    if (attr.numRegs != C::kLaunchRegs) return cudaErrorInvalidConfiguration;
+  }
   kern<<<dim3(static_cast<unsigned int>(n_units)), dim3(C::kThreads), C::kSmemAlloc, stream>>>(
       p, qmap, kmap, vmap, domap);
   return cudaGetLastError();

@@ -28,6 +28,10 @@
 // more than 8 (log2 units), so most tiles skip the O rescale; P stays
 // <= 2^8 and the result is unchanged because O and l share the same shift.
 // The exact running max is tracked alongside for the block-step state.
+//
+// Precision: tiles whose rows see fewer than kSplitKeys keys (and every
+// block step) store P as a bf16 pair, P_hi in columns [0,64) and the
+// rounding residual P_lo in [64,128) of S_t, and issue a second PV MMA.
 #include <climits>
 #include <cmath>
 
@@ -70,11 +74,14 @@ struct FwdCfg {
   static constexpr int kMmaWarp = kSoftmaxWarps + 1;
   // NQ = 2: three full warpgroups (the last holds the producer, the MMA
   // issuer and two idle warps) so registers can be re-split per warpgroup:
-  // 168 per thread at launch = 2 x 128 x 216 (softmax) + 128 x 72 (rest).
+  // 168 per thread at launch = 2 x 128 x 208 (softmax) + 128 x 88 (rest).
   static constexpr bool kResplit = NQ == 2;
   static constexpr int kThreads = kResplit ? 384 : (kSoftmaxWarps + 2) * 32;
-  static constexpr int kSoftmaxRegs = 216;
-  static constexpr int kOtherRegs = 72;
+  static constexpr int kLaunchRegs = 168;
+  static constexpr int kSoftmaxRegs = 208;
+  static constexpr int kOtherRegs = 88;
+  static_assert(!kResplit || 128 * (2 * kSoftmaxRegs + kOtherRegs) == kThreads * kLaunchRegs,
+                "register re-split must use exactly the launch pool");
   static constexpr uint32_t kTmemCols = NQ == 2 ? 512u : 256u;
   static constexpr uint32_t kOCol0 = NQ * 128u;
   static constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false, false);
@@ -244,6 +251,36 @@ __device__ __forceinline__ void issue_pv_mma(uint32_t tO, uint32_t tP, uint32_t 
   }
 }
 
+// P = 2^(s * c - shift) for one 128-key row: writes P (bf16 pairs) to TMEM
+// columns [0,64) -- and with kSplit the rounding residual to [64,128) --
+// and accumulates the fp32 row sum into four paired accumulators.
+template <bool kSplit>
+__device__ __forceinline__ void exp_pack_store(const float (&s)[kTile], uint64_t sl2x2,
+                                               uint64_t nbx2, uint64_t (&acc)[4], uint32_t tS) {
+#pragma unroll
+  for (int k = 0; k < 4; ++k) acc[k] = f2pack(0.f, 0.f);
+#pragma unroll
+  for (int q4 = 0; q4 < 4; ++q4) {
+    uint32_t pk[16];
+    uint32_t lo[kSplit ? 16 : 1];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      const int cc = q4 * 32 + 2 * e;
+      float x0, x1;
+      f2unpack(ffma2(f2pack(s[cc], s[cc + 1]), sl2x2, nbx2), x0, x1);
+      const float p0 = ex2(x0);
+      const float p1 = ex2(x1);
+      acc[e & 3] = fadd2(acc[e & 3], f2pack(p0, p1));
+      pk[e] = pack_bf16x2(p0, p1);
+      if constexpr (kSplit)
+        lo[e] = pack_bf16x2(p0 - __uint_as_float(pk[e] << 16),
+                            p1 - __uint_as_float(pk[e] & 0xffff0000u));
+    }
+    tmem_st16(tS + q4 * 16, pk);
+    if constexpr (kSplit) tmem_st16(tS + 64 + q4 * 16, lo);
+  }
+}
+
 template <int D, int NQ>
 __global__ void __launch_bounds__(FwdCfg<D, NQ>::kThreads, 1)
     fwd_kernel(const __grid_constant__ FwdParams p, const __grid_constant__ CUtensorMap qmap,
@@ -289,9 +326,10 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::kThreads, 1)
 
   Unit x = decode_unit(p, blockIdx.x);
   unit_qrange(p, x);
+  const bool split = p.block_mode || (p.causal ? (x.qmin + 1 < kSplitKeys) : (p.S < kSplitKeys));
 
   if (warp >= C::kSoftmaxWarps) {
-    if constexpr (C::kResplit) regs_decrease<C::kOtherRegs>();
+    if constexpr (C::kResplit) regs_set<C::kOtherRegs, C::kLaunchRegs>();
   if (warp == C::kProducerWarp) {
     // ------------------------------------------------------------ producer
     int c2, c3;
@@ -395,6 +433,9 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::kThreads, 1)
             tc_fence_after();
             issue_pv_mma<D>(tmem + C::kOCol0 + t * 128, tmem + t * 128,
                             v_saddr + vs * C::kTileBytes, C::kIdescPV, n > 0);
+            if (split)
+              issue_pv_mma<D>(tmem + C::kOCol0 + t * 128, tmem + t * 128 + 64,
+                              v_saddr + vs * C::kTileBytes, C::kIdescPV, true);
             if (t == NQ - 1) mma_commit(&bars[C::bVEmpty + vs]);
             if (has_next) {
               if (t == 0) {
@@ -424,7 +465,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::kThreads, 1)
     __syncwarp();
   }
   } else {
-    if constexpr (C::kResplit) regs_increase<C::kSoftmaxRegs>();
+    if constexpr (C::kResplit) regs_set<C::kSoftmaxRegs, C::kLaunchRegs>();
     // ------------------------------------------------------------ softmax
     const int t = warp >> 2;                // query tile of this warpgroup
     const int row = (warp & 3) * 32 + lane;  // TMEM lane == tile row
@@ -453,14 +494,11 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::kThreads, 1)
         break;
       }
       tc_fence_after();
+      uint32_t sr[kTile];
+      tmem_ld128(tS, sr);
       float s[kTile];
 #pragma unroll
-      for (int ch = 0; ch < kTile / 32; ++ch) {
-        uint32_t r[32];
-        tmem_ld32(tS + ch * 32, r);
-#pragma unroll
-        for (int e = 0; e < 32; ++e) s[ch * 32 + e] = __uint_as_float(r[e]);
-      }
+      for (int e = 0; e < kTile; ++e) s[e] = __uint_as_float(sr[e]);
       if (partial) {
         if (!p.block_mode) {
           int lim = p.Lk - 1;
@@ -478,9 +516,18 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::kThreads, 1)
           }
         }
       }
-      float mx = s[0];
+      // row max as eight short 3-input-max chains, then a small tree
+      float pm[8];
 #pragma unroll
-      for (int e = 1; e < kTile; ++e) mx = fmaxf(mx, s[e]);
+      for (int k = 0; k < 8; ++k) pm[k] = s[k];
+#pragma unroll
+      for (int e = 8; e + 16 <= kTile; e += 16)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) pm[k] = fmax3(pm[k], s[e + k], s[e + 8 + k]);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) pm[k] = fmaxf(pm[k], s[kTile - 8 + k]);
+      const float mx = fmax3(fmax3(pm[0], pm[1], pm[2]), fmax3(pm[3], pm[4], pm[5]),
+                             fmaxf(pm[6], pm[7]));
       const float mx2 = mx * sl2;
       m_max = fmaxf(m_max, mx2);
       const bool need = mx2 > m_run + kRescaleThreshold;
@@ -489,6 +536,16 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::kThreads, 1)
         alpha = ex2(m_run - mx2);  // 0 when m_run is still -inf
         m_run = mx2;
       }
+      l_sum *= alpha;
+      const float base = (m_run == -INFINITY) ? 0.f : m_run;
+      // P = 2^(s * scale * log2 e - shift): paired FMAs, four paired sums
+      const uint64_t sl2x2 = f2pack(sl2, sl2);
+      const uint64_t nbx2 = f2pack(-base, -base);
+      uint64_t acc[4];
+      if (split)
+        exp_pack_store<true>(s, sl2x2, nbx2, acc, tS);
+      else
+        exp_pack_store<false>(s, sl2x2, nbx2, acc, tS);
       if (n > 0 && __any_sync(kFull, need)) {
         // O_t row *= alpha.  The previous PV into O_t is complete: it was
         // issued before this tile's S MMA, whose commit we waited on.
@@ -501,22 +558,12 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::kThreads, 1)
           tmem_st32(tO + ch * 32, r);
         }
       }
-      l_sum *= alpha;
-      const float base = (m_run == -INFINITY) ? 0.f : m_run;
-      float rs = 0.f;
-#pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const float p0 = ex2(fmaf(s[q4 * 32 + 2 * e], sl2, -base));
-          const float p1 = ex2(fmaf(s[q4 * 32 + 2 * e + 1], sl2, -base));
-          rs += p0 + p1;
-          pk[e] = pack_bf16x2(p0, p1);
-        }
-        tmem_st16(tS + q4 * 16, pk);
-      }
-      l_sum += rs;
+      float a0, a1, a2, a3, a4, a5, a6, a7;
+      f2unpack(acc[0], a0, a1);
+      f2unpack(acc[1], a2, a3);
+      f2unpack(acc[2], a4, a5);
+      f2unpack(acc[3], a6, a7);
+      l_sum += ((a0 + a1) + (a2 + a3)) + ((a4 + a5) + (a6 + a7));
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
@@ -611,9 +658,8 @@ cudaError_t launch_fwd_t(const FwdParams &p, const CUtensorMap &qmap, const CUte
     cudaFuncAttributes attr;
     e = cudaFuncGetAttributes(&attr, kern);
     if (e != cudaSuccess) return e;
-    const long long pool = static_cast<long long>(attr.numRegs) * C::kThreads;
-    const long long want = 2LL * 128 * C::kSoftmaxRegs + 128LL * C::kOtherRegs;
-    if (pool < want) return cudaErrorInvalidConfiguration;
+    // The re-split assumes each warpgroup starts from exactly kLaunchRegs.
+    if (attr.numRegs != C::kLaunchRegs) return cudaErrorInvalidConfiguration;
   }
   kern<<<dim3(static_cast<unsigned int>(n_units)), dim3(C::kThreads), C::kSmemAlloc, stream>>>(
       p, qmap, kmap, vmap);

@@ -15,6 +15,13 @@ constexpr int kTile = 128;   // query rows per Q tile, keys per K/V tile
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
+// Rows that see fewer keys than this put large weights on single keys, so
+// their P (and dS) go to the tensor cores as a bf16 pair hi + lo instead of
+// one bf16 value: a bf16 operand keeps 8 significant bits, and on such rows
+// the dropped 2^-9 of each weight alone approaches the 1e-2 parity budget.
+// Longer rows spread the weights and keep plain bf16.
+constexpr int kSplitKeys = 4096;
+
 // ------------------------------------------------------------ placement
 // Token held at local row r of shard p.  Contiguous: shard p holds
 // [p*L, (p+1)*L).  Striped: token t lives on shard t mod N at row t div N

@@ -54,6 +54,9 @@ WORKLOADS = {
     "causal256k": Workload("long causal GQA b1 h32 kv8 d128 S262144 N8 striped", 1, 262144,
                            32, 8, 128, 8, True, (STRIPED,), 3, amplitude=0.5,
                            rows_per_head=256),
+    # profiling-size case: inputs still larger than L2, ~2 GB on the device
+    "causal32k": Workload("causal GQA fwd+bwd b1 h32 kv8 d128 S32768 N8 striped", 1, 32768, 32,
+                          8, 128, 8, True, (STRIPED,), 5, rows_per_head=128, backward=True),
     "bwd64k": Workload("causal GQA fwd+bwd b2 h32 kv8 d128 S65536 N16 striped", 2, 65536,
                        32, 8, 128, 16, True, (STRIPED,), 4, rows_per_head=128,
                        backward=True),
