@@ -152,6 +152,35 @@ ra_status ra_ring_attention_bwd(const uint16_t *q, const uint16_t *k, const uint
 /* (dq is zeroed on the stream and then accumulated; the workspace contents
  * need no initialisation and are scratch after the call.) */
 
+/* Size of the fixed scratch array behind ra_ring_attention_bwd_noalloc. */
+#define RA_BWD_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+
+/* The backward above without a caller-supplied workspace, for callers that
+ * cannot allocate device memory where they run it: inside a CUDA-graph
+ * capture (cudaMalloc cannot be captured), in plug-ins that only receive
+ * tensors from a host framework owning the allocator, or in loops that must
+ * not touch an allocator.  The pages have no counterpart to this call; it is
+ * a deployment convenience, not part of the method.
+ *   Arguments, results and error behaviour are those of
+ *   ra_ring_attention_bwd.  The scratch (D and the log2-domain LSE, see
+ *   ra_bwd_workspace_size) lives in a file-scope device array of
+ *   RA_BWD_NOALLOC_SCRATCH_BYTES (64 MiB) that every GPU loading the library
+ *   holds until the process exits; problems needing more return
+ *   RA_ERR_WORKSPACE with the sizes in ra_last_error(), e.g. b * h * S above
+ *   8M query rows when S / n_shards is a multiple of 128.
+ *   The first call on each device looks up the array's device address
+ *   (cudaGetSymbolAddress, with that device current): make that first call
+ *   outside any stream capture.  The call allocates nothing.
+ *   All calls on one device share its array: calls whose work overlaps on
+ *   that GPU (for example on two streams) race on it, so order them on one
+ *   stream or with events.  Nothing in the array needs to start at zero;
+ *   each call writes every word it later reads. */
+ra_status ra_ring_attention_bwd_noalloc(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                                        const float *out, const float *lse, const uint16_t *dout,
+                                        float *dq, float *dk, float *dv, int64_t S, int n_shards,
+                                        ra_layout layout, int causal, float scale, ra_dims dims,
+                                        void *stream);
+
 /* Token placement maps (the third page's section 6 example; "Striped
  * Attention" on the first page), computed on the device by the same functions
  * the attention kernels use:

@@ -71,6 +71,9 @@ def load(path: str | None = None):
             fn = getattr(lib, name)
             fn.argtypes = args
             fn.restype = I
+        lib.ra_ring_attention_bwd_noalloc.argtypes = [P, P, P, P, P, P, P, P, P, I64, I, I, I, F,
+                                                      Dims, P]
+        lib.ra_ring_attention_bwd_noalloc.restype = I
         lib.ra_bwd_workspace_size.argtypes = [I64, I, Dims]
         lib.ra_bwd_workspace_size.restype = ctypes.c_size_t
         lib.ra_last_error.argtypes = []
@@ -221,6 +224,25 @@ def ring_attention_bwd(q, k, v, out, lse, dout, n_shards: int, layout: int = STR
                                      workspace.numel() * workspace.element_size(), S,
                                      int(n_shards), int(layout), int(bool(causal)), float(scale),
                                      _dims(b, h, n_kv, d), _stream(stream)))
+    return dq, dk, dv
+
+
+def ring_attention_bwd_noalloc(q, k, v, out, lse, dout, n_shards: int, layout: int = STRIPED,
+                               causal: bool = True, scale: float = 0.0, dq=None, dk=None,
+                               dv=None, stream=None):
+    """The backward with the library's fixed scratch array instead of a
+    workspace (for callers that cannot allocate device memory at this point;
+    see ra_ring_attention_bwd_noalloc in include/ra.h)."""
+    lib = load()
+    b, S, h, d = q.shape
+    n_kv = k.shape[2]
+    dq = torch.empty((b, S, h, d), dtype=torch.float32, device=q.device) if dq is None else dq
+    dk = torch.empty((b, S, n_kv, d), dtype=torch.float32, device=q.device) if dk is None else dk
+    dv = torch.empty((b, S, n_kv, d), dtype=torch.float32, device=q.device) if dv is None else dv
+    _check(lib.ra_ring_attention_bwd_noalloc(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
+        _ptr(dv), S, int(n_shards), int(layout), int(bool(causal)), float(scale),
+        _dims(b, h, n_kv, d), _stream(stream)))
     return dq, dk, dv
 
 

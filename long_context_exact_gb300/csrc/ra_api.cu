@@ -162,6 +162,17 @@ ra_status launch_attention(const FwdParams &p, int d, const void *q, const void 
 }
 
 }  // namespace
+
+ra_status report_error(ra_status st, const char *fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+
 }  // namespace ra
 
 using namespace ra;

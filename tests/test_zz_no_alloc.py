@@ -1,0 +1,64 @@
+"""The allocation-free backward, ra_ring_attention_bwd_noalloc.
+
+It exists for callers that cannot allocate device memory where they run the
+backward (inside a CUDA-graph capture, in plug-ins handed tensors by a host
+framework that owns the allocator).  It must give what the workspace-taking
+ra_ring_attention_bwd gives, call after call, with its scratch in the
+library's fixed device array.  This file is collected last on purpose."""
+
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+from long_context_exact_gb300 import binding as ra
+from long_context_exact_gb300.inputs import CONTIGUOUS, STRIPED, make_inputs
+
+pytestmark = pytest.mark.gpu
+
+G_TOL = 1e-2   # the parity tolerance of the backward tests
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from long_context_exact_gb300 import build as b
+    b.build()
+    return ra.load()
+
+
+def _p(t):
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def test_noalloc_backward_matches_workspace_backward_twice(lib):
+    cases = [(1, 2048, 8, 2, 128, 4, STRIPED, True), (2, 1536, 4, 1, 128, 3, CONTIGUOUS, True)]
+    for (b, S, h, n_kv, d, N, layout, causal) in cases:   # two calls in a row
+        q, k, v, do = (t.cuda() for t in make_inputs(b, S, h, n_kv, d, seed=S + b,
+                                                      with_dout=True))
+        out, lse = ra.ring_attention(q, k, v, N, layout, causal)
+        ref = ra.ring_attention_bwd(q, k, v, out, lse, do, N, layout, causal)
+        dq = torch.full((b, S, h, d), float("nan"), device="cuda")
+        dk = torch.full((b, S, n_kv, d), float("nan"), device="cuda")
+        dv = torch.full((b, S, n_kv, d), float("nan"), device="cuda")
+        st = lib.ra_ring_attention_bwd_noalloc(
+            _p(q), _p(k), _p(v), _p(out), _p(lse), _p(do), _p(dq), _p(dk), _p(dv), S, N,
+            layout, int(causal), 0.0, ra.Dims(b, h, n_kv, d),
+            ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+        assert st == ra.RA_OK, lib.ra_last_error()
+        ra.stream_check()
+        for got, want in zip((dq, dk, dv), ref):
+            err = (got - want).abs().max().item()
+            assert np.isfinite(err) and err <= G_TOL, err
+
+
+def test_noalloc_rejects_problems_beyond_its_scratch(lib):
+    b, h, n_kv, d = 1, 32, 8, 128
+    S = 1 << 20          # needs 2 * 32 * 2^20 * 4 bytes = 256 MiB of scratch
+    fake = ctypes.c_void_p(0x10000)
+    st = lib.ra_ring_attention_bwd_noalloc(fake, fake, fake, fake, fake, fake, fake, fake, fake,
+                                           S, 8, STRIPED, 1, 0.0, ra.Dims(b, h, n_kv, d), None)
+    assert st == ra.RA_ERR_WORKSPACE
+    assert b"allocation-free" in lib.ra_last_error()
