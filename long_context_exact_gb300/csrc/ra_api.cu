@@ -139,6 +139,36 @@ ra_status make_map(CUtensorMap *map, const void *base, int layout, int b, int N,
   return RA_OK;
 }
 
+// fp32 dq [b, N*L, h, d] for the backward's bulk reductions: same 5-D view
+// as make_map, 32-column (128-byte) boxes of 32 rows, 128-byte swizzled.
+ra_status make_dq_map(CUtensorMap *map, const float *base, int layout, int b, int N, int L,
+                      int heads, int d) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return fail(RA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  const cuuint64_t tok = static_cast<cuuint64_t>(heads) * d * 4;
+  cuuint64_t dims[5] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(heads), 0, 0,
+                        static_cast<cuuint64_t>(b < 1 ? 1 : b)};
+  cuuint64_t strides[4] = {static_cast<cuuint64_t>(d) * 4, tok, 0, tok * N * L};
+  cuuint32_t box[5] = {32, 1, 1, 1, 1};
+  const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  if (layout == RA_LAYOUT_STRIPED) {
+    dims[2] = static_cast<cuuint64_t>(N);
+    dims[3] = static_cast<cuuint64_t>(L);
+    strides[2] = tok * N;
+    box[3] = 32;
+  } else {
+    dims[2] = static_cast<cuuint64_t>(L);
+    dims[3] = static_cast<cuuint64_t>(N);
+    strides[2] = tok * L;
+    box[2] = 32;
+  }
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 5, const_cast<float *>(base), dims,
+                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(RA_ERR_CUDA, "cuTensorMapEncodeTiled (dq) failed (%d)", (int)r);
+  return RA_OK;
+}
+
 ra_status launch_attention(const FwdParams &p, int d, const void *q, const void *k,
                            const void *v, long long q_rows_per_shard, long long k_rows_per_shard,
                            cudaStream_t stream) {
@@ -205,7 +235,7 @@ ra_status ra_block_step(const uint16_t *q, const uint16_t *k, const uint16_t *v,
   if (causal) {
     if (!q_pos || !k_pos) return fail(RA_ERR_INVALID_ARG, "causal block step needs q_pos and k_pos");
   }
-  float sc;
+  float sc = 0.f;
   if ((st = resolve_scale(scale, dims.d, &sc)) != RA_OK) return st;
   FwdParams p{};
   p.b = dims.b;
@@ -280,7 +310,7 @@ ra_status ra_ring_attention(const uint16_t *q, const uint16_t *k, const uint16_t
   RA_CHECK_PTR(v);
   RA_CHECK_PTR(out);
   RA_CHECK_PTR(lse);
-  float sc;
+  float sc = 0.f;
   if ((st = resolve_scale(scale, dims.d, &sc)) != RA_OK) return st;
   const long long L = S / n_shards;
   FwdParams p{};
@@ -340,7 +370,7 @@ ra_status ra_ring_attention_bwd(const uint16_t *q, const uint16_t *k, const uint
     return fail(RA_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need,
                 workspace == nullptr ? (size_t)0 : workspace_bytes);
   if (!aligned16(workspace)) return fail(RA_ERR_INVALID_ARG, "workspace is not 16-byte aligned");
-  float sc;
+  float sc = 0.f;
   if ((st = resolve_scale(scale, dims.d, &sc)) != RA_OK) return st;
   const int64_t L = S / n_shards;
   BwdParams p{};
@@ -364,17 +394,18 @@ ra_status ra_ring_attention_bwd(const uint16_t *q, const uint16_t *k, const uint
   p.dq = dq;
   p.dk = dk;
   p.dv = dv;
-  CUtensorMap qm, km, vm, dom;
+  CUtensorMap qm, km, vm, dom, dqm;
   if ((st = make_map(&qm, q, layout, dims.b, n_shards, p.L, dims.h, dims.d)) != RA_OK) return st;
   if ((st = make_map(&km, k, layout, dims.b, n_shards, p.L, dims.n_kv, dims.d)) != RA_OK) return st;
   if ((st = make_map(&vm, v, layout, dims.b, n_shards, p.L, dims.n_kv, dims.d)) != RA_OK) return st;
   if ((st = make_map(&dom, dout, layout, dims.b, n_shards, p.L, dims.h, dims.d)) != RA_OK) return st;
+  if ((st = make_dq_map(&dqm, dq, layout, dims.b, n_shards, p.L, dims.h, dims.d)) != RA_OK) return st;
   const long long n_units = static_cast<long long>(dims.b) * dims.n_kv * n_shards * p.n_ktiles;
   if (n_units > 0x7fffffffLL) return fail(RA_ERR_UNSUPPORTED, "too many work units (%lld)", n_units);
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaMemsetAsync(dq, 0, static_cast<size_t>(dims.b) * S * dims.h * dims.d * 4, cs);
   if (e != cudaSuccess) return cuda_fail(e, "dq clear");
-  e = counted(launch_bwd(p, dims.d, out, lse, dout, qm, km, vm, dom, n_units, sm_count(), cs), 2);
+  e = counted(launch_bwd(p, dims.d, out, lse, dout, qm, km, vm, dom, dqm, n_units, sm_count(), cs), 2);
   return e == cudaSuccess ? RA_OK : cuda_fail(e, "backward launch");
 }
 
@@ -406,9 +437,13 @@ ra_status ra_stream_check(void *stream) {
   if ((e = read_error_word_small(&words[1])) != cudaSuccess) return cuda_fail(e, "error word read");
   if ((e = read_error_word_bwd(&words[2])) != cudaSuccess) return cuda_fail(e, "error word read");
   for (unsigned int w : words) {
-    if (w != 0u)
-      return fail(RA_ERR_DEVICE_TIMEOUT, "device wait ran out (code %u, site 0x%x)", w & 0xffu,
+    if (w == 0u) continue;
+    if ((w & 0xffu) == 2u)
+      return fail(RA_ERR_UNSUPPORTED,
+                  "kernel refused to run: dynamic shared memory base misaligned (site 0x%x)",
                   w >> 8);
+    return fail(RA_ERR_DEVICE_TIMEOUT, "device wait ran out (code %u, site 0x%x)", w & 0xffu,
+                w >> 8);
   }
   return RA_OK;
 }

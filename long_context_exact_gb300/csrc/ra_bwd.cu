@@ -25,11 +25,13 @@
 // Warp roles (12 warps):
 //   warps 0-3  "softmax": thread = key row; P^T = exp2(S^T - LSE2), written to
 //              TMEM as bf16 (and its residual on split steps); dS^T =
-//              P^T (dP^T - D) to shared memory (residual over the step's dO
-//              tile once dV is done with it, on split steps)
-//   warps 4-7  dQ drain: TMEM -> registers -> red.global.add.v4.f32; at the
-//              end the dK / dV epilogue
-//   warp 8     TMA producer: K, V once; Q and dO tiles into a 2-deep ring
+//              P^T (dP^T - D) to shared memory (its residual to the staging
+//              buffer, on split steps)
+//   warps 4-7  dQ drain: TMEM -> registers -> staging buffer -> TMA bulk
+//              reduce-add into dq, 32 rows per warp (d = 128; vector
+//              reductions for d = 64); then the dK / dV epilogue
+//   warp 8     TMA producer: K, V once; Q tiles (with their rows' LSE2 and
+//              D) into a 2-deep ring, dO tiles into one buffer
 //   warp 9     TMEM allocator and MMA issuer (lane 0)
 //   warps 10-11 idle
 // TMEM columns: S^T then P_hi^T [0,64) + P_lo^T [64,128); dP^T then dQ
@@ -56,33 +58,41 @@ struct BwdCfg {
   static constexpr int kTileBytes = kHalves * kHalfBytes;  // 128 rows x D bf16
   static constexpr int kDsBytes = 2 * kHalfBytes;          // 128 keys x 128 queries bf16
   static constexpr int kQSt = 2;
+  static constexpr int kRowStatBytes = kTile * 4;          // one float per query row
+  // Shared memory: K, V (resident); Q ring with each stage's LSE2 and D rows;
+  // one dO tile; dS^T (hi); staging (dS_lo^T on split steps, then dQ).
   static constexpr int kKOff = 0;
   static constexpr int kVOff = kKOff + kTileBytes;
   static constexpr int kQOff = kVOff + kTileBytes;
   static constexpr int kDoOff = kQOff + kQSt * kTileBytes;
-  static constexpr int kDsOff = kDoOff + kQSt * kTileBytes;
-  // dS_lo^T (split steps): over the step's dO tile when that is as large as
-  // a dS tile (D = 128), else a buffer of its own.
-  static constexpr bool kDsLoInDo = kTileBytes >= kDsBytes;
-  static constexpr int kDsLoOff = kDsOff + kDsBytes;
-  static constexpr int kBarOff = kDsLoOff + (kDsLoInDo ? 0 : kDsBytes);
+  static constexpr int kDsOff = kDoOff + kTileBytes;
+  static constexpr int kStgOff = kDsOff + kDsBytes;
+  static constexpr int kStatOff = kStgOff + kDsBytes;
+  static constexpr int kBarOff = kStatOff + kQSt * 2 * kRowStatBytes;
   static constexpr int bKV = 0;
   static constexpr int bQFull = 1;
   static constexpr int bQEmpty = bQFull + kQSt;
-  static constexpr int bSFull = bQEmpty + kQSt;
+  static constexpr int bDoFull = bQEmpty + kQSt;
+  static constexpr int bDoEmpty = bDoFull + 1;
+  static constexpr int bSFull = bDoEmpty + 1;
   static constexpr int bDpFull = bSFull + 1;
   static constexpr int bPReady = bDpFull + 1;
   static constexpr int bDsReady = bPReady + 1;
   static constexpr int bDsEmpty = bDsReady + 1;
   static constexpr int bDqFull = bDsEmpty + 1;
   static constexpr int bDqEmpty = bDqFull + 1;
-  static constexpr int bDvDone = bDqEmpty + 1;
-  static constexpr int bDone = bDvDone + 1;
+  static constexpr int bStgEmpty = bDqEmpty + 1;
+  static constexpr int bDone = bStgEmpty + 1;
   static constexpr int bDrain = bDone + 1;
   static constexpr int kNumBars = bDrain + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kSmemBytes = kMiscOff + 16;
-  static constexpr int kSmemAlloc = kSmemBytes + 1024;
+  // Alignment slack for the 1024-byte aligned tiles: as much as the 227 KB
+  // limit leaves (the kernel checks at run time that its base needs no more).
+  static constexpr int kMaxSmem = 232448;
+  static constexpr int kSlack = kSmemBytes + 1024 <= kMaxSmem ? 1024 : kMaxSmem - kSmemBytes;
+  static_assert(kSlack >= 0, "shared memory layout too large");
+  static constexpr int kSmemAlloc = kSmemBytes + kSlack;
   static constexpr int kThreads = 384;
   // 168 registers per thread at launch = 128 x (232 softmax + 160 dQ drain
   // + 112 producer / MMA) re-split per warpgroup.
@@ -99,13 +109,21 @@ struct BwdCfg {
   static constexpr uint32_t kIdescKK = idesc_bf16_f32(128, 128, false, false);  // S^T, dP^T
   static constexpr uint32_t kIdescDv = idesc_bf16_f32(128, D, false, true);     // dV, dK
   static constexpr uint32_t kIdescDq = idesc_bf16_f32(128, D, true, true);      // dQ
+  // D = 128: each drain warp adds its 32 rows of the dQ tile into dq with TMA
+  // bulk reductions from its 8 KB of the staging buffer, 32 columns x 32 rows
+  // per box (128-byte swizzled), two boxes per round, two rounds.
+  // D = 64: vector reductions from registers.
+  static constexpr bool kDqTma = D == 128;
+  static constexpr int kDqBoxBytes = 32 * 32 * 4;
+  static constexpr int kDqWarpStgBytes = 2 * kDqBoxBytes;
 };
 
 enum : unsigned int {
   kSiteBProdKV = 0x51, kSiteBProdQ = 0x52,
   kSiteBMmaKV = 0x61, kSiteBMmaQ = 0x62, kSiteBMmaP = 0x63, kSiteBMmaDs = 0x64, kSiteBMmaDq = 0x65,
-  kSiteBSmS = 0x71, kSiteBSmDp = 0x72, kSiteBSmDs = 0x73, kSiteBSmDv = 0x74,
-  kSiteBDq = 0x81, kSiteBDone = 0x82,
+  kSiteBMmaDo = 0x66,
+  kSiteBSmS = 0x71, kSiteBSmDp = 0x72, kSiteBSmDs = 0x73, kSiteBSmStg = 0x74,
+  kSiteBDq = 0x81, kSiteBDone = 0x82, kSiteBProdDo = 0x53,
 };
 
 struct KvUnit {
@@ -228,10 +246,15 @@ template <int D>
 __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     bwd_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUtensorMap qmap,
                const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
-               const __grid_constant__ CUtensorMap domap) {
+               const __grid_constant__ CUtensorMap domap,
+               const __grid_constant__ CUtensorMap dqmap) {
   using C = BwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+  if (pad > static_cast<uint32_t>(C::kSlack)) {  // uniform: never touch smem beyond the allocation
+    if (threadIdx.x == 0) raise_error(kErrLayout, 0x5F);
+    return;
+  }
   uint8_t *smem = smem_raw + pad;
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kBarOff);
   uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + C::kMiscOff);
@@ -246,6 +269,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       mbar_init(&bars[C::bQFull + s], 1);
       mbar_init(&bars[C::bQEmpty + s], 1);
     }
+    mbar_init(&bars[C::bDoFull], 1);
+    mbar_init(&bars[C::bDoEmpty], 1);
     mbar_init(&bars[C::bSFull], 1);
     mbar_init(&bars[C::bDpFull], 1);
     mbar_init(&bars[C::bPReady], 4);
@@ -253,7 +278,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     mbar_init(&bars[C::bDsEmpty], 1);
     mbar_init(&bars[C::bDqFull], 1);
     mbar_init(&bars[C::bDqEmpty], 4);
-    mbar_init(&bars[C::bDvDone], 1);
+    mbar_init(&bars[C::bStgEmpty], 4);
     mbar_init(&bars[C::bDone], 1);
     mbar_init(&bars[C::bDrain], 1);
     *abort_flag = 0;
@@ -271,167 +296,187 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
 
   if (warp >= 8) {
     regs_set<C::kOtherRegs, C::kLaunchRegs>();
-  if (warp == C::kProducerWarp) {
-    // ------------------------------------------------------------ producer
-    int q_par[C::kQSt] = {-1, -1};
-    if (lane == 0) {
-      prefetch_tmap(&qmap);
-      prefetch_tmap(&kmap);
-      prefetch_tmap(&vmap);
-      prefetch_tmap(&domap);
-      int c2, c3;
-      shard_coords_b(p.layout, x.j, x.c * kTile, c2, c3);
-      mbar_arrive_expect_tx(&bars[C::bKV], 2 * C::kTileBytes);
-#pragma unroll
-      for (int hf = 0; hf < C::kHalves; ++hf) {
-        tma_load_5d(smem + C::kKOff + hf * C::kHalfBytes, &kmap, &bars[C::bKV], hf * 64, x.kh, c2,
-                    c3, x.bb);
-        tma_load_5d(smem + C::kVOff + hf * C::kHalfBytes, &vmap, &bars[C::bKV], hf * 64, x.kh, c2,
-                    c3, x.bb);
-      }
-    }
-    QIter it;
-    int i, a, hq, n = 0;
-    bool partial, split;
-    while (q_next(p, x, it, i, a, hq, partial, split)) {
+    if (warp == C::kProducerWarp) {
+      // ---------------------------------------------------------- producer
+      int q_par[C::kQSt] = {-1, -1};
+      int do_par = -1;
       if (lane == 0) {
-        const int st = n % C::kQSt;
-        const uint32_t ph = (n / C::kQSt) & 1;
-        if (mbar_wait(&bars[C::bQEmpty + st], ph ^ 1, abort_flag, kSiteBProdQ)) {
-          int c2, c3;
-          shard_coords_b(p.layout, i, a * kTile, c2, c3);
-          mbar_arrive_expect_tx(&bars[C::bQFull + st], 2 * C::kTileBytes);
+        prefetch_tmap(&qmap);
+        prefetch_tmap(&kmap);
+        prefetch_tmap(&vmap);
+        prefetch_tmap(&domap);
+        int c2, c3;
+        shard_coords_b(p.layout, x.j, x.c * kTile, c2, c3);
+        mbar_arrive_expect_tx(&bars[C::bKV], 2 * C::kTileBytes);
 #pragma unroll
-          for (int hf = 0; hf < C::kHalves; ++hf) {
-            tma_load_5d(smem + C::kQOff + st * C::kTileBytes + hf * C::kHalfBytes, &qmap,
-                        &bars[C::bQFull + st], hf * 64, hq, c2, c3, x.bb);
-            tma_load_5d(smem + C::kDoOff + st * C::kTileBytes + hf * C::kHalfBytes, &domap,
-                        &bars[C::bQFull + st], hf * 64, hq, c2, c3, x.bb);
-          }
-          q_par[st] = static_cast<int>(ph);
+        for (int hf = 0; hf < C::kHalves; ++hf) {
+          tma_load_5d(smem + C::kKOff + hf * C::kHalfBytes, &kmap, &bars[C::bKV], hf * 64, x.kh,
+                      c2, c3, x.bb);
+          tma_load_5d(smem + C::kVOff + hf * C::kHalfBytes, &vmap, &bars[C::bKV], hf * 64, x.kh,
+                      c2, c3, x.bb);
         }
       }
-      __syncwarp();
-      if (*abort_flag) break;
-      ++n;
-    }
-    if (lane == 0 && *abort_flag) {
-      mbar_wait_budget(&bars[C::bKV], 0, kWaitBudgetCycles);
-      for (int s = 0; s < C::kQSt; ++s)
-        if (q_par[s] >= 0) mbar_wait_budget(&bars[C::bQFull + s], q_par[s], kWaitBudgetCycles);
-    }
-  } else if (warp == C::kMmaWarp) {
-    // ------------------------------------------------------------ MMA issuer
-    bool ok = true;
-    if (lane == 0) ok = mbar_wait(&bars[C::bKV], 0, abort_flag, kSiteBMmaKV);
-    ok = __shfl_sync(kFull, ok ? 1 : 0, 0) != 0;
-    if (ok) {
-      tc_fence_after();
-      const uint32_t k_s = sbase + C::kKOff;
-      const uint32_t v_s = sbase + C::kVOff;
-      const uint32_t ds_s = sbase + C::kDsOff;
       QIter it;
       int i, a, hq, n = 0;
       bool partial, split;
-      bool has = q_next(p, x, it, i, a, hq, partial, split);
-      if (has && lane == 0) {
-        if (mbar_wait(&bars[C::bQFull + 0], 0, abort_flag, kSiteBMmaQ)) {
-          tc_fence_after();
-          mma_kk<D>(tmem + C::kColS, k_s, sbase + C::kQOff, C::kIdescKK);
-          mma_commit(&bars[C::bSFull]);
-        }
-      }
-      __syncwarp();
-      while (has && !*abort_flag) {
-        const bool cur_split = split;
-        const bool has_next = q_next(p, x, it, i, a, hq, partial, split);
+      while (q_next(p, x, it, i, a, hq, partial, split)) {
         if (lane == 0) {
+          int c2, c3;
+          shard_coords_b(p.layout, i, a * kTile, c2, c3);
           const int st = n % C::kQSt;
-          const uint32_t q_s = sbase + C::kQOff + st * C::kTileBytes;
-          const uint32_t do_s = sbase + C::kDoOff + st * C::kTileBytes;
-          const uint32_t dslo_s = C::kDsLoInDo ? do_s : sbase + C::kDsLoOff;
-          bool go = true;
-          if (n > 0) go = mbar_wait(&bars[C::bDqEmpty], (n - 1) & 1, abort_flag, kSiteBMmaDq);
+          const uint32_t ph = (n / C::kQSt) & 1;
+          bool go = mbar_wait(&bars[C::bQEmpty + st], ph ^ 1, abort_flag, kSiteBProdQ);
           if (go) {
-            tc_fence_after();
-            // dP^T = V dO^T
-            mma_kk<D>(tmem + C::kColDp, v_s, do_s, C::kIdescKK);
-            mma_commit(&bars[C::bDpFull]);
-            go = mbar_wait(&bars[C::bPReady], n & 1, abort_flag, kSiteBMmaP);
+            mbar_arrive_expect_tx(&bars[C::bQFull + st], C::kTileBytes + 2 * C::kRowStatBytes);
+#pragma unroll
+            for (int hf = 0; hf < C::kHalves; ++hf)
+              tma_load_5d(smem + C::kQOff + st * C::kTileBytes + hf * C::kHalfBytes, &qmap,
+                          &bars[C::bQFull + st], hf * 64, hq, c2, c3, x.bb);
+            const size_t qrow0 =
+                ((static_cast<size_t>(x.bb) * p.h + hq) * p.N + i) * p.Lpad + a * kTile;
+            uint8_t *stat = smem + C::kStatOff + st * 2 * C::kRowStatBytes;
+            bulk_copy_g2s(stat, p.lse2 + qrow0, C::kRowStatBytes, &bars[C::bQFull + st]);
+            bulk_copy_g2s(stat + C::kRowStatBytes, p.dvec + qrow0, C::kRowStatBytes,
+                          &bars[C::bQFull + st]);
+            q_par[st] = static_cast<int>(ph);
+            go = mbar_wait(&bars[C::bDoEmpty], (n & 1) ^ 1, abort_flag, kSiteBProdDo);
           }
           if (go) {
-            tc_fence_after();
-            // dV += P_hi^T dO + P_lo^T dO: A from TMEM (bf16 pairs), B = dO MN-major
+            mbar_arrive_expect_tx(&bars[C::bDoFull], C::kTileBytes);
 #pragma unroll
-            for (int kk = 0; kk < kTile / 16; ++kk)
-              mma_ts(tmem + C::kColDv, tmem + C::kColS + kk * 8,
-                     smem_desc_sw128(do_s + kk * 16 * 128, kTile * 128, 1024), C::kIdescDv,
-                     (n > 0 || kk > 0) ? 1u : 0u);
-            if (cur_split)
-#pragma unroll
-              for (int kk = 0; kk < kTile / 16; ++kk)
-                mma_ts(tmem + C::kColDv, tmem + C::kColS + 64 + kk * 8,
-                       smem_desc_sw128(do_s + kk * 16 * 128, kTile * 128, 1024), C::kIdescDv,
-                       1u);
-            mma_commit(&bars[C::bDvDone]);
-            if (has_next) {
-              const int st1 = (n + 1) % C::kQSt;
-              go = mbar_wait(&bars[C::bQFull + st1], ((n + 1) / C::kQSt) & 1, abort_flag,
-                             kSiteBMmaQ);
-              if (go) {
-                tc_fence_after();
-                mma_kk<D>(tmem + C::kColS, k_s, sbase + C::kQOff + st1 * C::kTileBytes,
-                          C::kIdescKK);
-                mma_commit(&bars[C::bSFull]);
-              }
-            }
-          }
-          if (go) go = mbar_wait(&bars[C::bDsReady], n & 1, abort_flag, kSiteBMmaDs);
-          if (go) {
-            tc_fence_after();
-            // dK += dS^T Q: A = dS^T (keys x queries, K-major), B = Q MN-major
-#pragma unroll
-            for (int kk = 0; kk < kTile / 16; ++kk)
-              mma_ss(tmem + C::kColDk,
-                     smem_desc_sw128(ds_s + (kk >> 2) * (kTile * 128) + (kk & 3) * 32, 16, 1024),
-                     smem_desc_sw128(q_s + kk * 16 * 128, kTile * 128, 1024), C::kIdescDv,
-                     (n > 0 || kk > 0) ? 1u : 0u);
-            if (cur_split)  // dK += dS_lo^T Q
-#pragma unroll
-              for (int kk = 0; kk < kTile / 16; ++kk)
-                mma_ss(tmem + C::kColDk,
-                       smem_desc_sw128(dslo_s + (kk >> 2) * (kTile * 128) + (kk & 3) * 32, 16,
-                                       1024),
-                       smem_desc_sw128(q_s + kk * 16 * 128, kTile * 128, 1024), C::kIdescDv, 1u);
-            // dQ = dS K: A = dS (queries x keys) read from dS^T MN-major, B = K MN-major
-#pragma unroll
-            for (int kk = 0; kk < kTile / 16; ++kk)
-              mma_ss(tmem + C::kColDp, smem_desc_sw128(ds_s + kk * 16 * 128, kTile * 128, 1024),
-                     smem_desc_sw128(k_s + kk * 16 * 128, kTile * 128, 1024), C::kIdescDq,
-                     kk > 0 ? 1u : 0u);
-            if (cur_split)  // dQ += dS_lo K
-#pragma unroll
-              for (int kk = 0; kk < kTile / 16; ++kk)
-                mma_ss(tmem + C::kColDp,
-                       smem_desc_sw128(dslo_s + kk * 16 * 128, kTile * 128, 1024),
-                       smem_desc_sw128(k_s + kk * 16 * 128, kTile * 128, 1024), C::kIdescDq, 1u);
-            mma_commit(&bars[C::bDqFull]);
-            mma_commit(&bars[C::bDsEmpty]);
-            mma_commit(&bars[C::bQEmpty + st]);
+            for (int hf = 0; hf < C::kHalves; ++hf)
+              tma_load_5d(smem + C::kDoOff + hf * C::kHalfBytes, &domap, &bars[C::bDoFull],
+                          hf * 64, hq, c2, c3, x.bb);
+            do_par = n & 1;
           }
         }
         __syncwarp();
+        if (*abort_flag) break;
         ++n;
-        has = has_next;
       }
-      if (lane == 0) mma_commit(&bars[C::bDone]);
+      if (lane == 0 && *abort_flag) {
+        // Let every copy this warp started land before the CTA unwinds.
+        mbar_wait_budget(&bars[C::bKV], 0, kWaitBudgetCycles);
+        for (int s = 0; s < C::kQSt; ++s)
+          if (q_par[s] >= 0) mbar_wait_budget(&bars[C::bQFull + s], q_par[s], kWaitBudgetCycles);
+        if (do_par >= 0) mbar_wait_budget(&bars[C::bDoFull], do_par, kWaitBudgetCycles);
+      }
+    } else if (warp == C::kMmaWarp) {
+      // ---------------------------------------------------------- MMA issuer
+      bool ok = true;
+      if (lane == 0) ok = mbar_wait(&bars[C::bKV], 0, abort_flag, kSiteBMmaKV);
+      ok = __shfl_sync(kFull, ok ? 1 : 0, 0) != 0;
+      if (ok) {
+        tc_fence_after();
+        const uint32_t k_s = sbase + C::kKOff;
+        const uint32_t v_s = sbase + C::kVOff;
+        const uint32_t do_s = sbase + C::kDoOff;
+        const uint32_t ds_s = sbase + C::kDsOff;
+        const uint32_t dslo_s = sbase + C::kStgOff;
+        QIter it;
+        int i, a, hq, n = 0;
+        bool partial, split;
+        bool has = q_next(p, x, it, i, a, hq, partial, split);
+        if (has && lane == 0) {
+          if (mbar_wait(&bars[C::bQFull + 0], 0, abort_flag, kSiteBMmaQ)) {
+            tc_fence_after();
+            mma_kk<D>(tmem + C::kColS, k_s, sbase + C::kQOff, C::kIdescKK);
+            mma_commit(&bars[C::bSFull]);
+          }
+        }
+        __syncwarp();
+        while (has && !*abort_flag) {
+          const bool cur_split = split;
+          const bool has_next = q_next(p, x, it, i, a, hq, partial, split);
+          if (lane == 0) {
+            const int st = n % C::kQSt;
+            const uint32_t q_s = sbase + C::kQOff + st * C::kTileBytes;
+            bool go = true;
+            if (n > 0) go = mbar_wait(&bars[C::bDqEmpty], (n - 1) & 1, abort_flag, kSiteBMmaDq);
+            if (go) go = mbar_wait(&bars[C::bDoFull], n & 1, abort_flag, kSiteBMmaDo);
+            if (go) {
+              tc_fence_after();
+              // dP^T = V dO^T
+              mma_kk<D>(tmem + C::kColDp, v_s, do_s, C::kIdescKK);
+              mma_commit(&bars[C::bDpFull]);
+              go = mbar_wait(&bars[C::bPReady], n & 1, abort_flag, kSiteBMmaP);
+            }
+            if (go) {
+              tc_fence_after();
+              // dV += P_hi^T dO (+ P_lo^T dO): A from TMEM (bf16 pairs), B = dO MN-major
+#pragma unroll
+              for (int kk = 0; kk < kTile / 16; ++kk)
+                mma_ts(tmem + C::kColDv, tmem + C::kColS + kk * 8,
+                       smem_desc_sw128(do_s + kk * 16 * 128, kTile * 128, 1024), C::kIdescDv,
+                       (n > 0 || kk > 0) ? 1u : 0u);
+              if (cur_split)
+#pragma unroll
+                for (int kk = 0; kk < kTile / 16; ++kk)
+                  mma_ts(tmem + C::kColDv, tmem + C::kColS + 64 + kk * 8,
+                         smem_desc_sw128(do_s + kk * 16 * 128, kTile * 128, 1024), C::kIdescDv,
+                         1u);
+              mma_commit(&bars[C::bDoEmpty]);
+              if (has_next) {
+                const int st1 = (n + 1) % C::kQSt;
+                go = mbar_wait(&bars[C::bQFull + st1], ((n + 1) / C::kQSt) & 1, abort_flag,
+                               kSiteBMmaQ);
+                if (go) {
+                  tc_fence_after();
+                  mma_kk<D>(tmem + C::kColS, k_s, sbase + C::kQOff + st1 * C::kTileBytes,
+                            C::kIdescKK);
+                  mma_commit(&bars[C::bSFull]);
+                }
+              }
+            }
+            if (go) go = mbar_wait(&bars[C::bDsReady], n & 1, abort_flag, kSiteBMmaDs);
+            if (go) {
+              tc_fence_after();
+              // dK += dS^T Q: A = dS^T (keys x queries, K-major), B = Q MN-major
+#pragma unroll
+              for (int kk = 0; kk < kTile / 16; ++kk)
+                mma_ss(tmem + C::kColDk,
+                       smem_desc_sw128(ds_s + (kk >> 2) * (kTile * 128) + (kk & 3) * 32, 16, 1024),
+                       smem_desc_sw128(q_s + kk * 16 * 128, kTile * 128, 1024), C::kIdescDv,
+                       (n > 0 || kk > 0) ? 1u : 0u);
+              if (cur_split)  // dK += dS_lo^T Q
+#pragma unroll
+                for (int kk = 0; kk < kTile / 16; ++kk)
+                  mma_ss(tmem + C::kColDk,
+                         smem_desc_sw128(dslo_s + (kk >> 2) * (kTile * 128) + (kk & 3) * 32, 16,
+                                         1024),
+                         smem_desc_sw128(q_s + kk * 16 * 128, kTile * 128, 1024), C::kIdescDv,
+                         1u);
+              // dQ = dS K: A = dS (queries x keys) read from dS^T MN-major, B = K MN-major
+#pragma unroll
+              for (int kk = 0; kk < kTile / 16; ++kk)
+                mma_ss(tmem + C::kColDp, smem_desc_sw128(ds_s + kk * 16 * 128, kTile * 128, 1024),
+                       smem_desc_sw128(k_s + kk * 16 * 128, kTile * 128, 1024), C::kIdescDq,
+                       kk > 0 ? 1u : 0u);
+              if (cur_split)  // dQ += dS_lo K
+#pragma unroll
+                for (int kk = 0; kk < kTile / 16; ++kk)
+                  mma_ss(tmem + C::kColDp,
+                         smem_desc_sw128(dslo_s + kk * 16 * 128, kTile * 128, 1024),
+                         smem_desc_sw128(k_s + kk * 16 * 128, kTile * 128, 1024), C::kIdescDq,
+                         1u);
+              mma_commit(&bars[C::bDqFull]);
+              mma_commit(&bars[C::bDsEmpty]);
+              mma_commit(&bars[C::bQEmpty + st]);
+            }
+          }
+          __syncwarp();
+          ++n;
+          has = has_next;
+        }
+        if (lane == 0) mma_commit(&bars[C::bDone]);
+      }
+      if (lane == 0) {
+        // Every MMA this thread issued has finished before TMEM is released.
+        mma_commit(&bars[C::bDrain]);
+        mbar_wait_budget(&bars[C::bDrain], 0, kWaitBudgetCycles);
+      }
+      __syncwarp();
     }
-    if (lane == 0) {
-      mma_commit(&bars[C::bDrain]);
-      mbar_wait_budget(&bars[C::bDrain], 0, kWaitBudgetCycles);
-    }
-    __syncwarp();
-  }
   } else if (warp < 4) {
     regs_set<C::kSoftmaxRegs, C::kLaunchRegs>();
     // ------------------------------------------------------------ softmax (thread = key)
@@ -444,35 +489,57 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     const int kp = token_at(p.layout, p.L, p.N, x.j, key_exists ? kr : p.L - 1);
     const float sl2 = p.scale_log2;
     uint8_t *ds_row = smem + C::kDsOff + row * 128;
+    uint8_t *dslo_row = smem + C::kStgOff + row * 128;
     QIter it;
     int i, a, hq, n = 0;
     bool partial, split;
     while (q_next(p, x, it, i, a, hq, partial, split)) {
-      const size_t qrow0 = ((static_cast<size_t>(x.bb) * p.h + hq) * p.N + i) * p.Lpad + a * kTile;
-      const float4 *lse4 = reinterpret_cast<const float4 *>(p.lse2 + qrow0);
-      const float4 *d4 = reinterpret_cast<const float4 *>(p.dvec + qrow0);
+      // this step's LSE2 and D rows, staged by the producer with the Q tile
+      const float4 *lse4 = reinterpret_cast<const float4 *>(
+          smem + C::kStatOff + (n % C::kQSt) * 2 * C::kRowStatBytes);
+      const float4 *d4 = lse4 + kTile / 4;
       // query columns c < c0 are masked for this key
       int c0 = 0;
       if (partial) c0 = first_row_at_or_after(p, i, kp) - a * kTile;
-      if (!key_exists) c0 = kTile;
+      if (!key_exists) {
+        c0 = kTile;
+        partial = true;
+      }
       if (!__all_sync(kFull, mbar_wait(&bars[C::bSFull], n & 1, abort_flag, kSiteBSmS))) break;
       tc_fence_after();
       float pf[kTile];  // P^T row of this key, fp32
       {
         uint32_t sr[kTile];
         tmem_ld128(tS, sr);
+        // LSE2 of 32 query columns at a time, the next group's loads in
+        // flight while the current group is exponentiated
+        float4 lc[8], ln[8];
 #pragma unroll
-        for (int e4 = 0; e4 < kTile / 4; ++e4) {
-          const float4 l4 = __ldg(lse4 + e4);
-          const int c = e4 * 4;
-          pf[c + 0] = ex2(fmaf(__uint_as_float(sr[c + 0]), sl2, -l4.x));
-          pf[c + 1] = ex2(fmaf(__uint_as_float(sr[c + 1]), sl2, -l4.y));
-          pf[c + 2] = ex2(fmaf(__uint_as_float(sr[c + 2]), sl2, -l4.z));
-          pf[c + 3] = ex2(fmaf(__uint_as_float(sr[c + 3]), sl2, -l4.w));
+        for (int e = 0; e < 8; ++e) lc[e] = lse4[e];
 #pragma unroll
-          for (int u = 0; u < 4; ++u)
-            if (c + u < c0) pf[c + u] = 0.f;
+        for (int ch = 0; ch < 4; ++ch) {
+          if (ch < 3) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) ln[e] = lse4[(ch + 1) * 8 + e];
+          }
+#pragma unroll
+          for (int e4 = 0; e4 < 8; ++e4) {
+            const int c = ch * 32 + e4 * 4;
+            pf[c + 0] = ex2(fmaf(__uint_as_float(sr[c + 0]), sl2, -lc[e4].x));
+            pf[c + 1] = ex2(fmaf(__uint_as_float(sr[c + 1]), sl2, -lc[e4].y));
+            pf[c + 2] = ex2(fmaf(__uint_as_float(sr[c + 2]), sl2, -lc[e4].z));
+            pf[c + 3] = ex2(fmaf(__uint_as_float(sr[c + 3]), sl2, -lc[e4].w));
+          }
+          if (ch < 3) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) lc[e] = ln[e];
+          }
         }
+      }
+      if (partial) {  // causal diagonal: columns before c0 do not see this key
+#pragma unroll
+        for (int c = 0; c < kTile; ++c)
+          if (c < c0) pf[c] = 0.f;
       }
       // P_hi^T to columns [0,64) (and P_lo^T to [64,128) on split steps)
       if (split)
@@ -486,37 +553,37 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
 
       bool go = mbar_wait(&bars[C::bDpFull], n & 1, abort_flag, kSiteBSmDp);
       if (go) go = mbar_wait(&bars[C::bDsEmpty], (n & 1) ^ 1, abort_flag, kSiteBSmDs);
-      // the residual goes over this step's dO tile once dV has read it
-      if (go && split && C::kDsLoInDo)
-        go = mbar_wait(&bars[C::bDvDone], n & 1, abort_flag, kSiteBSmDv);
+      // the residual goes to the staging buffer once the drain is done with it
+      if (C::kDqTma && go && split && n > 0)
+        go = mbar_wait(&bars[C::bStgEmpty], (n - 1) & 1, abort_flag, kSiteBSmStg);
       if (!__all_sync(kFull, go)) break;
       tc_fence_after();
-      uint8_t *dslo_row = (C::kDsLoInDo ? smem + C::kDoOff + (n % C::kQSt) * C::kTileBytes
-                                        : smem + C::kDsLoOff) +
-                          row * 128;
+      uint32_t rc[32], rn[32];
+      float4 dc[8], dn[8];
+      tmem_ld32_start(tDp, rc);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) dc[e] = d4[e];
+      tmem_ld_wait_regs(rc);
 #pragma unroll
       for (int ch = 0; ch < 4; ++ch) {
-        uint32_t r[32];
-        tmem_ld32(tDp + ch * 32, r);
+        if (ch < 3) {  // next 32 columns of dP^T and D in flight
+          tmem_ld32_start(tDp + (ch + 1) * 32, rn);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) dn[e] = d4[(ch + 1) * 8 + e];
+        }
         uint32_t whi[16], wlo[16];
+        float sv[32];
 #pragma unroll
         for (int e4 = 0; e4 < 8; ++e4) {
-          const float4 dd = __ldg(d4 + ch * 8 + e4);
           const int c = ch * 32 + e4 * 4;
-          const float s0 = pf[c + 0] * (__uint_as_float(r[e4 * 4 + 0]) - dd.x);
-          const float s1 = pf[c + 1] * (__uint_as_float(r[e4 * 4 + 1]) - dd.y);
-          const float s2 = pf[c + 2] * (__uint_as_float(r[e4 * 4 + 2]) - dd.z);
-          const float s3 = pf[c + 3] * (__uint_as_float(r[e4 * 4 + 3]) - dd.w);
-          const uint32_t h01 = pack_bf16x2(s0, s1);
-          const uint32_t h23 = pack_bf16x2(s2, s3);
-          whi[e4 * 2 + 0] = h01;
-          whi[e4 * 2 + 1] = h23;
-          wlo[e4 * 2 + 0] = pack_bf16x2(s0 - __uint_as_float(h01 << 16),
-                                        s1 - __uint_as_float(h01 & 0xffff0000u));
-          wlo[e4 * 2 + 1] = pack_bf16x2(s2 - __uint_as_float(h23 << 16),
-                                        s3 - __uint_as_float(h23 & 0xffff0000u));
+          sv[e4 * 4 + 0] = pf[c + 0] * (__uint_as_float(rc[e4 * 4 + 0]) - dc[e4].x);
+          sv[e4 * 4 + 1] = pf[c + 1] * (__uint_as_float(rc[e4 * 4 + 1]) - dc[e4].y);
+          sv[e4 * 4 + 2] = pf[c + 2] * (__uint_as_float(rc[e4 * 4 + 2]) - dc[e4].z);
+          sv[e4 * 4 + 3] = pf[c + 3] * (__uint_as_float(rc[e4 * 4 + 3]) - dc[e4].w);
         }
-        // dS_hi^T: 32 queries = four 16-byte chunks of this key's row, 128-byte swizzled
+#pragma unroll
+        for (int e = 0; e < 16; ++e) whi[e] = pack_bf16x2(sv[2 * e], sv[2 * e + 1]);
+        // 32 queries = four 16-byte chunks of this key's row, 128-byte swizzled
         uint8_t *half = ds_row + (ch >> 1) * (kTile * 128);
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
@@ -525,6 +592,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
               make_uint4(whi[u * 4 + 0], whi[u * 4 + 1], whi[u * 4 + 2], whi[u * 4 + 3]);
         }
         if (split) {
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            wlo[e] = pack_bf16x2(sv[2 * e] - __uint_as_float(whi[e] << 16),
+                                 sv[2 * e + 1] - __uint_as_float(whi[e] & 0xffff0000u));
           uint8_t *half_lo = dslo_row + (ch >> 1) * (kTile * 128);
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
@@ -533,6 +604,13 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                 make_uint4(wlo[u * 4 + 0], wlo[u * 4 + 1], wlo[u * 4 + 2], wlo[u * 4 + 3]);
           }
         }
+        if (ch < 3) {
+          tmem_ld_wait_regs(rn);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) rc[e] = rn[e];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) dc[e] = dn[e];
+        }
       }
       fence_proxy_async_smem();
       tc_fence_before();
@@ -540,12 +618,13 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       if (lane == 0) mbar_arrive(&bars[C::bDsReady]);
       ++n;
     }
-  } else if (warp < 8) {
+  } else {
     regs_set<C::kDrainRegs, C::kLaunchRegs>();
     // ------------------------------------------------------------ dQ drain, then dK/dV
     const int row = (warp & 3) * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tDq = tmem + lane_off + C::kColDp;
+    uint8_t *stg = smem + C::kStgOff + (warp & 3) * C::kDqWarpStgBytes;  // this warp's 32 rows
     QIter it;
     int i, a, hq, n = 0;
     bool partial, split;
@@ -556,34 +635,67 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         break;
       }
       tc_fence_after();
-      const int qr = a * kTile + row;
-      const bool exists = qr < p.L;
-      float *dst = p.dq + ((static_cast<size_t>(x.bb) * p.S +
-                            token_at(p.layout, p.L, p.N, i, exists ? qr : 0)) *
-                               p.h +
-                           hq) *
-                              D;
       uint32_t r[D / 32][32];
 #pragma unroll
       for (int ch = 0; ch < D / 32; ++ch) tmem_ld32(tDq + ch * 32, r[ch]);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[C::bDqEmpty]);
-      if (exists) {
+      if constexpr (C::kDqTma) {
+        // Two rounds of two 32 x 32 boxes through this warp's staging slice;
+        // the staging buffer is free: this step's dS_lo^T readers finished
+        // before dQ was committed, and the previous round's read completed.
+        int c2, c3;
+        shard_coords_b(p.layout, i, a * kTile + (warp & 3) * 32, c2, c3);
 #pragma unroll
-        for (int ch = 0; ch < D / 32; ++ch)
+        for (int round = 0; round < 2; ++round) {
 #pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            float *ptr = dst + ch * 32 + u * 4;
-            asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(ptr),
-                         "f"(__uint_as_float(r[ch][u * 4 + 0]) * p.scale),
-                         "f"(__uint_as_float(r[ch][u * 4 + 1]) * p.scale),
-                         "f"(__uint_as_float(r[ch][u * 4 + 2]) * p.scale),
-                         "f"(__uint_as_float(r[ch][u * 4 + 3]) * p.scale)
-                         : "memory");
+          for (int bx = 0; bx < 2; ++bx) {
+            const int ch = round * 2 + bx;
+            uint8_t *rowp = stg + bx * C::kDqBoxBytes + lane * 128;
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+              *reinterpret_cast<float4 *>(rowp + ((u ^ (lane & 7)) * 16)) =
+                  make_float4(__uint_as_float(r[ch][4 * u + 0]) * p.scale,
+                              __uint_as_float(r[ch][4 * u + 1]) * p.scale,
+                              __uint_as_float(r[ch][4 * u + 2]) * p.scale,
+                              __uint_as_float(r[ch][4 * u + 3]) * p.scale);
           }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+#pragma unroll
+            for (int bx = 0; bx < 2; ++bx)
+              tma_reduce_add_5d(&dqmap, stg + bx * C::kDqBoxBytes, (round * 2 + bx) * 32, hq, c2,
+                                c3, x.bb);
+            bulk_commit_group();
+            bulk_wait_group0<true>();  // staging read: reusable
+          }
+          __syncwarp();
+        }
+        if (lane == 0) mbar_arrive(&bars[C::bStgEmpty]);
+      } else {
+        const int qr = a * kTile + row;
+        if (qr < p.L) {
+          float *dst = p.dq + ((static_cast<size_t>(x.bb) * p.S + token_at(p.layout, p.L, p.N, i, qr)) *
+                                   p.h + hq) * D;
+#pragma unroll
+          for (int ch = 0; ch < D / 32; ++ch)
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+              asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(
+                               dst + ch * 32 + u * 4),
+                           "f"(__uint_as_float(r[ch][u * 4 + 0]) * p.scale),
+                           "f"(__uint_as_float(r[ch][u * 4 + 1]) * p.scale),
+                           "f"(__uint_as_float(r[ch][u * 4 + 2]) * p.scale),
+                           "f"(__uint_as_float(r[ch][u * 4 + 3]) * p.scale)
+                           : "memory");
+        }
       }
       ++n;
+    }
+    if constexpr (C::kDqTma) {
+      if (lane == 0) bulk_wait_group0<false>();  // this warp's reductions complete
     }
     // dK, dV of this key tile
     bool have = n > 0 && !aborted;
@@ -593,11 +705,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     const int kr = x.c * kTile + row;
     const bool write = kr < p.L && !*abort_flag && (n == 0 || have);
     const size_t off =
-        ((static_cast<size_t>(x.bb) * p.S +
-          token_at(p.layout, p.L, p.N, x.j, kr < p.L ? kr : 0)) *
-             p.n_kv +
-         x.kh) *
-        D;
+        ((static_cast<size_t>(x.bb) * p.S + token_at(p.layout, p.L, p.N, x.j, kr < p.L ? kr : 0)) *
+             p.n_kv + x.kh) * D;
 #pragma unroll
     for (int which = 0; which < 2; ++which) {
       const uint32_t col = which == 0 ? C::kColDk : C::kColDv;
@@ -608,10 +717,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         uint32_t r[32];
         if (have) tmem_ld32(tmem + lane_off + col + ch * 32, r);
         if (write) {
-          float4 *d4 = reinterpret_cast<float4 *>(dst + ch * 32);
+          float4 *o4 = reinterpret_cast<float4 *>(dst + ch * 32);
 #pragma unroll
           for (int u = 0; u < 8; ++u)
-            d4[u] = have ? make_float4(__uint_as_float(r[u * 4 + 0]) * mul,
+            o4[u] = have ? make_float4(__uint_as_float(r[u * 4 + 0]) * mul,
                                        __uint_as_float(r[u * 4 + 1]) * mul,
                                        __uint_as_float(r[u * 4 + 2]) * mul,
                                        __uint_as_float(r[u * 4 + 3]) * mul)
@@ -673,8 +782,9 @@ __global__ void bwd_pre_kernel(BwdParams p, const float *out, const float *lse,
 template <int D>
 cudaError_t launch_bwd_t(const BwdParams &p, const float *out, const float *lse,
                          const uint16_t *dout, const CUtensorMap &qmap, const CUtensorMap &kmap,
-                         const CUtensorMap &vmap, const CUtensorMap &domap, long long n_units,
-                         int n_sm, cudaStream_t stream) {
+                         const CUtensorMap &vmap, const CUtensorMap &domap,
+                         const CUtensorMap &dqmap, long long n_units, int n_sm,
+                         cudaStream_t stream) {
   using C = BwdCfg<D>;
   const long long pre_rows = static_cast<long long>(p.b) * p.h * p.N * p.Lpad;
   long long pre_blocks = (pre_rows * 32 + 255) / 256;
@@ -695,7 +805,7 @@ cudaError_t launch_bwd_t(const BwdParams &p, const float *out, const float *lse,
     if (attr.numRegs != C::kLaunchRegs) return cudaErrorInvalidConfiguration;
   }
   kern<<<dim3(static_cast<unsigned int>(n_units)), dim3(C::kThreads), C::kSmemAlloc, stream>>>(
-      p, qmap, kmap, vmap, domap);
+      p, qmap, kmap, vmap, domap, dqmap);
   return cudaGetLastError();
 }
 
@@ -703,13 +813,16 @@ cudaError_t launch_bwd_t(const BwdParams &p, const float *out, const float *lse,
 
 cudaError_t launch_bwd(const BwdParams &p, int d, const float *out, const float *lse,
                        const uint16_t *dout, const CUtensorMap &qmap, const CUtensorMap &kmap,
-                       const CUtensorMap &vmap, const CUtensorMap &domap, long long n_units,
-                       int n_sm, cudaStream_t stream) {
+                       const CUtensorMap &vmap, const CUtensorMap &domap,
+                       const CUtensorMap &dqmap, long long n_units, int n_sm,
+                       cudaStream_t stream) {
   if (n_units <= 0) return cudaSuccess;
   if (d == 128)
-    return launch_bwd_t<128>(p, out, lse, dout, qmap, kmap, vmap, domap, n_units, n_sm, stream);
+    return launch_bwd_t<128>(p, out, lse, dout, qmap, kmap, vmap, domap, dqmap, n_units, n_sm,
+                             stream);
   if (d == 64)
-    return launch_bwd_t<64>(p, out, lse, dout, qmap, kmap, vmap, domap, n_units, n_sm, stream);
+    return launch_bwd_t<64>(p, out, lse, dout, qmap, kmap, vmap, domap, dqmap, n_units, n_sm,
+                            stream);
   return cudaErrorInvalidValue;
 }
 

@@ -34,6 +34,7 @@
 // rounding residual P_lo in [64,128) of S_t, and issue a second PV MMA.
 #include <climits>
 #include <cmath>
+#include <type_traits>
 
 #include "ra_internal.cuh"
 #include "ra_ptx.cuh"
@@ -487,6 +488,10 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::kThreads, 1)
     int j, c, n = 0;
     bool partial;
     bool aborted = false;
+    // One copy of the tile loop per precision mode, chosen once per unit, so
+    // the hot loop carries no branch on it.
+    auto tile_loop = [&](auto split_tag) {
+    constexpr bool kSplit = decltype(split_tag)::value;
     while (kv_next(p, x, it, j, c, partial)) {
       const bool got = mbar_wait(&bars[C::bSFull + t], n & 1, abort_flag, kSiteSmS);
       if (!__all_sync(kFull, got)) {  // tcgen05.ld/st below are warp-collective
@@ -536,16 +541,6 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::kThreads, 1)
         alpha = ex2(m_run - mx2);  // 0 when m_run is still -inf
         m_run = mx2;
       }
-      l_sum *= alpha;
-      const float base = (m_run == -INFINITY) ? 0.f : m_run;
-      // P = 2^(s * scale * log2 e - shift): paired FMAs, four paired sums
-      const uint64_t sl2x2 = f2pack(sl2, sl2);
-      const uint64_t nbx2 = f2pack(-base, -base);
-      uint64_t acc[4];
-      if (split)
-        exp_pack_store<true>(s, sl2x2, nbx2, acc, tS);
-      else
-        exp_pack_store<false>(s, sl2x2, nbx2, acc, tS);
       if (n > 0 && __any_sync(kFull, need)) {
         // O_t row *= alpha.  The previous PV into O_t is complete: it was
         // issued before this tile's S MMA, whose commit we waited on.
@@ -558,6 +553,13 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::kThreads, 1)
           tmem_st32(tO + ch * 32, r);
         }
       }
+      l_sum *= alpha;
+      const float base = (m_run == -INFINITY) ? 0.f : m_run;
+      // P = 2^(s * scale * log2 e - shift): paired FMAs, four paired sums
+      const uint64_t sl2x2 = f2pack(sl2, sl2);
+      const uint64_t nbx2 = f2pack(-base, -base);
+      uint64_t acc[4];
+      exp_pack_store<kSplit>(s, sl2x2, nbx2, acc, tS);
       float a0, a1, a2, a3, a4, a5, a6, a7;
       f2unpack(acc[0], a0, a1);
       f2unpack(acc[1], a2, a3);
@@ -570,6 +572,11 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::kThreads, 1)
       if (lane == 0) mbar_arrive(&bars[C::bPReady + t]);
       ++n;
     }
+    };
+    if (split)
+      tile_loop(std::true_type{});
+    else
+      tile_loop(std::false_type{});
 
     // ------------------------------------------------------------ epilogue
     bool have_o = n > 0 && !aborted;

@@ -7,7 +7,7 @@
 #include <cuda_runtime.h>
 #include <cstdint>
 
-#include "../../include/ra.h"
+#include "ra.h"
 
 namespace ra {
 
@@ -95,8 +95,9 @@ cudaError_t launch_fwd(const FwdParams &p, int d, int nq, const CUtensorMap &qma
 // Backward launch (ra_bwd.cu): the D / LSE2 pre-pass, then the main kernel.
 cudaError_t launch_bwd(const BwdParams &p, int d, const float *out, const float *lse,
                        const uint16_t *dout, const CUtensorMap &qmap, const CUtensorMap &kmap,
-                       const CUtensorMap &vmap, const CUtensorMap &domap, long long n_units,
-                       int n_sm, cudaStream_t stream);
+                       const CUtensorMap &vmap, const CUtensorMap &domap,
+                       const CUtensorMap &dqmap, long long n_units, int n_sm,
+                       cudaStream_t stream);
 
 // Element-wise kernels (ra_small.cu).
 cudaError_t launch_finalize(float *o, const float *l, const float *m, float *lse, int b,
