@@ -134,10 +134,11 @@ __device__ __forceinline__ int warp_max(int v) {
 
 // Token positions covered by the unit's query tile.  Warp-collective in
 // block mode (positions come from q_pos).
+template <bool kBlock>
 __device__ __forceinline__ void unit_qrange(const FwdParams &p, Unit &x) {
   const int r0 = x.a * kTile;
   const int r1 = min(r0 + kTile, p.L) - 1;
-  if (!p.block_mode) {
+  if constexpr (!kBlock) {
     x.qmin = token_at(p.layout, p.L, p.N, x.i, r0);
     x.qmax = token_at(p.layout, p.L, p.N, x.i, r1);
     return;
@@ -163,10 +164,11 @@ struct KvIter {
 // Next key/value tile of the unit in ring order.  Returns false at the end.
 // `partial` marks tiles that need an element mask (causal diagonal or the
 // ragged last tile).  Warp-collective in block mode.
+template <bool kBlock>
 __device__ __forceinline__ bool kv_next(const FwdParams &p, const Unit &x, KvIter &it, int &j,
                                         int &c, bool &partial) {
   const int n_complete = p.Lk / kTile;
-  if (!p.block_mode) {
+  if constexpr (!kBlock) {
     while (it.c >= it.c_end) {
       if (++it.s >= p.N) return false;
       it.j = kv_shard_at(x.i, it.s, p.N);
@@ -189,7 +191,7 @@ __device__ __forceinline__ bool kv_next(const FwdParams &p, const Unit &x, KvIte
     partial = it.c >= it.c_full;
     ++it.c;
     return true;
-  }
+  } else {
   while (it.c < p.n_ktiles) {
     c = it.c++;
     j = 0;
@@ -213,6 +215,7 @@ __device__ __forceinline__ bool kv_next(const FwdParams &p, const Unit &x, KvIte
     return true;
   }
   return false;
+  }
 }
 
 // (c2, c3) tensor-map coordinates of local row r of shard p: striped maps are
@@ -282,7 +285,7 @@ __device__ __forceinline__ void exp_pack_store(const float (&s)[kTile], uint64_t
   }
 }
 
-template <int D, int NQ>
+template <int D, int NQ, bool kBlock>
 __global__ void __launch_bounds__(FwdCfg<D, NQ>::kThreads, 1)
     fwd_kernel(const __grid_constant__ FwdParams p, const __grid_constant__ CUtensorMap qmap,
                const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap) {
@@ -326,8 +329,8 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::kThreads, 1)
   const uint32_t tmem = *tmem_holder;
 
   Unit x = decode_unit(p, blockIdx.x);
-  unit_qrange(p, x);
-  const bool split = p.block_mode || (p.causal ? (x.qmin + 1 < kSplitKeys) : (p.S < kSplitKeys));
+  unit_qrange<kBlock>(p, x);
+  const bool split = kBlock || (p.causal ? (x.qmin + 1 < kSplitKeys) : (p.S < kSplitKeys));
 
   if (warp >= C::kSoftmaxWarps) {
     if constexpr (C::kResplit) regs_set<C::kOtherRegs, C::kLaunchRegs>();
@@ -355,7 +358,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::kThreads, 1)
     KvIter it;
     int j, c, n = 0;
     bool partial;
-    while (kv_next(p, x, it, j, c, partial)) {
+    while (kv_next<kBlock>(p, x, it, j, c, partial)) {
       if (lane == 0) {
         shard_coords(p.layout, j, c * kTile, c2, c3);
         const int ks = n % C::kKSt;
@@ -404,7 +407,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::kThreads, 1)
       KvIter it;
       int j, c, n = 0;
       bool partial;
-      bool has = kv_next(p, x, it, j, c, partial);
+      bool has = kv_next<kBlock>(p, x, it, j, c, partial);
       if (has && lane == 0) {
         if (mbar_wait(&bars[C::bKFull + 0], 0, abort_flag, kSiteMmaK)) {
           tc_fence_after();
@@ -418,7 +421,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::kThreads, 1)
       }
       __syncwarp();
       while (has && !*abort_flag) {
-        const bool has_next = kv_next(p, x, it, j, c, partial);
+        const bool has_next = kv_next<kBlock>(p, x, it, j, c, partial);
         if (lane == 0) {
           const int vs = n % C::kVSt;
           const uint32_t vph = (n / C::kVSt) & 1;
@@ -477,7 +480,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::kThreads, 1)
     const int r_abs = x.a * kTile + row;
     const bool row_exists = r_abs < p.L;
     const int r_cl = row_exists ? r_abs : p.L - 1;
-    const int qp = p.block_mode ? (p.causal ? p.q_pos[r_cl] : 0)
+    const int qp = kBlock ? (p.causal ? p.q_pos[r_cl] : 0)
                                 : token_at(p.layout, p.L, p.N, x.i, r_cl);
     const float sl2 = p.scale_log2;
 
@@ -492,7 +495,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::kThreads, 1)
     // the hot loop carries no branch on it.
     auto tile_loop = [&](auto split_tag) {
     constexpr bool kSplit = decltype(split_tag)::value;
-    while (kv_next(p, x, it, j, c, partial)) {
+    while (kv_next<kBlock>(p, x, it, j, c, partial)) {
       const bool got = mbar_wait(&bars[C::bSFull + t], n & 1, abort_flag, kSiteSmS);
       if (!__all_sync(kFull, got)) {  // tcgen05.ld/st below are warp-collective
         aborted = true;
@@ -505,7 +508,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::kThreads, 1)
 #pragma unroll
       for (int e = 0; e < kTile; ++e) s[e] = __uint_as_float(sr[e]);
       if (partial) {
-        if (!p.block_mode) {
+        if constexpr (!kBlock) {
           int lim = p.Lk - 1;
           if (p.causal) lim = min(lim, last_visible_row(p.layout, p.L, p.N, j, qp));
           const int climit = lim - c * kTile;
@@ -585,7 +588,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::kThreads, 1)
       tc_fence_after();
     }
     have_o = __all_sync(kFull, have_o && *abort_flag == 0);
-    if (!p.block_mode) {
+    if constexpr (!kBlock) {
       const int tok = token_at(p.layout, p.L, p.N, x.i, r_cl);
       const size_t orow = ((static_cast<size_t>(x.bb) * p.S + tok) * p.h + hq) * D;
       const bool live = have_o && l_sum > 0.f;
@@ -652,11 +655,11 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::kThreads, 1)
   }
 }
 
-template <int D, int NQ>
+template <int D, int NQ, bool kBlock>
 cudaError_t launch_fwd_t(const FwdParams &p, const CUtensorMap &qmap, const CUtensorMap &kmap,
                          const CUtensorMap &vmap, long long n_units, cudaStream_t stream) {
   using C = FwdCfg<D, NQ>;
-  auto kern = fwd_kernel<D, NQ>;
+  auto kern = fwd_kernel<D, NQ, kBlock>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemAlloc);
   if (e != cudaSuccess) return e;
@@ -679,10 +682,19 @@ cudaError_t launch_fwd(const FwdParams &p, int d, int nq, const CUtensorMap &qma
                        const CUtensorMap &kmap, const CUtensorMap &vmap, long long n_units,
                        cudaStream_t stream) {
   if (n_units <= 0) return cudaSuccess;
-  if (d == 128 && nq == 2) return launch_fwd_t<128, 2>(p, qmap, kmap, vmap, n_units, stream);
-  if (d == 128 && nq == 1) return launch_fwd_t<128, 1>(p, qmap, kmap, vmap, n_units, stream);
-  if (d == 64 && nq == 2) return launch_fwd_t<64, 2>(p, qmap, kmap, vmap, n_units, stream);
-  if (d == 64 && nq == 1) return launch_fwd_t<64, 1>(p, qmap, kmap, vmap, n_units, stream);
+  const bool blk = p.block_mode != 0;
+  if (d == 128 && nq == 2)
+    return blk ? launch_fwd_t<128, 2, true>(p, qmap, kmap, vmap, n_units, stream)
+               : launch_fwd_t<128, 2, false>(p, qmap, kmap, vmap, n_units, stream);
+  if (d == 128 && nq == 1)
+    return blk ? launch_fwd_t<128, 1, true>(p, qmap, kmap, vmap, n_units, stream)
+               : launch_fwd_t<128, 1, false>(p, qmap, kmap, vmap, n_units, stream);
+  if (d == 64 && nq == 2)
+    return blk ? launch_fwd_t<64, 2, true>(p, qmap, kmap, vmap, n_units, stream)
+               : launch_fwd_t<64, 2, false>(p, qmap, kmap, vmap, n_units, stream);
+  if (d == 64 && nq == 1)
+    return blk ? launch_fwd_t<64, 1, true>(p, qmap, kmap, vmap, n_units, stream)
+               : launch_fwd_t<64, 1, false>(p, qmap, kmap, vmap, n_units, stream);
   return cudaErrorInvalidValue;
 }
 
