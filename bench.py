@@ -46,6 +46,8 @@ def _args():
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the layout / causal-imbalance measurements")
     return ap.parse_args()
 
 
@@ -178,6 +180,85 @@ def run_reference(a, rank, world):
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }), flush=True)
+
+
+# ---------------------------------------------------------------- extras
+def _time_ms(fn, reps=2):
+    import torch
+    fn()
+    torch.cuda.synchronize()
+    best = None
+    for _ in range(reps):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fn()
+        e1.record()
+        torch.cuda.synchronize()
+        t = e0.elapsed_time(e1)
+        best = t if best is None else min(best, t)
+    return best
+
+
+def layout_and_imbalance_report(w, q, k, v, dev):
+    """Forward of the same shape non-causal and with contiguous shards, and
+    the causal load-balance picture of the third page's section 6: time one
+    ra_block_step per (query shard i, ring step s), t(i, s), and form the
+    makespan an N-device ring would see, T = sum_s max_i t(i, s), and its
+    utilisation sum t / (N T)."""
+    import torch
+
+    from long_context_exact_gb300 import accounting
+    from long_context_exact_gb300 import binding as ra
+    from long_context_exact_gb300.inputs import CONTIGUOUS, STRIPED
+
+    out = torch.empty((w.b, w.S, w.h, w.d), dtype=torch.float32, device=dev)
+    lse = torch.empty((w.b, w.h, w.S), dtype=torch.float32, device=dev)
+    rep = {}
+    f_nc = accounting.fwd_useful_flops(w.b, w.S, w.h, w.d, False)
+    f_c = accounting.fwd_useful_flops(w.b, w.S, w.h, w.d, True)
+    for name, layout, causal, flops in (("noncausal", STRIPED, False, f_nc),
+                                        ("causal_striped", STRIPED, True, f_c),
+                                        ("causal_contiguous", CONTIGUOUS, True, f_c)):
+        ms = _time_ms(lambda: ra.ring_attention(q, k, v, w.n_shards, layout, causal, out=out,
+                                                lse=lse))
+        rep[name + "_fwd_ms"] = ms
+        rep[name + "_fwd_tflops"] = flops / (ms / 1e3) / 1e12
+    rep["striped_causal_vs_noncausal_per_useful_flop"] = (
+        rep["causal_striped_fwd_tflops"] / rep["noncausal_fwd_tflops"])
+    del out, lse
+    # per-(shard, step) block steps
+    N, L = w.n_shards, w.S // w.n_shards
+    for name, layout in (("contiguous", CONTIGUOUS), ("striped", STRIPED)):
+        _, _, tok = ra.position_map(layout, w.S, N, device=dev)
+        t = [[0.0] * N for _ in range(N)]
+        for i in range(N):
+            qi = q.index_select(1, tok[i].long()).contiguous()
+            st = ra.new_state(w.b, L, w.h, w.d, dev)
+            for s_ in range(N):
+                j = (i - s_) % N
+                kj = k.index_select(1, tok[j].long()).contiguous()
+                vj = v.index_select(1, tok[j].long()).contiguous()
+                torch.cuda.synchronize()
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record()
+                ra.block_step(qi, kj, vj, st, tok[i], tok[j], True)
+                e1.record()
+                torch.cuda.synchronize()
+                t[i][s_] = e0.elapsed_time(e1)
+                del kj, vj
+            del qi, st
+        total = sum(sum(r) for r in t)
+        makespan = sum(max(t[i][s_] for i in range(N)) for s_ in range(N))
+        rep["ring_" + name] = {
+            "sum_ms": total, "makespan_ms": makespan, "utilisation": total / (N * makespan),
+            "per_shard_ms": [sum(t[i]) for i in range(N)]}
+    rep["model_utilisation_contiguous"] = {
+        "(N+1)/2N": accounting.causal_utilisation_contiguous(N),
+        "N/(2N-1)": accounting.causal_utilisation_contiguous(N, half_diagonal=True)}
+    ra.stream_check()
+    return rep
 
 
 # ---------------------------------------------------------------- our arm
@@ -349,6 +430,10 @@ def run_ours(a, rank, world, local_rank):
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": e2e_ms / a.steps}
 
+    extras = None
+    if rank == 0 and not a.no_extras:
+        extras = layout_and_imbalance_report(w, q, k, v, dev)
+
     cpu = None
     if rank == 0 and world == 1 and not a.no_cpu_baseline:
         fwd_rows, bwd_rows = 16, 4
@@ -377,6 +462,7 @@ def run_ours(a, rank, world, local_rank):
             "bwd_tflops": (f_bwd / (bwd_ms / 1e3) / 1e12) if have_bwd else None,
             "clocks": clk, "e2e": e2e, "gpu_launches": launches, "roofline": roofline,
             "cpu_baseline": cpu,
+            "extras": extras,
         }
         print(json.dumps(line), flush=True)
 

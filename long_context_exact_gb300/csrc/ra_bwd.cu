@@ -156,12 +156,15 @@ __device__ __forceinline__ int first_row_at_or_after(const BwdParams &p, int i, 
 }
 
 struct QIter {
-  int s = -1, i = 0, a = 0, a_full = 0, hh = 0;
+  int s = -1, i = 0, a = 0, a_lo = 0, a_full = 0, hh = 0;
 };
 
 // Next (query shard i, query tile a, query head hq) that meets this key
-// tile, in ring order.  `partial` marks steps that need the causal element
-// mask.
+// tile: shards in ring order; inside a shard the query tiles from the last
+// down to the first visible one, so every key tile of a KV head starts on the
+// same query tile and concurrently resident CTAs stream the same Q / dO
+// tiles.  `partial` marks steps that need the causal element mask; `split`
+// steps whose query tile has a row seeing fewer than kSplitKeys keys.
 __device__ __forceinline__ bool q_next(const BwdParams &p, const KvUnit &x, QIter &it, int &i,
                                        int &a, int &hq, bool &partial, bool &split) {
   bool have = false;
@@ -170,7 +173,7 @@ __device__ __forceinline__ bool q_next(const BwdParams &p, const KvUnit &x, QIte
       have = true;
     } else {
       it.hh = 0;
-      if (++it.a < p.n_qtiles) have = true;
+      if (--it.a >= it.a_lo) have = true;
     }
   }
   while (!have) {
@@ -178,17 +181,18 @@ __device__ __forceinline__ bool q_next(const BwdParams &p, const KvUnit &x, QIte
     it.i = (x.j + it.s) % p.N;
     it.hh = 0;
     if (!p.causal) {
-      it.a = 0;
+      it.a_lo = 0;
       it.a_full = 0;
     } else {
       // visible query tiles: those whose last row sees the tile's first key
       const int r_vis = max(0, first_row_at_or_after(p, it.i, x.kmin));
-      it.a = r_vis >= p.L ? p.n_qtiles : r_vis / kTile;
+      it.a_lo = r_vis >= p.L ? p.n_qtiles : r_vis / kTile;
       // unmasked query tiles: every row sees the tile's last key
       const int r_full = max(0, first_row_at_or_after(p, it.i, x.kmax));
       it.a_full = min(p.n_qtiles, (r_full + kTile - 1) / kTile);
     }
-    have = it.a < p.n_qtiles;
+    it.a = p.n_qtiles - 1;
+    have = it.a >= it.a_lo;
   }
   i = it.i;
   a = it.a;
