@@ -22,19 +22,21 @@
 // residual): dV += P_hi^T dO + P_lo^T dO, dK += dS_hi^T Q + dS_lo^T Q,
 // dQ = dS_hi K + dS_lo K.
 //
-// Warp roles (12 warps):
-//   warps 0-3  "softmax": thread = key row; P^T = exp2(S^T - LSE2), written to
-//              TMEM as bf16 (and its residual on split steps); dS^T =
-//              P^T (dP^T - D) to shared memory (its residual to the staging
-//              buffer, on split steps)
-//   warps 4-7  dQ drain: TMEM -> registers -> staging buffer -> TMA bulk
+// Warp roles (16 warps):
+//   warps 0-7  "softmax", two warpgroups each owning 64 of the 128 query
+//              columns for all 128 keys (thread = key row): P^T =
+//              exp2(S^T - LSE2) to TMEM as bf16 (and its residual on split
+//              steps); dS^T = P^T (dP^T - D) to shared memory (its residual to
+//              the staging buffer, on split steps)
+//   warps 8-11 dQ drain: TMEM -> registers -> staging buffer -> TMA bulk
 //              reduce-add into dq, 32 rows per warp (d = 128; vector
 //              reductions for d = 64); then the dK / dV epilogue
-//   warp 8     TMA producer: K, V once; Q tiles (with their rows' LSE2 and
+//   warp 12    TMA producer: K, V once; Q tiles (with their rows' LSE2 and
 //              D) into a 2-deep ring, dO tiles into one buffer
-//   warp 9     TMEM allocator and MMA issuer (lane 0)
-//   warps 10-11 idle
-// TMEM columns: S^T then P_hi^T [0,64) + P_lo^T [64,128); dP^T then dQ
+//   warp 13    TMEM allocator and MMA issuer (lane 0)
+//   warps 14-15 idle
+// TMEM columns: S^T [0,128), then P^T over it: query columns 64h..64h+63
+// as bf16 pairs hi at 64h + [0,32), lo at 64h + [32,64); dP^T then dQ
 // [128,256); dV [256,..); dK [384,..).
 // MMAs per step: S^T = K Q^T, dP^T = V dO^T (SS, both K-major);
 // dV += P^T dO (A from TMEM, dO MN-major); dK += dS^T Q (dS^T K-major, Q
@@ -93,17 +95,20 @@ struct BwdCfg {
   static constexpr int kSlack = kSmemBytes + 1024 <= kMaxSmem ? 1024 : kMaxSmem - kSmemBytes;
   static_assert(kSlack >= 0, "shared memory layout too large");
   static constexpr int kSmemAlloc = kSmemBytes + kSlack;
-  static constexpr int kThreads = 384;
-  // 168 registers per thread at launch = 128 x (232 softmax + 160 dQ drain
-  // + 112 producer / MMA) re-split per warpgroup.
-  static constexpr int kLaunchRegs = 168;
-  static constexpr int kSoftmaxRegs = 232;
-  static constexpr int kDrainRegs = 160;
+  static constexpr int kThreads = 512;
+  // 128 registers per thread at launch = 128 x (152 + 152 softmax halves
+  // + 96 dQ drain + 112 producer / MMA) re-split per warpgroup.
+  static constexpr int kLaunchRegs = 128;
+  static constexpr int kSoftmaxRegs = 152;
+  static constexpr int kDrainRegs = 96;
   static constexpr int kOtherRegs = 112;
-  static_assert(128 * (kSoftmaxRegs + kDrainRegs + kOtherRegs) == kThreads * kLaunchRegs,
+  static_assert(128 * (2 * kSoftmaxRegs + kDrainRegs + kOtherRegs) == kThreads * kLaunchRegs,
                 "register re-split must use exactly the launch pool");
-  static constexpr int kProducerWarp = 8;
-  static constexpr int kMmaWarp = 9;
+  static constexpr int kSoftmaxWarps = 8;
+  static constexpr int kDrainWarp0 = 8;
+  static constexpr int kProducerWarp = 12;
+  static constexpr int kMmaWarp = 13;
+  static constexpr int kHalfCols = 64;  // query columns per softmax warpgroup
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColS = 0, kColDp = 128, kColDv = 256, kColDk = 384;
   static constexpr uint32_t kIdescKK = idesc_bf16_f32(128, 128, false, false);  // S^T, dP^T
@@ -225,24 +230,26 @@ __device__ __forceinline__ void mma_kk(uint32_t d_tmem, uint32_t a_saddr, uint32
   }
 }
 
-// P^T row (fp32) to TMEM as bf16 pairs in columns [0,64); with kSplit the
-// rounding residual too, in columns [64,128).
+// 64 columns of a P^T row (fp32), query columns [c_base, c_base + 64), to
+// TMEM as bf16 pairs over the S^T columns they came from: at c_base + [0,32),
+// and with kSplit the rounding residual at c_base + [32,64).  Each softmax
+// warpgroup so overwrites only the S^T columns it has itself read.
 template <bool kSplit>
-__device__ __forceinline__ void store_p_pair(const float (&pf)[kTile], uint32_t tS) {
+__device__ __forceinline__ void store_p_half(const float (&pf)[64], uint32_t tS, int c_base) {
 #pragma unroll
-  for (int q4 = 0; q4 < 4; ++q4) {
+  for (int q2 = 0; q2 < 2; ++q2) {
     uint32_t hi[16];
     uint32_t lo[kSplit ? 16 : 1];
 #pragma unroll
     for (int e = 0; e < 16; ++e) {
-      const int c = q4 * 32 + 2 * e;
+      const int c = q2 * 32 + 2 * e;
       hi[e] = pack_bf16x2(pf[c], pf[c + 1]);
       if constexpr (kSplit)
         lo[e] = pack_bf16x2(pf[c] - __uint_as_float(hi[e] << 16),
                             pf[c + 1] - __uint_as_float(hi[e] & 0xffff0000u));
     }
-    tmem_st16(tS + q4 * 16, hi);
-    if constexpr (kSplit) tmem_st16(tS + 64 + q4 * 16, lo);
+    tmem_st16(tS + c_base + q2 * 16, hi);
+    if constexpr (kSplit) tmem_st16(tS + c_base + 32 + q2 * 16, lo);
   }
 }
 
@@ -277,8 +284,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     mbar_init(&bars[C::bDoEmpty], 1);
     mbar_init(&bars[C::bSFull], 1);
     mbar_init(&bars[C::bDpFull], 1);
-    mbar_init(&bars[C::bPReady], 4);
-    mbar_init(&bars[C::bDsReady], 4);
+    mbar_init(&bars[C::bPReady], 8);
+    mbar_init(&bars[C::bDsReady], 8);
     mbar_init(&bars[C::bDsEmpty], 1);
     mbar_init(&bars[C::bDqFull], 1);
     mbar_init(&bars[C::bDqEmpty], 4);
@@ -298,7 +305,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
   const uint32_t tmem = *tmem_holder;
   const KvUnit x = decode_kv_unit(p, blockIdx.x);
 
-  if (warp >= 8) {
+  if (warp >= C::kProducerWarp) {
     regs_set<C::kOtherRegs, C::kLaunchRegs>();
     if (warp == C::kProducerWarp) {
       // ---------------------------------------------------------- producer
@@ -410,13 +417,13 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
               // dV += P_hi^T dO (+ P_lo^T dO): A from TMEM (bf16 pairs), B = dO MN-major
 #pragma unroll
               for (int kk = 0; kk < kTile / 16; ++kk)
-                mma_ts(tmem + C::kColDv, tmem + C::kColS + kk * 8,
+                mma_ts(tmem + C::kColDv, tmem + C::kColS + (kk >> 2) * 64 + (kk & 3) * 8,
                        smem_desc_sw128(do_s + kk * 16 * 128, kTile * 128, 1024), C::kIdescDv,
                        (n > 0 || kk > 0) ? 1u : 0u);
               if (cur_split)
 #pragma unroll
                 for (int kk = 0; kk < kTile / 16; ++kk)
-                  mma_ts(tmem + C::kColDv, tmem + C::kColS + 64 + kk * 8,
+                  mma_ts(tmem + C::kColDv, tmem + C::kColS + (kk >> 2) * 64 + 32 + (kk & 3) * 8,
                          smem_desc_sw128(do_s + kk * 16 * 128, kTile * 128, 1024), C::kIdescDv,
                          1u);
               mma_commit(&bars[C::bDoEmpty]);
@@ -481,75 +488,68 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       }
       __syncwarp();
     }
-  } else if (warp < 4) {
+  } else if (warp < C::kSoftmaxWarps) {
     regs_set<C::kSoftmaxRegs, C::kLaunchRegs>();
     // ------------------------------------------------------------ softmax (thread = key)
-    const int row = warp * 32 + lane;
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const int half = warp >> 2;          // which 64 query columns
+    const int cb = half * C::kHalfCols;  // first query column of this warpgroup
+    const int row = (warp & 3) * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_off + C::kColS;
-    const uint32_t tDp = tmem + lane_off + C::kColDp;
+    const uint32_t tDp = tmem + lane_off + C::kColDp + cb;
     const int kr = x.c * kTile + row;
     const bool key_exists = kr < p.L;
     const int kp = token_at(p.layout, p.L, p.N, x.j, key_exists ? kr : p.L - 1);
     const float sl2 = p.scale_log2;
-    uint8_t *ds_row = smem + C::kDsOff + row * 128;
-    uint8_t *dslo_row = smem + C::kStgOff + row * 128;
+    // this warpgroup's 64 query columns are one 128-byte-swizzled half of dS^T
+    uint8_t *ds_row = smem + C::kDsOff + half * (kTile * 128) + row * 128;
+    uint8_t *dslo_row = smem + C::kStgOff + half * (kTile * 128) + row * 128;
     QIter it;
     int i, a, hq, n = 0;
     bool partial, split;
     while (q_next(p, x, it, i, a, hq, partial, split)) {
       // this step's LSE2 and D rows, staged by the producer with the Q tile
       const float4 *lse4 = reinterpret_cast<const float4 *>(
-          smem + C::kStatOff + (n % C::kQSt) * 2 * C::kRowStatBytes);
+                               smem + C::kStatOff + (n % C::kQSt) * 2 * C::kRowStatBytes) +
+                           cb / 4;
       const float4 *d4 = lse4 + kTile / 4;
-      // query columns c < c0 are masked for this key
+      // query columns cb + c with c < c0 are masked for this key
       int c0 = 0;
-      if (partial) c0 = first_row_at_or_after(p, i, kp) - a * kTile;
+      if (partial) c0 = first_row_at_or_after(p, i, kp) - a * kTile - cb;
       if (!key_exists) {
-        c0 = kTile;
+        c0 = C::kHalfCols;
         partial = true;
       }
       if (!__all_sync(kFull, mbar_wait(&bars[C::bSFull], n & 1, abort_flag, kSiteBSmS))) break;
       tc_fence_after();
-      float pf[kTile];  // P^T row of this key, fp32
+      float pf[C::kHalfCols];  // this warpgroup's half of the P^T row, fp32
       {
-        uint32_t sr[kTile];
-        tmem_ld128(tS, sr);
-        // LSE2 of 32 query columns at a time, the next group's loads in
-        // flight while the current group is exponentiated
-        float4 lc[8], ln[8];
+        uint32_t sr[2][32];
+        tmem_ld32_start(tS + cb, sr[0]);
+        tmem_ld32_start(tS + cb + 32, sr[1]);
+        float4 l4[16];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) lc[e] = lse4[e];
+        for (int e = 0; e < 16; ++e) l4[e] = lse4[e];
+        tmem_ld_wait_regs(sr[0]);
+        tmem_ld_wait_regs(sr[1]);
 #pragma unroll
-        for (int ch = 0; ch < 4; ++ch) {
-          if (ch < 3) {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) ln[e] = lse4[(ch + 1) * 8 + e];
-          }
-#pragma unroll
-          for (int e4 = 0; e4 < 8; ++e4) {
-            const int c = ch * 32 + e4 * 4;
-            pf[c + 0] = ex2(fmaf(__uint_as_float(sr[c + 0]), sl2, -lc[e4].x));
-            pf[c + 1] = ex2(fmaf(__uint_as_float(sr[c + 1]), sl2, -lc[e4].y));
-            pf[c + 2] = ex2(fmaf(__uint_as_float(sr[c + 2]), sl2, -lc[e4].z));
-            pf[c + 3] = ex2(fmaf(__uint_as_float(sr[c + 3]), sl2, -lc[e4].w));
-          }
-          if (ch < 3) {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) lc[e] = ln[e];
-          }
+        for (int e4 = 0; e4 < 16; ++e4) {
+          const int c = e4 * 4;
+          pf[c + 0] = ex2(fmaf(__uint_as_float(sr[c >> 5][(c + 0) & 31]), sl2, -l4[e4].x));
+          pf[c + 1] = ex2(fmaf(__uint_as_float(sr[c >> 5][(c + 1) & 31]), sl2, -l4[e4].y));
+          pf[c + 2] = ex2(fmaf(__uint_as_float(sr[c >> 5][(c + 2) & 31]), sl2, -l4[e4].z));
+          pf[c + 3] = ex2(fmaf(__uint_as_float(sr[c >> 5][(c + 3) & 31]), sl2, -l4[e4].w));
         }
       }
       if (partial) {  // causal diagonal: columns before c0 do not see this key
 #pragma unroll
-        for (int c = 0; c < kTile; ++c)
+        for (int c = 0; c < C::kHalfCols; ++c)
           if (c < c0) pf[c] = 0.f;
       }
-      // P_hi^T to columns [0,64) (and P_lo^T to [64,128) on split steps)
       if (split)
-        store_p_pair<true>(pf, tS);
+        store_p_half<true>(pf, tS, cb);
       else
-        store_p_pair<false>(pf, tS);
+        store_p_half<false>(pf, tS, cb);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
@@ -562,58 +562,58 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         go = mbar_wait(&bars[C::bStgEmpty], (n - 1) & 1, abort_flag, kSiteBSmStg);
       if (!__all_sync(kFull, go)) break;
       tc_fence_after();
-      uint32_t rc[32], rn[32];
-      float4 dc[8], dn[8];
-      tmem_ld32_start(tDp, rc);
+      // 16 query columns at a time; the next group's dP^T and D in flight
+      uint32_t rc[16], rn[16];
+      float4 dc[4], dn[4];
+      tmem_ld16_start(tDp, rc);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) dc[e] = d4[e];
-      tmem_ld_wait_regs(rc);
+      for (int e = 0; e < 4; ++e) dc[e] = d4[e];
+      tmem_ld_wait_regs16(rc);
 #pragma unroll
       for (int ch = 0; ch < 4; ++ch) {
-        if (ch < 3) {  // next 32 columns of dP^T and D in flight
-          tmem_ld32_start(tDp + (ch + 1) * 32, rn);
+        if (ch < 3) {
+          tmem_ld16_start(tDp + (ch + 1) * 16, rn);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) dn[e] = d4[(ch + 1) * 8 + e];
+          for (int e = 0; e < 4; ++e) dn[e] = d4[(ch + 1) * 4 + e];
         }
-        uint32_t whi[16], wlo[16];
-        float sv[32];
+        float sv[16];
 #pragma unroll
-        for (int e4 = 0; e4 < 8; ++e4) {
-          const int c = ch * 32 + e4 * 4;
+        for (int e4 = 0; e4 < 4; ++e4) {
+          const int c = ch * 16 + e4 * 4;
           sv[e4 * 4 + 0] = pf[c + 0] * (__uint_as_float(rc[e4 * 4 + 0]) - dc[e4].x);
           sv[e4 * 4 + 1] = pf[c + 1] * (__uint_as_float(rc[e4 * 4 + 1]) - dc[e4].y);
           sv[e4 * 4 + 2] = pf[c + 2] * (__uint_as_float(rc[e4 * 4 + 2]) - dc[e4].z);
           sv[e4 * 4 + 3] = pf[c + 3] * (__uint_as_float(rc[e4 * 4 + 3]) - dc[e4].w);
         }
+        uint32_t whi[8];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) whi[e] = pack_bf16x2(sv[2 * e], sv[2 * e + 1]);
-        // 32 queries = four 16-byte chunks of this key's row, 128-byte swizzled
-        uint8_t *half = ds_row + (ch >> 1) * (kTile * 128);
+        for (int e = 0; e < 8; ++e) whi[e] = pack_bf16x2(sv[2 * e], sv[2 * e + 1]);
+        // 16 queries = two 16-byte chunks of this key's row, 128-byte swizzled
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int chunk = ((ch & 1) * 4 + u) ^ (row & 7);
-          *reinterpret_cast<uint4 *>(half + chunk * 16) =
+        for (int u = 0; u < 2; ++u) {
+          const int chunk = (ch * 2 + u) ^ (row & 7);
+          *reinterpret_cast<uint4 *>(ds_row + chunk * 16) =
               make_uint4(whi[u * 4 + 0], whi[u * 4 + 1], whi[u * 4 + 2], whi[u * 4 + 3]);
         }
         if (split) {
+          uint32_t wlo[8];
 #pragma unroll
-          for (int e = 0; e < 16; ++e)
+          for (int e = 0; e < 8; ++e)
             wlo[e] = pack_bf16x2(sv[2 * e] - __uint_as_float(whi[e] << 16),
                                  sv[2 * e + 1] - __uint_as_float(whi[e] & 0xffff0000u));
-          uint8_t *half_lo = dslo_row + (ch >> 1) * (kTile * 128);
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int chunk = ((ch & 1) * 4 + u) ^ (row & 7);
-            *reinterpret_cast<uint4 *>(half_lo + chunk * 16) =
+          for (int u = 0; u < 2; ++u) {
+            const int chunk = (ch * 2 + u) ^ (row & 7);
+            *reinterpret_cast<uint4 *>(dslo_row + chunk * 16) =
                 make_uint4(wlo[u * 4 + 0], wlo[u * 4 + 1], wlo[u * 4 + 2], wlo[u * 4 + 3]);
           }
         }
         if (ch < 3) {
-          tmem_ld_wait_regs(rn);
+          tmem_ld_wait_regs16(rn);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) rc[e] = rn[e];
+          for (int e = 0; e < 16; ++e) rc[e] = rn[e];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) dc[e] = dn[e];
+          for (int e = 0; e < 4; ++e) dc[e] = dn[e];
         }
       }
       fence_proxy_async_smem();
@@ -622,7 +622,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       if (lane == 0) mbar_arrive(&bars[C::bDsReady]);
       ++n;
     }
-  } else {
+  } else if (warp < C::kDrainWarp0 + 4) {
     regs_set<C::kDrainRegs, C::kLaunchRegs>();
     // ------------------------------------------------------------ dQ drain, then dK/dV
     const int row = (warp & 3) * 32 + lane;
@@ -639,12 +639,6 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         break;
       }
       tc_fence_after();
-      uint32_t r[D / 32][32];
-#pragma unroll
-      for (int ch = 0; ch < D / 32; ++ch) tmem_ld32(tDq + ch * 32, r[ch]);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[C::bDqEmpty]);
       if constexpr (C::kDqTma) {
         // Two rounds of two 32 x 32 boxes through this warp's staging slice;
         // the staging buffer is free: this step's dS_lo^T readers finished
@@ -653,17 +647,28 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         shard_coords_b(p.layout, i, a * kTile + (warp & 3) * 32, c2, c3);
 #pragma unroll
         for (int round = 0; round < 2; ++round) {
+          uint32_t r[2][32];
+          tmem_ld32_start(tDq + round * 64, r[0]);
+          tmem_ld32_start(tDq + round * 64 + 32, r[1]);
+          tmem_ld_wait_regs(r[0]);
+          tmem_ld_wait_regs(r[1]);
+          if (round == 1) {  // every dQ column is in registers: TMEM free for dP
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[C::bDqEmpty]);
+            if (lane == 0) bulk_wait_group0<true>();  // round 0's staging read
+            __syncwarp();
+          }
 #pragma unroll
           for (int bx = 0; bx < 2; ++bx) {
-            const int ch = round * 2 + bx;
             uint8_t *rowp = stg + bx * C::kDqBoxBytes + lane * 128;
 #pragma unroll
             for (int u = 0; u < 8; ++u)
               *reinterpret_cast<float4 *>(rowp + ((u ^ (lane & 7)) * 16)) =
-                  make_float4(__uint_as_float(r[ch][4 * u + 0]) * p.scale,
-                              __uint_as_float(r[ch][4 * u + 1]) * p.scale,
-                              __uint_as_float(r[ch][4 * u + 2]) * p.scale,
-                              __uint_as_float(r[ch][4 * u + 3]) * p.scale);
+                  make_float4(__uint_as_float(r[bx][4 * u + 0]) * p.scale,
+                              __uint_as_float(r[bx][4 * u + 1]) * p.scale,
+                              __uint_as_float(r[bx][4 * u + 2]) * p.scale,
+                              __uint_as_float(r[bx][4 * u + 3]) * p.scale);
           }
           fence_proxy_async_smem();
           __syncwarp();
@@ -673,12 +678,20 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
               tma_reduce_add_5d(&dqmap, stg + bx * C::kDqBoxBytes, (round * 2 + bx) * 32, hq, c2,
                                 c3, x.bb);
             bulk_commit_group();
-            bulk_wait_group0<true>();  // staging read: reusable
           }
-          __syncwarp();
         }
-        if (lane == 0) mbar_arrive(&bars[C::bStgEmpty]);
+        if (lane == 0) {
+          bulk_wait_group0<true>();  // round 1's staging read: slice reusable
+          mbar_arrive(&bars[C::bStgEmpty]);
+        }
+        __syncwarp();
       } else {
+        uint32_t r[D / 32][32];
+#pragma unroll
+        for (int ch = 0; ch < D / 32; ++ch) tmem_ld32(tDq + ch * 32, r[ch]);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[C::bDqEmpty]);
         const int qr = a * kTile + row;
         if (qr < p.L) {
           float *dst = p.dq + ((static_cast<size_t>(x.bb) * p.S + token_at(p.layout, p.L, p.N, i, qr)) *
