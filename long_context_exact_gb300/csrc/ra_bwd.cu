@@ -112,8 +112,7 @@ struct BwdCfg {
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColS = 0, kColDp = 128, kColDv = 256, kColDk = 384;
   static constexpr uint32_t kIdescKK = idesc_bf16_f32(128, 128, false, false);  // S^T, dP^T
-  static constexpr uint32_t kIdescDv = idesc_bf16_f32(128, D, false, true);     // dV, dK
-  static constexpr uint32_t kIdescDq = idesc_bf16_f32(128, D, true, true);      // dQ
+  static constexpr uint32_t kIdescDv = idesc_bf16_f32(128, D, false, true);     // dV
   // D = 128: each drain warp adds its 32 rows of the dQ tile into dq with TMA
   // bulk reductions from its 8 KB of the staging buffer, 32 columns x 32 rows
   // per box (128-byte swizzled), two boxes per round, two rounds.
@@ -228,6 +227,37 @@ __device__ __forceinline__ void mma_kk(uint32_t d_tmem, uint32_t a_saddr, uint32
     mma_ss(d_tmem, smem_desc_sw128(a_saddr + off, 16, 1024),
            smem_desc_sw128(b_saddr + off, 16, 1024), idesc, kk > 0 ? 1u : 0u);
   }
+}
+
+// dK (+)= dS^T Q: A = dS^T (keys x queries, K-major), B = Q MN-major.
+template <int D>
+__device__ __forceinline__ void issue_dk(uint32_t d_tmem, uint32_t ds_saddr, uint32_t q_saddr,
+                                         bool accumulate) {
+#pragma unroll
+  for (int kk = 0; kk < kTile / 16; ++kk)
+    mma_ss(d_tmem, smem_desc_sw128(ds_saddr + (kk >> 2) * (kTile * 128) + (kk & 3) * 32, 16, 1024),
+           smem_desc_sw128(q_saddr + kk * 16 * 128, kTile * 128, 1024),
+           idesc_bf16_f32(128, D, false, true), (accumulate || kk > 0) ? 1u : 0u);
+}
+
+// dQ = dS K: A = dS (queries x keys) read from dS^T MN-major, B = K MN-major;
+// issue_dq_acc adds to what is there.
+template <int D>
+__device__ __forceinline__ void issue_dq_step(uint32_t d_tmem, uint32_t ds_saddr, uint32_t k_saddr,
+                                              bool accumulate) {
+#pragma unroll
+  for (int kk = 0; kk < kTile / 16; ++kk)
+    mma_ss(d_tmem, smem_desc_sw128(ds_saddr + kk * 16 * 128, kTile * 128, 1024),
+           smem_desc_sw128(k_saddr + kk * 16 * 128, kTile * 128, 1024),
+           idesc_bf16_f32(128, D, true, true), (accumulate || kk > 0) ? 1u : 0u);
+}
+template <int D>
+__device__ __forceinline__ void issue_dq(uint32_t d_tmem, uint32_t ds_saddr, uint32_t k_saddr) {
+  issue_dq_step<D>(d_tmem, ds_saddr, k_saddr, false);
+}
+template <int D>
+__device__ __forceinline__ void issue_dq_acc(uint32_t d_tmem, uint32_t ds_saddr, uint32_t k_saddr) {
+  issue_dq_step<D>(d_tmem, ds_saddr, k_saddr, true);
 }
 
 // 64 columns of a P^T row (fp32), query columns [c_base, c_base + 64), to
@@ -442,35 +472,21 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
             if (go) go = mbar_wait(&bars[C::bDsReady], n & 1, abort_flag, kSiteBMmaDs);
             if (go) {
               tc_fence_after();
-              // dK += dS^T Q: A = dS^T (keys x queries, K-major), B = Q MN-major
-#pragma unroll
-              for (int kk = 0; kk < kTile / 16; ++kk)
-                mma_ss(tmem + C::kColDk,
-                       smem_desc_sw128(ds_s + (kk >> 2) * (kTile * 128) + (kk & 3) * 32, 16, 1024),
-                       smem_desc_sw128(q_s + kk * 16 * 128, kTile * 128, 1024), C::kIdescDv,
-                       (n > 0 || kk > 0) ? 1u : 0u);
-              if (cur_split)  // dK += dS_lo^T Q
-#pragma unroll
-                for (int kk = 0; kk < kTile / 16; ++kk)
-                  mma_ss(tmem + C::kColDk,
-                         smem_desc_sw128(dslo_s + (kk >> 2) * (kTile * 128) + (kk & 3) * 32, 16,
-                                         1024),
-                         smem_desc_sw128(q_s + kk * 16 * 128, kTile * 128, 1024), C::kIdescDv,
-                         1u);
-              // dQ = dS K: A = dS (queries x keys) read from dS^T MN-major, B = K MN-major
-#pragma unroll
-              for (int kk = 0; kk < kTile / 16; ++kk)
-                mma_ss(tmem + C::kColDp, smem_desc_sw128(ds_s + kk * 16 * 128, kTile * 128, 1024),
-                       smem_desc_sw128(k_s + kk * 16 * 128, kTile * 128, 1024), C::kIdescDq,
-                       kk > 0 ? 1u : 0u);
-              if (cur_split)  // dQ += dS_lo K
-#pragma unroll
-                for (int kk = 0; kk < kTile / 16; ++kk)
-                  mma_ss(tmem + C::kColDp,
-                         smem_desc_sw128(dslo_s + kk * 16 * 128, kTile * 128, 1024),
-                         smem_desc_sw128(k_s + kk * 16 * 128, kTile * 128, 1024), C::kIdescDq,
-                         1u);
-              mma_commit(&bars[C::bDqFull]);
+              if (!cur_split) {
+                // dQ first, so the drain (and with it the next dP^T) starts
+                // while dK accumulates
+                issue_dq<D>(tmem + C::kColDp, ds_s, k_s);
+                mma_commit(&bars[C::bDqFull]);
+                issue_dk<D>(tmem + C::kColDk, ds_s, q_s, n > 0);
+              } else {
+                // the drain stages dQ where dS_lo^T is: every reader of
+                // dS_lo^T completes before dQ is handed over
+                issue_dk<D>(tmem + C::kColDk, ds_s, q_s, n > 0);
+                issue_dk<D>(tmem + C::kColDk, dslo_s, q_s, true);
+                issue_dq<D>(tmem + C::kColDp, ds_s, k_s);
+                issue_dq_acc<D>(tmem + C::kColDp, dslo_s, k_s);
+                mma_commit(&bars[C::bDqFull]);
+              }
               mma_commit(&bars[C::bDsEmpty]);
               mma_commit(&bars[C::bQEmpty + st]);
             }
