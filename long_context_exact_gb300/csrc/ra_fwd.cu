@@ -159,6 +159,11 @@ __device__ __forceinline__ void unit_qrange(const FwdParams &p, Unit &x) {
 
 struct KvIter {
   int s = -1, j = 0, c = 0, c_end = 0, c_full = 0;
+  // block mode: a window of 32 key tiles starting at `win`, with bit t of
+  // `keep` set when tile win + t holds a key some query of the unit sees,
+  // and of `part` when that tile needs the element mask
+  int win = -1;
+  uint32_t keep = 0, part = 0;
 };
 
 // Next key/value tile of the unit in ring order.  Returns false at the end.
@@ -192,29 +197,65 @@ __device__ __forceinline__ bool kv_next(const FwdParams &p, const Unit &x, KvIte
     ++it.c;
     return true;
   } else {
-  while (it.c < p.n_ktiles) {
-    c = it.c++;
-    j = 0;
     if (!p.causal) {
+      if (it.c >= p.n_ktiles) return false;
+      c = it.c++;
+      j = 0;
       partial = c >= n_complete;
       return true;
     }
-    int lo = INT_MAX, hi = INT_MIN;
-    for (int e = threadIdx.x & 31; e < kTile; e += 32) {
-      const int kr = c * kTile + e;
-      if (kr < p.Lk) {
-        const int v = p.k_pos[kr];
-        lo = min(lo, v);
-        hi = max(hi, v);
+    const int lane = threadIdx.x & 31;
+    while (true) {
+      if (it.win < 0 || it.c >= it.win + 32) {
+        if (it.c >= p.n_ktiles) return false;
+        // Classify the next 32 key tiles from their positions' min and max:
+        // eight tiles at a time, every lane loading four positions of each
+        // (coalesced), then one warp reduction per tile.
+        it.win = it.c;
+        it.keep = 0;
+        it.part = 0;
+#pragma unroll 1
+        for (int sb = 0; sb < 4; ++sb) {
+          int lo[8], hi[8];
+#pragma unroll
+          for (int t = 0; t < 8; ++t) {
+            lo[t] = INT_MAX;
+            hi[t] = INT_MIN;
+            const int tile = it.win + sb * 8 + t;
+#pragma unroll
+            for (int e = 0; e < kTile / 32; ++e) {
+              const int kr = tile * kTile + e * 32 + lane;
+              if (tile < p.n_ktiles && kr < p.Lk) {
+                const int v = p.k_pos[kr];
+                lo[t] = min(lo[t], v);
+                hi[t] = max(hi[t], v);
+              }
+            }
+          }
+#pragma unroll
+          for (int t = 0; t < 8; ++t) {
+            lo[t] = warp_min(lo[t]);
+            hi[t] = warp_max(hi[t]);
+            const int tile = it.win + sb * 8 + t;
+            if (tile < p.n_ktiles && lo[t] <= x.qmax) {  // else every key follows every query
+              it.keep |= 1u << (sb * 8 + t);
+              if (tile >= n_complete || hi[t] > x.qmin) it.part |= 1u << (sb * 8 + t);
+            }
+          }
+        }
       }
+      const uint32_t rem = it.keep & (~0u << (it.c - it.win));
+      if (rem == 0) {
+        it.c = it.win + 32;
+        continue;
+      }
+      const int t = __ffs(rem) - 1;
+      c = it.win + t;
+      j = 0;
+      partial = (it.part >> t) & 1u;
+      it.c = c + 1;
+      return true;
     }
-    lo = warp_min(lo);
-    hi = warp_max(hi);
-    if (lo > x.qmax) continue;  // every key after every query: skip
-    partial = (c >= n_complete) || (hi > x.qmin);
-    return true;
-  }
-  return false;
   }
 }
 
