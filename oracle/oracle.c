@@ -51,12 +51,19 @@ static double dot(const double *a, const double *b, int d)
 /* ------------------------------------------------------------------------ */
 /* Token placement.  [P3 section 6] contiguous: [0,1][2,3][4,5][6,7];
  * striped (stride N): [0,4][1,5][2,6][3,7].  [P1 "Striped Attention"]: token
- * t goes to device t mod N.  layout 0 = contiguous, 1 = striped.
+ * t goes to device t mod N.  [P1 "Zig-Zag Ring Attention"]: the sequence is
+ * cut into 2N half-blocks of C = S / 2N tokens and device p holds half-blocks
+ * p and 2N-1-p; reading (recorded in the design notes): the early half-block
+ * comes first in local order, so local rows [0, C) are tokens [pC, pC+C) and
+ * rows [C, 2C) are tokens [(2N-1-p)C, (2N-p)C).
+ * layout 0 = contiguous, 1 = striped, 2 = zig-zag.
  * shard_of[t], local_of[t] for every token; token_of[p*L + r] inverse map.  */
 ORC_API int orc_position_map(int layout, int64_t S, int N, int32_t *shard_of,
                              int32_t *local_of, int32_t *token_of)
 {
-    if (N <= 0 || S < 0 || S % N != 0 || (layout != 0 && layout != 1))
+    if (N <= 0 || S < 0 || S % N != 0 || layout < 0 || layout > 2)
+        return 1;
+    if (layout == 2 && S % (2 * (int64_t)N) != 0)
         return 1;
     int64_t L = S / N;
     for (int64_t t = 0; t < S; ++t) {
@@ -64,9 +71,19 @@ ORC_API int orc_position_map(int layout, int64_t S, int N, int32_t *shard_of,
         if (layout == 0) {
             p = t / L;
             r = t % L;
-        } else {
+        } else if (layout == 1) {
             p = t % N;
             r = t / N;
+        } else {
+            int64_t C = L / 2;
+            int64_t half = t / C;              /* which of the 2N half-blocks */
+            if (half < N) {
+                p = half;
+                r = t % C;
+            } else {
+                p = 2 * (int64_t)N - 1 - half;
+                r = C + t % C;
+            }
         }
         shard_of[t] = (int32_t)p;
         local_of[t] = (int32_t)r;

@@ -31,6 +31,7 @@ _lib = None
 
 CONTIGUOUS = 0
 STRIPED = 1
+ZIGZAG = 2
 
 
 def build(force: bool = False) -> str:
@@ -104,9 +105,9 @@ def default_scale(d: int) -> float:
 
 # --------------------------------------------------------------------------
 def position_map(layout: int, S: int, N: int):
-    """Token placement (contiguous / striped), third page section 6 and the
-    first page's "Striped Attention".  Returns (shard_of[S], local_of[S],
-    token_of[N, S//N]) as int32."""
+    """Token placement (contiguous / striped / zig-zag), third page section 6
+    and the first page's "Striped Attention" and "Zig-Zag Ring Attention".
+    Returns (shard_of[S], local_of[S], token_of[N, S//N]) as int32."""
     lib = _load()
     shard = np.empty(S, np.int32)
     local = np.empty(S, np.int32)

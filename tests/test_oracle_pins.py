@@ -146,7 +146,7 @@ def test_noncausal_key_permutation_invariance(orc):
     np.testing.assert_allclose(l1, l2, atol=1e-13)
 
 
-@pytest.mark.parametrize("layout", [0, 1])
+@pytest.mark.parametrize("layout", [0, 1, 2])
 @pytest.mark.parametrize("N", [1, 2, 4, 8])
 @pytest.mark.parametrize("causal", [False, True])
 def test_blockwise_ring_recurrence_is_exact(orc, layout, N, causal):
@@ -234,7 +234,38 @@ def test_position_map_matches_printed_example(orc):
         np.testing.assert_array_equal(tok[shard, local], np.arange(8))
 
 
-@pytest.mark.parametrize("layout", [0, 1])
+def test_position_map_zigzag_matches_page_rule(orc):
+    with open(os.path.join(GOLDEN, "position_map_zigzag.txt")) as f:
+        cases = [line.split() for line in f if line.strip() and not line.startswith("#")]
+    assert cases
+    for S, N, *toks in cases:
+        S, N = int(S), int(N)
+        shard, local, tok = orc.position_map(2, S, N)
+        np.testing.assert_array_equal(tok, np.array([int(t) for t in toks], np.int32).reshape(N, -1))
+        np.testing.assert_array_equal(tok[shard, local], np.arange(S))
+
+
+def test_position_map_zigzag_balances_causal_work(orc):
+    # The page: zig-zag gives every device the same number of causal
+    # (query, key) pairs, N/2 full-block equivalents.  Under the inclusive
+    # rule a query at position t sees t + 1 keys; summed over the two
+    # half-blocks of C = L/2 tokens of device p this is N L^2 / 2 + L / 2 for
+    # every p (the L/2 is the diagonal's half of the elements).
+    for S, N in ((64, 4), (4096, 8), (1 << 14, 16)):
+        _, _, tok = orc.position_map(2, S, N)
+        L = S // N
+        work = (tok.astype(np.int64) + 1).sum(axis=1)
+        assert np.all(work == N * L * L // 2 + L // 2), (S, N, work)
+        _, _, tok_c = orc.position_map(0, S, N)
+        assert len(set((tok_c.astype(np.int64) + 1).sum(axis=1).tolist())) == N  # contiguous is not
+
+
+def test_position_map_zigzag_rejects_odd_half_blocks(orc):
+    with pytest.raises(ValueError):
+        orc.position_map(2, 12, 4)   # 12 tokens cannot form 8 equal half-blocks
+
+
+@pytest.mark.parametrize("layout", [0, 1, 2])
 def test_position_map_round_trip(orc, layout):
     S, N = 4096, 16
     shard, local, tok = orc.position_map(layout, S, N)
