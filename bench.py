@@ -201,8 +201,9 @@ def _time_ms(fn, reps=2):
 
 
 def layout_and_imbalance_report(w, q, k, v, dev):
-    """Forward of the same shape non-causal and with contiguous shards, and
-    the causal load-balance picture of the third page's section 6: time one
+    """Forward of the same shape non-causal, with contiguous shards and with
+    zig-zag shards, and the causal load-balance picture of the third page's
+    section 6 (and the first page's striped and zig-zag remedies): time one
     ra_block_step per (query shard i, ring step s), t(i, s), and form the
     makespan an N-device ring would see, T = sum_s max_i t(i, s), and its
     utilisation sum t / (N T)."""
@@ -210,7 +211,7 @@ def layout_and_imbalance_report(w, q, k, v, dev):
 
     from long_context_exact_gb300 import accounting
     from long_context_exact_gb300 import binding as ra
-    from long_context_exact_gb300.inputs import CONTIGUOUS, STRIPED
+    from long_context_exact_gb300.inputs import CONTIGUOUS, STRIPED, ZIGZAG
 
     out = torch.empty((w.b, w.S, w.h, w.d), dtype=torch.float32, device=dev)
     lse = torch.empty((w.b, w.h, w.S), dtype=torch.float32, device=dev)
@@ -219,7 +220,8 @@ def layout_and_imbalance_report(w, q, k, v, dev):
     f_c = accounting.fwd_useful_flops(w.b, w.S, w.h, w.d, True)
     for name, layout, causal, flops in (("noncausal", STRIPED, False, f_nc),
                                         ("causal_striped", STRIPED, True, f_c),
-                                        ("causal_contiguous", CONTIGUOUS, True, f_c)):
+                                        ("causal_contiguous", CONTIGUOUS, True, f_c),
+                                        ("causal_zigzag", ZIGZAG, True, f_c)):
         ms = _time_ms(lambda: ra.ring_attention(q, k, v, w.n_shards, layout, causal, out=out,
                                                 lse=lse))
         rep[name + "_fwd_ms"] = ms
@@ -229,7 +231,7 @@ def layout_and_imbalance_report(w, q, k, v, dev):
     del out, lse
     # per-(shard, step) block steps
     N, L = w.n_shards, w.S // w.n_shards
-    for name, layout in (("contiguous", CONTIGUOUS), ("striped", STRIPED)):
+    for name, layout in (("contiguous", CONTIGUOUS), ("striped", STRIPED), ("zigzag", ZIGZAG)):
         _, _, tok = ra.position_map(layout, w.S, N, device=dev)
         t = [[0.0] * N for _ in range(N)]
         for i in range(N):

@@ -70,7 +70,12 @@ typedef enum {
 
 typedef enum {
   RA_LAYOUT_CONTIGUOUS = 0,   /* shard p holds tokens [p*L, (p+1)*L) */
-  RA_LAYOUT_STRIPED = 1       /* shard p holds tokens p, p+N, p+2N, ... */
+  RA_LAYOUT_STRIPED = 1,      /* shard p holds tokens p, p+N, p+2N, ... */
+  RA_LAYOUT_ZIGZAG = 2        /* 2N half-blocks of C = L/2 tokens; shard p holds
+                                 half-block p (local rows [0, C)) and half-block
+                                 2N-1-p (rows [C, L)): the first page's "Zig-Zag
+                                 Ring Attention".  Needs S % (2N) == 0, and for
+                                 the attention calls C % 128 == 0. */
 } ra_layout;
 
 typedef struct {
@@ -122,7 +127,8 @@ ra_status ra_merge(const float *o_a, const float *lse_a, const float *o_b, const
  *   q [b, S, h, d] bf16, k, v [b, S, n_kv, d] bf16, in natural token order
  *   out [b, S, h, d] float, lse [b, h, S] float, in natural token order.
  * The layout only changes which tokens form a shard (and so the visit order
- * and the masked-tile pattern), never the result. */
+ * and the masked-tile pattern), never the result.  RA_ERR_UNSUPPORTED for a
+ * zig-zag layout whose half-blocks are not whole 128-token tiles. */
 ra_status ra_ring_attention(const uint16_t *q, const uint16_t *k, const uint16_t *v, float *out,
                             float *lse, int64_t S, int n_shards, ra_layout layout, int causal,
                             float scale, ra_dims dims, void *stream);
@@ -182,8 +188,8 @@ ra_status ra_ring_attention_bwd_noalloc(const uint16_t *q, const uint16_t *k, co
                                         void *stream);
 
 /* Token placement maps (the third page's section 6 example; "Striped
- * Attention" on the first page), computed on the device by the same functions
- * the attention kernels use:
+ * Attention" and "Zig-Zag Ring Attention" on the first page), computed on the
+ * device by the same functions the attention kernels use:
  *   shard_of[t], local_of[t] for t in [0, S);  token_of[p * L + r] inverse.
  * Any of the three device pointers may be NULL to skip that map. */
 ra_status ra_position_map(ra_layout layout, int64_t S, int n_shards, int32_t *shard_of,

@@ -6,7 +6,7 @@ draws the seeded synthetic workloads; ``accounting`` holds the useful-FLOP
 and byte formulas used for reporting.
 """
 
-from .inputs import CONTIGUOUS, STRIPED  # noqa: F401
+from .inputs import CONTIGUOUS, STRIPED, ZIGZAG  # noqa: F401
 
-__all__ = ["CONTIGUOUS", "STRIPED"]
+__all__ = ["CONTIGUOUS", "STRIPED", "ZIGZAG"]
 __version__ = "0.1.0"

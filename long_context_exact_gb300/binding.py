@@ -13,7 +13,7 @@ import threading
 
 import torch
 
-from .inputs import CONTIGUOUS, STRIPED  # noqa: F401  (re-exported layout ids)
+from .inputs import CONTIGUOUS, STRIPED, ZIGZAG  # noqa: F401  (re-exported layout ids)
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "libra.so")

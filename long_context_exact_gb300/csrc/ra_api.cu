@@ -59,6 +59,22 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
     if (!aligned16(p)) return fail(RA_ERR_INVALID_ARG, "%s is not 16-byte aligned", #p);  \
   } while (0)
 
+bool known_layout(int layout) {
+  return layout == RA_LAYOUT_CONTIGUOUS || layout == RA_LAYOUT_STRIPED ||
+         layout == RA_LAYOUT_ZIGZAG;
+}
+
+// Zig-zag shards are two half-blocks of S / 2N tokens each; the attention
+// kernels need every 128-row tile inside one half-block.
+ra_status check_zigzag_tiles(int layout, int64_t S, int n_shards) {
+  if (layout != RA_LAYOUT_ZIGZAG) return RA_OK;
+  if (S % (2LL * n_shards) != 0 || (S / (2LL * n_shards)) % kTile != 0)
+    return fail(RA_ERR_UNSUPPORTED,
+                "zig-zag needs half-blocks (S / 2N = %lld / %d) of whole %d-token tiles",
+                (long long)S, 2 * n_shards, kTile);
+  return RA_OK;
+}
+
 ra_status check_dims(const ra_dims &dm) {
   if (dm.b < 0 || dm.h <= 0 || dm.n_kv <= 0 || dm.d <= 0)
     return fail(RA_ERR_INVALID_ARG, "dims must be positive (b >= 0): b=%d h=%d n_kv=%d d=%d",
@@ -297,13 +313,13 @@ ra_status ra_ring_attention(const uint16_t *q, const uint16_t *k, const uint16_t
                             float scale, ra_dims dims, void *stream) {
   ra_status st;
   if ((st = check_dims(dims)) != RA_OK) return st;
-  if (layout != RA_LAYOUT_CONTIGUOUS && layout != RA_LAYOUT_STRIPED)
-    return fail(RA_ERR_INVALID_ARG, "unknown layout %d", (int)layout);
+  if (!known_layout(layout)) return fail(RA_ERR_INVALID_ARG, "unknown layout %d", (int)layout);
   if (S < 0) return fail(RA_ERR_INVALID_ARG, "negative S");
   if (n_shards < 1) return fail(RA_ERR_INVALID_ARG, "n_shards must be >= 1");
   if (S >= (1LL << 31)) return fail(RA_ERR_UNSUPPORTED, "S must be below 2^31");
   if (S % n_shards != 0)
     return fail(RA_ERR_UNSUPPORTED, "S=%lld is not a multiple of n_shards=%d", (long long)S, n_shards);
+  if ((st = check_zigzag_tiles(layout, S, n_shards)) != RA_OK) return st;
   if (S == 0 || dims.b == 0) return RA_OK;
   RA_CHECK_PTR(q);
   RA_CHECK_PTR(k);
@@ -348,13 +364,13 @@ ra_status ra_ring_attention_bwd(const uint16_t *q, const uint16_t *k, const uint
                                 int causal, float scale, ra_dims dims, void *stream) {
   ra_status st;
   if ((st = check_dims(dims)) != RA_OK) return st;
-  if (layout != RA_LAYOUT_CONTIGUOUS && layout != RA_LAYOUT_STRIPED)
-    return fail(RA_ERR_INVALID_ARG, "unknown layout %d", (int)layout);
+  if (!known_layout(layout)) return fail(RA_ERR_INVALID_ARG, "unknown layout %d", (int)layout);
   if (S < 0) return fail(RA_ERR_INVALID_ARG, "negative S");
   if (n_shards < 1) return fail(RA_ERR_INVALID_ARG, "n_shards must be >= 1");
   if (S >= (1LL << 31)) return fail(RA_ERR_UNSUPPORTED, "S must be below 2^31");
   if (S % n_shards != 0)
     return fail(RA_ERR_UNSUPPORTED, "S=%lld is not a multiple of n_shards=%d", (long long)S, n_shards);
+  if ((st = check_zigzag_tiles(layout, S, n_shards)) != RA_OK) return st;
   if (S == 0 || dims.b == 0) return RA_OK;
   RA_CHECK_PTR(q);
   RA_CHECK_PTR(k);
@@ -411,11 +427,12 @@ ra_status ra_ring_attention_bwd(const uint16_t *q, const uint16_t *k, const uint
 
 ra_status ra_position_map(ra_layout layout, int64_t S, int n_shards, int32_t *shard_of,
                           int32_t *local_of, int32_t *token_of, void *stream) {
-  if (layout != RA_LAYOUT_CONTIGUOUS && layout != RA_LAYOUT_STRIPED)
-    return fail(RA_ERR_INVALID_ARG, "unknown layout %d", (int)layout);
+  if (!known_layout(layout)) return fail(RA_ERR_INVALID_ARG, "unknown layout %d", (int)layout);
   if (S < 0 || n_shards < 1) return fail(RA_ERR_INVALID_ARG, "S >= 0 and n_shards >= 1 required");
   if (S >= (1LL << 31)) return fail(RA_ERR_UNSUPPORTED, "S must be below 2^31");
   if (S % n_shards != 0) return fail(RA_ERR_UNSUPPORTED, "S is not a multiple of n_shards");
+  if (layout == RA_LAYOUT_ZIGZAG && S % (2LL * n_shards) != 0)
+    return fail(RA_ERR_UNSUPPORTED, "zig-zag needs S to be a multiple of 2 * n_shards");
   if (S == 0) return RA_OK;
   cudaError_t e = counted(launch_position_map(layout, static_cast<int>(S), n_shards, shard_of,
                                               local_of, token_of, static_cast<cudaStream_t>(stream)));

@@ -153,12 +153,6 @@ __device__ __forceinline__ KvUnit decode_kv_unit(const BwdParams &p, long long u
   return x;
 }
 
-// First local row of query shard i whose token position is >= pos.
-__device__ __forceinline__ int first_row_at_or_after(const BwdParams &p, int i, int pos) {
-  if (p.layout == RA_LAYOUT_STRIPED) return -floordiv(i - pos, p.N);  // ceil((pos - i) / N)
-  return pos - i * p.L;
-}
-
 struct QIter {
   int s = -1, i = 0, a = 0, a_lo = 0, a_full = 0, hh = 0;
 };
@@ -189,10 +183,10 @@ __device__ __forceinline__ bool q_next(const BwdParams &p, const KvUnit &x, QIte
       it.a_full = 0;
     } else {
       // visible query tiles: those whose last row sees the tile's first key
-      const int r_vis = max(0, first_row_at_or_after(p, it.i, x.kmin));
+      const int r_vis = max(0, first_row_at_or_after(p.layout, p.L, p.N, it.i, x.kmin));
       it.a_lo = r_vis >= p.L ? p.n_qtiles : r_vis / kTile;
       // unmasked query tiles: every row sees the tile's last key
-      const int r_full = max(0, first_row_at_or_after(p, it.i, x.kmax));
+      const int r_full = max(0, first_row_at_or_after(p.layout, p.L, p.N, it.i, x.kmax));
       it.a_full = min(p.n_qtiles, (r_full + kTile - 1) / kTile);
     }
     it.a = p.n_qtiles - 1;
@@ -205,16 +199,6 @@ __device__ __forceinline__ bool q_next(const BwdParams &p, const KvUnit &x, QIte
   split = p.causal ? (token_at(p.layout, p.L, p.N, it.i, it.a * kTile) + 1 < kSplitKeys)
                    : (p.S < kSplitKeys);
   return true;
-}
-
-__device__ __forceinline__ void shard_coords_b(int layout, int p, int r, int &c2, int &c3) {
-  if (layout == RA_LAYOUT_STRIPED) {
-    c2 = p;
-    c3 = r;
-  } else {
-    c2 = r;
-    c3 = p;
-  }
 }
 
 // D = A B^T style: both operands K-major 128 x D tiles (M = N = 128).
@@ -347,7 +331,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         prefetch_tmap(&vmap);
         prefetch_tmap(&domap);
         int c2, c3;
-        shard_coords_b(p.layout, x.j, x.c * kTile, c2, c3);
+        map_coords(p.layout, p.L, p.N, x.j, x.c * kTile, c2, c3);
         mbar_arrive_expect_tx(&bars[C::bKV], 2 * C::kTileBytes);
 #pragma unroll
         for (int hf = 0; hf < C::kHalves; ++hf) {
@@ -363,7 +347,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       while (q_next(p, x, it, i, a, hq, partial, split)) {
         if (lane == 0) {
           int c2, c3;
-          shard_coords_b(p.layout, i, a * kTile, c2, c3);
+          map_coords(p.layout, p.L, p.N, i, a * kTile, c2, c3);
           const int st = n % C::kQSt;
           const uint32_t ph = (n / C::kQSt) & 1;
           bool go = mbar_wait(&bars[C::bQEmpty + st], ph ^ 1, abort_flag, kSiteBProdQ);
@@ -531,7 +515,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       const float4 *d4 = lse4 + kTile / 4;
       // query columns cb + c with c < c0 are masked for this key
       int c0 = 0;
-      if (partial) c0 = first_row_at_or_after(p, i, kp) - a * kTile - cb;
+      if (partial) c0 = first_row_at_or_after(p.layout, p.L, p.N, i, kp) - a * kTile - cb;
       if (!key_exists) {
         c0 = C::kHalfCols;
         partial = true;
@@ -660,7 +644,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         // the staging buffer is free: this step's dS_lo^T readers finished
         // before dQ was committed, and the previous round's read completed.
         int c2, c3;
-        shard_coords_b(p.layout, i, a * kTile + (warp & 3) * 32, c2, c3);
+        map_coords(p.layout, p.L, p.N, i, a * kTile + (warp & 3) * 32, c2, c3);
 #pragma unroll
         for (int round = 0; round < 2; ++round) {
           uint32_t r[2][32];

@@ -259,18 +259,6 @@ __device__ __forceinline__ bool kv_next(const FwdParams &p, const Unit &x, KvIte
   }
 }
 
-// (c2, c3) tensor-map coordinates of local row r of shard p: striped maps are
-// (.., shard, row, ..), contiguous ones (.., row, shard, ..).
-__device__ __forceinline__ void shard_coords(int layout, int p, int r, int &c2, int &c3) {
-  if (layout == RA_LAYOUT_STRIPED) {
-    c2 = p;
-    c3 = r;
-  } else {
-    c2 = r;
-    c3 = p;
-  }
-}
-
 template <int D>
 __device__ __forceinline__ void issue_s_mma(uint32_t tS, uint32_t q_saddr, uint32_t k_saddr,
                                             uint32_t idesc) {
@@ -383,7 +371,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::kThreads, 1)
       prefetch_tmap(&kmap);
       prefetch_tmap(&vmap);
       mbar_arrive_expect_tx(&bars[C::bQFull], NQ * C::kTileBytes);
-      shard_coords(p.layout, x.i, x.a * kTile, c2, c3);
+      map_coords(p.layout, p.L, p.N, x.i, x.a * kTile, c2, c3);
 #pragma unroll
       for (int t = 0; t < NQ; ++t) {
         const int hq = x.kh * p.g + x.pr * NQ + t;
@@ -401,7 +389,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::kThreads, 1)
     bool partial;
     while (kv_next<kBlock>(p, x, it, j, c, partial)) {
       if (lane == 0) {
-        shard_coords(p.layout, j, c * kTile, c2, c3);
+        map_coords(p.layout, p.L, p.N, j, c * kTile, c2, c3);
         const int ks = n % C::kKSt;
         const uint32_t kph = (n / C::kKSt) & 1;
         if (mbar_wait(&bars[C::bKEmpty + ks], kph ^ 1, abort_flag, kSiteProdK)) {

@@ -26,8 +26,17 @@ constexpr int kSplitKeys = 4096;
 // Token held at local row r of shard p.  Contiguous: shard p holds
 // [p*L, (p+1)*L).  Striped: token t lives on shard t mod N at row t div N
 // (the first page's "Striped Attention"; the third page's section 6 example).
+// Zig-zag (the first page's "Zig-Zag Ring Attention"): 2N half-blocks of
+// C = L/2 tokens, shard p holding half-block p at rows [0, C) and half-block
+// 2N-1-p at rows [C, L).  Under every layout a shard's tokens increase with
+// the local row, so the keys of a shard that a query sees form a prefix.
 __host__ __device__ __forceinline__ int token_at(int layout, int L, int N, int p, int r) {
-  return layout == RA_LAYOUT_STRIPED ? r * N + p : p * L + r;
+  if (layout == RA_LAYOUT_STRIPED) return r * N + p;
+  if (layout == RA_LAYOUT_ZIGZAG) {
+    const int C = L >> 1;
+    return r < C ? p * C + r : (2 * N - 1 - p) * C + (r - C);
+  }
+  return p * L + r;
 }
 
 // Key/value shard that query shard i meets at ring step s: (i - s) mod N
@@ -43,9 +52,51 @@ __host__ __device__ __forceinline__ int floordiv(int a, int b) {  // b > 0
 }
 
 // Largest local key row of shard j visible to a query at position qp, under
-// the inclusive causal rule (key position <= query position); may be < 0.
+// the inclusive causal rule (key position <= query position); may be < 0
+// (nothing visible) or >= L (the whole shard).
 __host__ __device__ __forceinline__ int last_visible_row(int layout, int L, int N, int j, int qp) {
-  return layout == RA_LAYOUT_STRIPED ? floordiv(qp - j, N) : qp - j * L;
+  if (layout == RA_LAYOUT_STRIPED) return floordiv(qp - j, N);
+  if (layout == RA_LAYOUT_ZIGZAG) {
+    const int C = L >> 1;
+    const int early = j * C, late = (2 * N - 1 - j) * C;
+    if (qp < early + C) return qp - early;
+    return qp < late ? C - 1 : C + (qp - late);
+  }
+  return qp - j * L;
+}
+
+// First local row of shard i whose token is >= pos; <= 0 when every row is,
+// >= L when none is.
+__host__ __device__ __forceinline__ int first_row_at_or_after(int layout, int L, int N, int i,
+                                                              int pos) {
+  if (layout == RA_LAYOUT_STRIPED) return -floordiv(i - pos, N);  // ceil((pos - i) / N)
+  if (layout == RA_LAYOUT_ZIGZAG) {
+    const int C = L >> 1;
+    const int early = i * C, late = (2 * N - 1 - i) * C;
+    if (pos < early + C) return pos - early;
+    return pos <= late ? C : C + (pos - late);
+  }
+  return pos - i * L;
+}
+
+// Coordinates (c2, c3) of local row r of shard p in the 5-D tensor-map view
+// of a [b, S, heads, d] tensor: striped maps are (x, head, shard, row, batch),
+// the others (x, head, row, shard, batch) over contiguous blocks of L tokens.
+// A zig-zag row is addressed through its token in the contiguous view (a
+// tile never straddles a half-block, so its rows stay consecutive tokens).
+__host__ __device__ __forceinline__ void map_coords(int layout, int L, int N, int p, int r,
+                                                    int &c2, int &c3) {
+  if (layout == RA_LAYOUT_STRIPED) {
+    c2 = p;
+    c3 = r;
+  } else if (layout == RA_LAYOUT_ZIGZAG) {
+    const int t = token_at(layout, L, N, p, r);
+    c2 = t % L;
+    c3 = t / L;
+  } else {
+    c2 = r;
+    c3 = p;
+  }
 }
 
 // ------------------------------------------------------------ parameters

@@ -59,30 +59,28 @@ ra_status ra_ring_attention_bwd_noalloc(const uint16_t *q, const uint16_t *k, co
                                         float *dq, float *dk, float *dv, int64_t S, int n_shards,
                                         ra_layout layout, int causal, float scale, ra_dims dims,
                                         void *stream) {
+  // Validate exactly as the ordinary entry point does: called without a
+  // workspace it checks every argument and launches nothing, answering
+  // RA_ERR_WORKSPACE when the arguments are good (RA_OK for an empty problem).
+  const ra_status st = ra_ring_attention_bwd(q, k, v, out, lse, dout, dq, dk, dv, nullptr, 0, S,
+                                             n_shards, layout, causal, scale, dims, stream);
+  if (st != RA_ERR_WORKSPACE) return st;
   const size_t need = ra_bwd_workspace_size(S, n_shards, dims);
-  if (need > ra::kNoAllocScratchBytes) {
-    // Malformed arguments are reported as the ordinary entry point reports
-    // them (it validates before it needs a workspace, and launches nothing).
-    const ra_status st = ra_ring_attention_bwd(q, k, v, out, lse, dout, dq, dk, dv, nullptr, 0,
-                                               S, n_shards, layout, causal, scale, dims, stream);
-    if (st != RA_ERR_WORKSPACE) return st;
+  if (need > ra::kNoAllocScratchBytes)
     return ra::report_error(RA_ERR_WORKSPACE,
                             "the allocation-free backward holds %zu bytes of scratch; this "
                             "problem needs %zu (b * h * n_shards * rows per shard rounded up "
                             "to 128, times 8 bytes)",
                             ra::kNoAllocScratchBytes, need);
-  }
   void *scratch = nullptr;
-  if (need > 0) {
-    cudaError_t e = ra::scratch_for_current_device(&scratch);
-    if (e != cudaSuccess)
-      return ra::report_error(RA_ERR_CUDA, "scratch address lookup: %s", cudaGetErrorString(e));
-  }
+  cudaError_t e = ra::scratch_for_current_device(&scratch);
+  if (e != cudaSuccess)
+    return ra::report_error(RA_ERR_CUDA, "scratch address lookup: %s", cudaGetErrorString(e));
   // The scratch needs no clearing: the pre-pass writes every word the main
   // kernel reads before it runs (and dq is cleared on the stream as usual).
-  return ra_ring_attention_bwd(q, k, v, out, lse, dout, dq, dk, dv,
-                               need > 0 ? scratch : nullptr, need > 0 ? ra::kNoAllocScratchBytes : 0,
-                               S, n_shards, layout, causal, scale, dims, stream);
+  return ra_ring_attention_bwd(q, k, v, out, lse, dout, dq, dk, dv, scratch,
+                               ra::kNoAllocScratchBytes, S, n_shards, layout, causal, scale, dims,
+                               stream);
 }
 
 }  // extern "C"

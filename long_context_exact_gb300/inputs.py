@@ -21,6 +21,7 @@ import torch
 
 CONTIGUOUS = 0
 STRIPED = 1
+ZIGZAG = 2
 
 
 @dataclass(frozen=True)

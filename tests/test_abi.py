@@ -110,6 +110,23 @@ def test_map_and_order_validation(lib):
     assert lib.ra_selftest_wait_timeout(0, None) == binding.RA_ERR_INVALID_ARG
 
 
+def test_zigzag_shape_validation(lib):
+    d = _dims()
+    # half-blocks must be whole 128-token tiles for the attention calls
+    assert lib.ra_ring_attention(FAKE, FAKE, FAKE, FAKE, FAKE, 1024, 8, 2, 1, 0.0, d, None) == \
+        binding.RA_ERR_UNSUPPORTED                      # S / 2N = 64
+    assert "zig-zag" in lib.ra_last_error().decode()
+    assert lib.ra_ring_attention(FAKE, FAKE, FAKE, FAKE, FAKE, 1536, 4, 2, 1, 0.0, d, None) == \
+        binding.RA_ERR_UNSUPPORTED                      # S / 2N = 192
+    assert lib.ra_ring_attention_bwd(*([FAKE] * 9), FAKE, 1 << 30, 1024, 8, 2, 1, 0.0, d,
+                                     None) == binding.RA_ERR_UNSUPPORTED
+    assert lib.ra_ring_attention_bwd_noalloc(*([FAKE] * 9), 1024, 8, 2, 1, 0.0, d,
+                                             None) == binding.RA_ERR_UNSUPPORTED
+    # the maps only need an even split into 2N half-blocks
+    assert lib.ra_position_map(2, 12, 4, FAKE, FAKE, FAKE, None) == binding.RA_ERR_UNSUPPORTED
+    assert lib.ra_position_map(3, 16, 4, FAKE, FAKE, FAKE, None) == binding.RA_ERR_INVALID_ARG
+
+
 def test_workspace_size(lib):
     lib.ra_bwd_workspace_size.argtypes = [ctypes.c_int64, ctypes.c_int, binding.Dims]
     n = lib.ra_bwd_workspace_size(65536, 16, _dims(b=2, h=32, n_kv=8))

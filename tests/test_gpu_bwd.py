@@ -11,8 +11,8 @@ import pytest
 import torch
 
 from long_context_exact_gb300 import binding as ra
-from long_context_exact_gb300.inputs import (CONTIGUOUS, STRIPED, WORKLOADS, make_inputs,
-                                             sample_rows, workload_inputs)
+from long_context_exact_gb300.inputs import (CONTIGUOUS, STRIPED, WORKLOADS, ZIGZAG,
+                                             make_inputs, sample_rows, workload_inputs)
 
 pytestmark = pytest.mark.gpu
 
@@ -53,6 +53,10 @@ CASES = [
     (1, 384, 3, 1, 64, 2, STRIPED, True),         # d = 64, g = 3
     (1, 200, 4, 1, 128, 1, CONTIGUOUS, True),     # one ragged shard
     (1, 1, 2, 1, 128, 1, CONTIGUOUS, True),       # a single token
+    (1, 1024, 4, 2, 128, 4, ZIGZAG, True),        # zig-zag: half-blocks of one tile
+    (1, 2048, 8, 2, 128, 8, ZIGZAG, True),
+    (1, 1024, 3, 1, 64, 2, ZIGZAG, True),         # d = 64, g = 3
+    (1, 512, 4, 2, 128, 2, ZIGZAG, False),
 ]
 
 
@@ -74,14 +78,16 @@ def test_backward_custom_scale(orc):
 
 
 def test_backward_layouts_agree_and_sum_invariants():
-    """Contiguous and striped give the same gradients; sum_j dK_j = 0 and
+    """Contiguous, striped and zig-zag give the same gradients; sum_j dK_j = 0 and
     sum_j dV_j = sum of dO over the group's query heads (per KV head)."""
     b, S, h, n_kv, d, N = 1, 4096, 8, 2, 128, 8
     q, k, v, do = make_inputs(b, S, h, n_kv, d, seed=11, with_dout=True)
     gc = _run(q, k, v, do, N, CONTIGUOUS, True)
     gs = _run(q, k, v, do, N, STRIPED, True)
-    for a, c in zip(gc, gs):
+    gz = _run(q, k, v, do, N, ZIGZAG, True)
+    for a, c, z in zip(gc, gs, gz):
         assert _err(a, c) <= G_TOL
+        assert _err(a, z) <= G_TOL
     dk, dv = gs[1], gs[2]
     assert np.abs(dk.sum(1)).max() <= 5e-2
     gd = do.double().numpy().reshape(b, S, n_kv, h // n_kv, d).sum(axis=(1, 3))

@@ -10,8 +10,8 @@ import pytest
 import torch
 
 from long_context_exact_gb300 import binding as ra
-from long_context_exact_gb300.inputs import (CONTIGUOUS, STRIPED, WORKLOADS, make_inputs,
-                                             sample_rows, workload_inputs)
+from long_context_exact_gb300.inputs import (CONTIGUOUS, STRIPED, WORKLOADS, ZIGZAG,
+                                             make_inputs, sample_rows, workload_inputs)
 
 pytestmark = pytest.mark.gpu
 
@@ -48,7 +48,7 @@ def _cmp(out, lse, ref_out, ref_lse, rows=None):
 
 
 # ------------------------------------------------------------------ maps
-@pytest.mark.parametrize("layout", [CONTIGUOUS, STRIPED])
+@pytest.mark.parametrize("layout", [CONTIGUOUS, STRIPED, ZIGZAG])
 @pytest.mark.parametrize("S,N", [(8, 4), (1024, 4), (65536, 8), (65536, 16), (3 * 200, 3)])
 def test_position_map_bit_exact(orc, layout, S, N):
     shard, local, tok = ra.position_map(layout, S, N)
@@ -78,6 +78,11 @@ SMALL = [
     (1, 300, 4, 1, 128, 1, CONTIGUOUS, True),      # N = 1, ragged single shard
     (1, 64, 8, 2, 128, 1, STRIPED, True),          # shorter than one tile
     (1, 1, 2, 1, 64, 1, CONTIGUOUS, True),         # a single token
+    (1, 1024, 8, 2, 128, 4, ZIGZAG, True),         # zig-zag: half-blocks of one tile
+    (2, 2048, 8, 2, 128, 8, ZIGZAG, True),
+    (1, 2048, 4, 4, 64, 2, ZIGZAG, True),          # g = 1, d = 64, four-tile half-blocks
+    (1, 1536, 6, 2, 64, 2, ZIGZAG, False),         # g = 3 (odd), non-causal
+    (1, 256, 4, 1, 128, 1, ZIGZAG, True),          # N = 1: one shard, two half-blocks
 ]
 
 
@@ -94,11 +99,13 @@ def test_layouts_agree_and_results_are_deterministic():
     q, k, v = _dev(*make_inputs(1, 4096, 8, 2, 128, seed=5))
     oc, lc = ra.ring_attention(q, k, v, 8, CONTIGUOUS, True)
     os_, ls_ = ra.ring_attention(q, k, v, 8, STRIPED, True)
+    oz, lz = ra.ring_attention(q, k, v, 8, ZIGZAG, True)
     ra.stream_check()
     # each path is within O_TOL of the exact result; P is rounded to bf16 on
-    # both, in different accumulation orders
-    assert (oc - os_).abs().max().item() < O_TOL
-    assert (lc - ls_).abs().max().item() < 1e-4
+    # all, in different accumulation orders
+    for o_, l_ in ((os_, ls_), (oz, lz)):
+        assert (oc - o_).abs().max().item() < O_TOL
+        assert (lc - l_).abs().max().item() < 1e-4
     o2, l2 = ra.ring_attention(q, k, v, 8, STRIPED, True)
     assert torch.equal(o2, os_) and torch.equal(l2, ls_)
 
@@ -153,13 +160,14 @@ def test_block_step_matches_oracle_update(orc, Lq, Lk, causal, g, d):
     _cmp(out, lse, r_out, r_lse)
 
 
-def test_block_steps_over_ring_reproduce_full_attention(orc):
+@pytest.mark.parametrize("layout", [CONTIGUOUS, STRIPED, ZIGZAG])
+def test_block_steps_over_ring_reproduce_full_attention(orc, layout):
     """ra_block_step over the N shards in ring order, then ra_finalize,
     equals the direct definition (the pages' exactness claim)."""
     b, S, h, n_kv, d, N = 1, 1024, 8, 2, 128, 4
     q, k, v = make_inputs(b, S, h, n_kv, d, seed=99)
     ref_o, ref_l = orc.attn_fwd_rows(q, k, v, True)
-    _, _, tok = orc.position_map(STRIPED, S, N)
+    _, _, tok = orc.position_map(layout, S, N)
     order = orc.ring_order(N)
     out = torch.empty((b, S, h, d), dtype=torch.float32)
     lse = torch.empty((b, h, S), dtype=torch.float32)
@@ -247,6 +255,10 @@ def test_workload_noncausal_32k(orc):
 
 def test_workload_causal_64k_both_layouts(orc):
     _workload_parity(orc, "causal64k")
+
+
+def test_workload_causal_64k_zigzag(orc):
+    _workload_parity(orc, "causal64k", layouts=(ZIGZAG,))
 
 
 def test_workload_causal_256k_striped(orc):
