@@ -263,6 +263,64 @@ def layout_and_imbalance_report(w, q, k, v, dev):
     return rep
 
 
+def exp2_roof_report(w, dev, clk):
+    """The forward's second roof: the measured exp2 rate of the special-
+    function units (ra_ex2_probe) turned into the useful TFLOP/s it allows.
+    Every attended (query, key) element costs one exp2 and 4 d useful FLOPs
+    forward; the backward recomputes one exp2 per element for 10 d FLOPs."""
+    import torch
+
+    from long_context_exact_gb300 import binding as ra
+
+    iters = 2048
+    sink, n = ra.ex2_probe(iters)
+    best = _time_ms(lambda: ra.ex2_probe(iters, sink), reps=3)
+    ra.stream_check()
+    rate = n / (best / 1e3)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    mhz = (clk or {}).get("sm_mhz")
+    return {"exp2_per_s": rate, "ms": best, "exp2_evaluated": n,
+            "per_sm_per_clk": rate / sms / (mhz * 1e6) if mhz else None,
+            "clock_note": "per-clock figure uses the median SM clock of the timed region",
+            "fwd_roof_tflops": rate * 4 * w.d / 1e12,
+            "bwd_roof_tflops": rate * 10 * w.d / 1e12}
+
+
+def hbm_kernel_report(w, dev, peaks):
+    """Achieved HBM bandwidth of the memory-bound kernels on one shard's rows
+    (what a ring step of the block path finalizes or merges): ra_finalize
+    reads and rewrites O and reads l, m, writing LSE; ra_merge reads two
+    (O, LSE) pairs and writes one."""
+    import torch
+
+    from long_context_exact_gb300 import binding as ra
+
+    L = w.S // w.n_shards
+    gen = torch.Generator(device=dev).manual_seed(7)
+    shape = (w.b, L, w.h, w.d)
+    o_a = torch.randn(shape, generator=gen, device=dev)
+    o_b = torch.randn(shape, generator=gen, device=dev)
+    o_c = torch.randn(shape, generator=gen, device=dev)
+    lse_a = torch.randn((w.b, w.h, L), generator=gen, device=dev)
+    lse_b = torch.randn((w.b, w.h, L), generator=gen, device=dev)
+    lse_c = torch.empty_like(lse_a)
+    m = torch.randn((w.b, w.h, L), generator=gen, device=dev)
+    l = 1.0 + torch.rand((w.b, w.h, L), generator=gen, device=dev)
+    o_bytes = o_a.numel() * 4
+    row_bytes = lse_a.numel() * 4
+    out = {}
+    fin_ms = _time_ms(lambda: ra.finalize((m, l, o_c), lse=lse_c), reps=3)
+    mrg_ms = _time_ms(lambda: ra.merge(o_a, lse_a, o_b, lse_b, o=o_c, lse=lse_c), reps=3)
+    ra.stream_check()
+    for name, ms, nbytes in (("finalize", fin_ms, 2 * o_bytes + 3 * row_bytes),
+                             ("merge", mrg_ms, 3 * o_bytes + 3 * row_bytes)):
+        gbs = nbytes / (ms / 1e3) / 1e9
+        out[name] = {"ms": ms, "bytes": nbytes, "gbs": gbs, "frac_of_hbm_peak": gbs / peaks["hbm_gbs"],
+                     "rows": f"b={w.b} x L={L} x h={w.h}, d={w.d}"}
+    del o_a, o_b, o_c
+    return out
+
+
 # ---------------------------------------------------------------- our arm
 def run_ours(a, rank, world, local_rank):
     import torch
@@ -435,6 +493,8 @@ def run_ours(a, rank, world, local_rank):
     extras = None
     if rank == 0 and not a.no_extras:
         extras = layout_and_imbalance_report(w, q, k, v, dev)
+        extras["exp2_roof"] = exp2_roof_report(w, dev, clk)
+        extras["hbm_kernels"] = hbm_kernel_report(w, dev, peaks)
 
     cpu = None
     if rank == 0 and world == 1 and not a.no_cpu_baseline:
@@ -453,7 +513,7 @@ def run_ours(a, rank, world, local_rank):
             "data": "synthetic",
             "config": {"workload": w.name, "b": w.b, "S": w.S, "h": w.h, "n_kv": w.n_kv,
                        "d": w.d, "n_shards": w.n_shards,
-                       "layout": "striped" if layout == STRIPED else "contiguous",
+                       "layout": {0: "contiguous", 1: "striped", 2: "zigzag"}[layout],
                        "causal": w.causal, "backward": have_bwd,
                        "l2": "inputs larger than L2 (Q alone is "
                              f"{q.numel() * 2 / 1e9:.2f} GB); no flush",

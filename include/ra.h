@@ -205,6 +205,17 @@ ra_status ra_ring_order(int n_shards, int32_t *order, void *stream);
  * check, RA_ERR_CUDA on a CUDA error, RA_OK otherwise. */
 ra_status ra_stream_check(void *stream);
 
+/* Measurement probe for the second roof of the forward: the exp2 rate of
+ * the special-function units (every attention element needs one exp2 beside
+ * its two multiply-adds on the tensor cores).  Launches
+ * ra_ex2_probe_threads() threads, 4 CTAs of 256 per SM, each evaluating
+ * 8 * iters dependent-chain exp2 (ex2.approx) and writing one float to
+ * sink[thread]; the caller times the launch.  iters in 1 .. 2^24;
+ * sink_floats must be at least ra_ex2_probe_threads().  The pages have no
+ * counterpart to this call; it supports the roofline report only. */
+ra_status ra_ex2_probe(int64_t iters, float *sink, int64_t sink_floats, void *stream);
+int64_t ra_ex2_probe_threads(void);
+
 /* Failure-detection self test: launches one CTA that waits on an mbarrier
  * nothing will ever arrive on, with a wait budget of `budget_cycles` SM
  * clocks (1 .. 2^31).  The wait runs out, the kernel records a timeout and

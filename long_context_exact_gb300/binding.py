@@ -80,6 +80,10 @@ def load(path: str | None = None):
         lib.ra_last_error.restype = ctypes.c_char_p
         lib.ra_version.argtypes = []
         lib.ra_version.restype = I
+        lib.ra_ex2_probe.argtypes = [I64, P, I64, P]
+        lib.ra_ex2_probe.restype = I
+        lib.ra_ex2_probe_threads.argtypes = []
+        lib.ra_ex2_probe_threads.restype = I64
         lib.ra_launch_count.argtypes = []
         lib.ra_launch_count.restype = ctypes.c_uint64
         _lib = lib
@@ -273,6 +277,17 @@ def stream_check(stream=None):
 def launch_count() -> int:
     """Kernels the library has launched in this process."""
     return int(load().ra_launch_count())
+
+
+def ex2_probe(iters: int, sink=None, stream=None):
+    """Launch the exp2-rate probe; returns (sink tensor, exp2 evaluated).
+    The caller brackets the call with CUDA events."""
+    lib = load()
+    n = int(lib.ra_ex2_probe_threads())
+    if sink is None:
+        sink = torch.empty(n, dtype=torch.float32, device="cuda")
+    _check(lib.ra_ex2_probe(iters, _ptr(sink), sink.numel(), _stream(stream)))
+    return sink, 8 * iters * n
 
 
 def selftest_wait_timeout(budget_cycles: int, stream=None):

@@ -465,6 +465,21 @@ ra_status ra_stream_check(void *stream) {
   return RA_OK;
 }
 
+ra_status ra_ex2_probe(int64_t iters, float *sink, int64_t sink_floats, void *stream) {
+  if (iters < 1 || iters > (1LL << 24)) return fail(RA_ERR_INVALID_ARG, "iters out of range");
+  RA_CHECK_PTR(sink);
+  const int threads = 256;
+  const long long blocks = static_cast<long long>(sm_count()) * 4;
+  if (sink_floats < blocks * threads)
+    return fail(RA_ERR_INVALID_ARG, "sink holds %lld floats, %lld needed", (long long)sink_floats,
+                blocks * threads);
+  cudaError_t e = counted(launch_ex2_probe(iters, sink, static_cast<int>(blocks), threads,
+                                           static_cast<cudaStream_t>(stream)));
+  return e == cudaSuccess ? RA_OK : cuda_fail(e, "ex2 probe launch");
+}
+
+int64_t ra_ex2_probe_threads(void) { return static_cast<int64_t>(sm_count()) * 4 * 256; }
+
 ra_status ra_selftest_wait_timeout(long long budget_cycles, void *stream) {
   if (budget_cycles < 1 || budget_cycles > (1LL << 31))
     return fail(RA_ERR_INVALID_ARG, "budget_cycles out of range");

@@ -160,6 +160,8 @@ cudaError_t launch_position_map(int layout, int S, int N, int32_t *shard_of, int
                                 int32_t *token_of, cudaStream_t stream);
 cudaError_t launch_ring_order(int N, int32_t *order, cudaStream_t stream);
 cudaError_t launch_wait_timeout_selftest(long long budget, cudaStream_t stream);
+cudaError_t launch_ex2_probe(long long iters, float *sink, int blocks, int threads,
+                             cudaStream_t stream);
 // Record a message for ra_last_error() on this thread and return `st`.
 ra_status report_error(ra_status st, const char *fmt, ...) __attribute__((format(printf, 2, 3)));
 

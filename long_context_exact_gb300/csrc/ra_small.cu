@@ -133,6 +133,25 @@ __global__ void wait_timeout_selftest_kernel(long long budget) {
   }
 }
 
+// Throughput probe for the exp2 unit: each thread runs eight independent
+// chains x <- 2^(-x) (values stay in [1/2, 1]), so the SFU pipes, not
+// latency, bound it.  The chains' sum is written so nothing is elided.
+__global__ void ex2_probe_kernel(long long iters, float *sink) {
+  float x0 = 0.1f, x1 = 0.2f, x2 = 0.3f, x3 = 0.4f, x4 = 0.5f, x5 = 0.6f, x6 = 0.7f, x7 = 0.8f;
+  for (long long i = 0; i < iters; ++i) {
+    x0 = ex2(-x0);
+    x1 = ex2(-x1);
+    x2 = ex2(-x2);
+    x3 = ex2(-x3);
+    x4 = ex2(-x4);
+    x5 = ex2(-x5);
+    x6 = ex2(-x6);
+    x7 = ex2(-x7);
+  }
+  sink[static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x] =
+      x0 + x1 + x2 + x3 + x4 + x5 + x6 + x7;
+}
+
 }  // namespace
 
 cudaError_t launch_finalize(float *o, const float *l, const float *m, float *lse, int b,
@@ -164,6 +183,12 @@ cudaError_t launch_position_map(int layout, int S, int N, int32_t *shard_of, int
 cudaError_t launch_ring_order(int N, int32_t *order, cudaStream_t stream) {
   const int n = N * N;
   ring_order_kernel<<<(n + kEwThreads - 1) / kEwThreads, kEwThreads, 0, stream>>>(N, order);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_ex2_probe(long long iters, float *sink, int blocks, int threads,
+                             cudaStream_t stream) {
+  ex2_probe_kernel<<<blocks, threads, 0, stream>>>(iters, sink);
   return cudaGetLastError();
 }
 

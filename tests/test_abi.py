@@ -127,6 +127,14 @@ def test_zigzag_shape_validation(lib):
     assert lib.ra_position_map(3, 16, 4, FAKE, FAKE, FAKE, None) == binding.RA_ERR_INVALID_ARG
 
 
+def test_ex2_probe_validation(lib):
+    n = lib.ra_ex2_probe_threads()
+    assert n > 0 and n % 256 == 0
+    assert lib.ra_ex2_probe(0, FAKE, n, None) == binding.RA_ERR_INVALID_ARG
+    assert lib.ra_ex2_probe(16, None, n, None) == binding.RA_ERR_INVALID_ARG
+    assert lib.ra_ex2_probe(16, FAKE, n - 1, None) == binding.RA_ERR_INVALID_ARG
+
+
 def test_workspace_size(lib):
     lib.ra_bwd_workspace_size.argtypes = [ctypes.c_int64, ctypes.c_int, binding.Dims]
     n = lib.ra_bwd_workspace_size(65536, 16, _dims(b=2, h=32, n_kv=8))
