@@ -51,6 +51,28 @@ def _args():
     return ap.parse_args()
 
 
+def max_over_ranks(ms: float, world: int, device) -> float:
+    """The slowest rank's time: every rank contributes its own measurement and
+    all of them receive the maximum (a no-op for one rank)."""
+    if world <= 1:
+        return ms
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(step_flops: float, steps: int, world: int, ms: float) -> float:
+    """Whole-job useful TFLOP/s: every rank runs `steps` steps of its own
+    replica; the job takes as long as the slowest rank."""
+    return step_flops * steps * world / (ms / 1e3) / 1e12
+
+
+def replica_seed(seed: int, rank: int) -> int:
+    """Seed of rank `rank`'s replica inputs (independent batches per rank)."""
+    return seed + 1000 * rank
+
+
 def _peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -340,7 +362,7 @@ def run_ours(a, rank, world, local_rank):
         torch.distributed.barrier()
     ra.load()
 
-    gen = torch.Generator(device=dev).manual_seed(w.seed + 1000 * rank)
+    gen = torch.Generator(device=dev).manual_seed(replica_seed(w.seed, rank))
 
     def rnd(*shape):
         x = torch.randn(shape, generator=gen, device=dev, dtype=torch.float32)
@@ -411,15 +433,12 @@ def run_ours(a, rank, world, local_rank):
     clk = clocks.stop()
     ra.stream_check()
     elapsed_ms = t_start.elapsed_time(t_end)
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(elapsed_ms, world, dev)
 
     f_fwd = accounting.fwd_useful_flops(w.b, w.S, w.h, w.d, w.causal)
     f_bwd = accounting.bwd_useful_flops(w.b, w.S, w.h, w.d, w.causal) if have_bwd else 0.0
     step_flops = f_fwd + f_bwd
-    value = step_flops * a.steps * world / (elapsed_ms / 1e3) / 1e12
+    value = job_rate(step_flops, a.steps, world, elapsed_ms)
     fwd_ms = statistics.mean(e0.elapsed_time(e1) for e0, e1, _ in ev)
     bwd_ms = statistics.mean(e1.elapsed_time(e2) for _, e1, e2 in ev) if have_bwd else 0.0
     peaks = _peaks()
@@ -482,11 +501,8 @@ def run_ours(a, rank, world, local_rank):
         torch.cuda.synchronize()
         ra.stream_check()
         e2e_ms = s0.elapsed_time(s1)
-        if world > 1:
-            t = torch.tensor([e2e_ms], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            e2e_ms = float(t.item())
-        e2e = {"value": step_flops * a.steps * world / (e2e_ms / 1e3) / 1e12, "unit": "TFLOP/s",
+        e2e_ms = max_over_ranks(e2e_ms, world, dev)
+        e2e = {"value": job_rate(step_flops, a.steps, world, e2e_ms), "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": e2e_ms / a.steps}
 
