@@ -410,18 +410,27 @@ ra_status ra_ring_attention_bwd(const uint16_t *q, const uint16_t *k, const uint
   p.dq = dq;
   p.dk = dk;
   p.dv = dv;
-  CUtensorMap qm, km, vm, dom, dqm;
+  CUtensorMap qm, km, vm, dom, dqm, dkm, dvm;
   if ((st = make_map(&qm, q, layout, dims.b, n_shards, p.L, dims.h, dims.d)) != RA_OK) return st;
   if ((st = make_map(&km, k, layout, dims.b, n_shards, p.L, dims.n_kv, dims.d)) != RA_OK) return st;
   if ((st = make_map(&vm, v, layout, dims.b, n_shards, p.L, dims.n_kv, dims.d)) != RA_OK) return st;
   if ((st = make_map(&dom, dout, layout, dims.b, n_shards, p.L, dims.h, dims.d)) != RA_OK) return st;
   if ((st = make_dq_map(&dqm, dq, layout, dims.b, n_shards, p.L, dims.h, dims.d)) != RA_OK) return st;
-  const long long n_units = static_cast<long long>(dims.b) * dims.n_kv * n_shards * p.n_ktiles;
+  if ((st = make_dq_map(&dkm, dk, layout, dims.b, n_shards, p.L, dims.n_kv, dims.d)) != RA_OK) return st;
+  if ((st = make_dq_map(&dvm, dv, layout, dims.b, n_shards, p.L, dims.n_kv, dims.d)) != RA_OK) return st;
+  // one unit per (key tile, query shard, query head)
+  const long long n_units =
+      static_cast<long long>(dims.b) * dims.h * n_shards * n_shards * p.n_ktiles;
   if (n_units > 0x7fffffffLL) return fail(RA_ERR_UNSUPPORTED, "too many work units (%lld)", n_units);
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaMemsetAsync(dq, 0, static_cast<size_t>(dims.b) * S * dims.h * dims.d * 4, cs);
-  if (e != cudaSuccess) return cuda_fail(e, "dq clear");
-  e = counted(launch_bwd(p, dims.d, out, lse, dout, qm, km, vm, dom, dqm, n_units, sm_count(), cs), 2);
+  if (e == cudaSuccess)
+    e = cudaMemsetAsync(dk, 0, static_cast<size_t>(dims.b) * S * dims.n_kv * dims.d * 4, cs);
+  if (e == cudaSuccess)
+    e = cudaMemsetAsync(dv, 0, static_cast<size_t>(dims.b) * S * dims.n_kv * dims.d * 4, cs);
+  if (e != cudaSuccess) return cuda_fail(e, "gradient clear");
+  e = counted(launch_bwd(p, dims.d, out, lse, dout, qm, km, vm, dom, dqm, dkm, dvm, n_units,
+                         sm_count(), cs), 2);
   return e == cudaSuccess ? RA_OK : cuda_fail(e, "backward launch");
 }
 

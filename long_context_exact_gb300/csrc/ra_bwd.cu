@@ -6,13 +6,16 @@
 //     P  = exp(S - LSE),      S = scale Q K^T
 //     dV_j += P^T dO,         dP = dO V^T,       dS = P * (dP - D)
 //     dK_j += scale dS^T Q,   dQ_i += scale dS K
-// One CTA owns one 128-key tile of one KV head and keeps K, V in shared
-// memory and dK, dV in tensor memory.  Like the key/value block that carries
-// its gradient accumulators around the ring, the tile meets the query shards
-// in ring order: shard (j + s) mod N at step s, and inside each shard every
-// query tile the causal rule does not mask completely, for each of the g
-// query heads of its GQA group.  dQ partial tiles are added into the fp32 dq
-// output with vector reductions.
+// One CTA handles one 128-key tile of one KV head against one query shard i
+// and one query head of its GQA group: K, V stay in shared memory and the
+// unit's dK, dV accumulate in tensor memory over every query tile of shard i
+// the causal rule does not mask completely.  The key/value block of the
+// pages carries its gradient accumulators around the ring and meets shard
+// (j + s) mod N at step s; here the N shards (and g heads) of a tile are
+// separate units whose dK, dV partials are summed into the fp32 dk, dv with
+// bulk reductions, as the dQ partial tiles are into dq.  The sum does not
+// depend on the order.  Splitting by shard keeps the dq tiles that the
+// resident CTAs add into (one shard and head: n_qtiles x 64 KB) inside L2.
 //
 // Precision: bf16 operands with fp32 accumulation lose up to 2^-9 of each
 // product term, which on query rows with few visible keys (large weights)
@@ -132,71 +135,65 @@ enum : unsigned int {
 
 struct KvUnit {
   int bb, kh, j, c;   // batch, kv head, kv shard, kv tile
+  int i, hq;          // the query shard and query head it meets
   int kmin, kmax;     // token positions of the tile's first and last existing key
+  int a_lo, a_full;   // visible query tiles a >= a_lo; unmasked ones a >= a_full
 };
 
-// Units: groups of (batch, kv head, kv shard); inside a group the key tiles
-// run first to last (under a causal mask the first tiles meet the most query
-// tiles), so long units start first and neighbours share query tiles in L2.
+// Units: one 128-key tile against one query shard and one query head of its
+// group; dK and dV of the tile are summed over its units with reductions.
+// Units run grouped by (batch, kv head, query shard, query head) with the key
+// tiles innermost, so the CTAs resident together read the same Q / dO tiles
+// and add their dQ partials into the same 64 KB dq tiles: one group's dq
+// rows (n_qtiles x 64 KB) stay in L2 while every key tile adds to them.
 __device__ __forceinline__ KvUnit decode_kv_unit(const BwdParams &p, long long u) {
   KvUnit x;
   x.c = static_cast<int>(u % p.n_ktiles);
   long long g = u / p.n_ktiles;
   x.j = static_cast<int>(g % p.N);
   g /= p.N;
+  const int hh = static_cast<int>(g % p.g);
+  g /= p.g;
+  x.i = static_cast<int>(g % p.N);
+  g /= p.N;
   x.kh = static_cast<int>(g % p.n_kv);
   x.bb = static_cast<int>(g / p.n_kv);
+  x.hq = x.kh * p.g + hh;
   const int r0 = x.c * kTile;
   const int r1 = min(r0 + kTile, p.L) - 1;
   x.kmin = token_at(p.layout, p.L, p.N, x.j, r0);
   x.kmax = token_at(p.layout, p.L, p.N, x.j, r1);
+  if (!p.causal) {
+    x.a_lo = 0;
+    x.a_full = 0;
+  } else {
+    // visible query tiles: those whose last row sees the tile's first key
+    const int r_vis = max(0, first_row_at_or_after(p.layout, p.L, p.N, x.i, x.kmin));
+    x.a_lo = r_vis >= p.L ? p.n_qtiles : r_vis / kTile;
+    // unmasked query tiles: every row sees the tile's last key
+    const int r_full = max(0, first_row_at_or_after(p.layout, p.L, p.N, x.i, x.kmax));
+    x.a_full = min(p.n_qtiles, (r_full + kTile - 1) / kTile);
+  }
   return x;
 }
 
 struct QIter {
-  int s = -1, i = 0, a = 0, a_lo = 0, a_full = 0, hh = 0;
+  int a = INT_MAX;
 };
 
-// Next (query shard i, query tile a, query head hq) that meets this key
-// tile: shards in ring order; inside a shard the query tiles from the last
-// down to the first visible one, so every key tile of a KV head starts on the
-// same query tile and concurrently resident CTAs stream the same Q / dO
-// tiles.  `partial` marks steps that need the causal element mask; `split`
-// steps whose query tile has a row seeing fewer than kSplitKeys keys.
+// Next query tile of the unit, from the last down to the first visible one
+// (every key tile of a group starts on the same query tile).  `partial` marks
+// steps that need the causal element mask; `split` steps whose query tile
+// has a row seeing fewer than kSplitKeys keys.
 __device__ __forceinline__ bool q_next(const BwdParams &p, const KvUnit &x, QIter &it, int &i,
                                        int &a, int &hq, bool &partial, bool &split) {
-  bool have = false;
-  if (it.s >= 0) {
-    if (++it.hh < p.g) {
-      have = true;
-    } else {
-      it.hh = 0;
-      if (--it.a >= it.a_lo) have = true;
-    }
-  }
-  while (!have) {
-    if (++it.s >= p.N) return false;
-    it.i = (x.j + it.s) % p.N;
-    it.hh = 0;
-    if (!p.causal) {
-      it.a_lo = 0;
-      it.a_full = 0;
-    } else {
-      // visible query tiles: those whose last row sees the tile's first key
-      const int r_vis = max(0, first_row_at_or_after(p.layout, p.L, p.N, it.i, x.kmin));
-      it.a_lo = r_vis >= p.L ? p.n_qtiles : r_vis / kTile;
-      // unmasked query tiles: every row sees the tile's last key
-      const int r_full = max(0, first_row_at_or_after(p.layout, p.L, p.N, it.i, x.kmax));
-      it.a_full = min(p.n_qtiles, (r_full + kTile - 1) / kTile);
-    }
-    it.a = p.n_qtiles - 1;
-    have = it.a >= it.a_lo;
-  }
-  i = it.i;
+  it.a = it.a == INT_MAX ? p.n_qtiles - 1 : it.a - 1;
+  if (it.a < x.a_lo) return false;
+  i = x.i;
   a = it.a;
-  hq = x.kh * p.g + it.hh;
-  partial = it.a < it.a_full;
-  split = p.causal ? (token_at(p.layout, p.L, p.N, it.i, it.a * kTile) + 1 < kSplitKeys)
+  hq = x.hq;
+  partial = it.a < x.a_full;
+  split = p.causal ? (token_at(p.layout, p.L, p.N, x.i, it.a * kTile) + 1 < kSplitKeys)
                    : (p.S < kSplitKeys);
   return true;
 }
@@ -272,8 +269,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     bwd_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUtensorMap qmap,
                const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                const __grid_constant__ CUtensorMap domap,
-               const __grid_constant__ CUtensorMap dqmap) {
+               const __grid_constant__ CUtensorMap dqmap,
+               const __grid_constant__ CUtensorMap dkmap,
+               const __grid_constant__ CUtensorMap dvmap) {
   using C = BwdCfg<D>;
+  const KvUnit x = decode_kv_unit(p, blockIdx.x);
+  if (x.a_lo >= p.n_qtiles) return;  // no query of this shard sees the tile: nothing to add
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   if (pad > static_cast<uint32_t>(C::kSlack)) {  // uniform: never touch smem beyond the allocation
@@ -317,7 +318,6 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
-  const KvUnit x = decode_kv_unit(p, blockIdx.x);
 
   if (warp >= C::kProducerWarp) {
     regs_set<C::kOtherRegs, C::kLaunchRegs>();
@@ -714,34 +714,78 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     if constexpr (C::kDqTma) {
       if (lane == 0) bulk_wait_group0<false>();  // this warp's reductions complete
     }
-    // dK, dV of this key tile
+    // dK, dV of this unit, added into dk and dv (other units of the tile add
+    // theirs): through this warp's staging slice with bulk reductions for
+    // d = 128, vector reductions for d = 64.
     bool have = n > 0 && !aborted;
     if (have) have = mbar_wait(&bars[C::bDone], 0, abort_flag, kSiteBDone);
     have = __all_sync(kFull, have && *abort_flag == 0);
-    if (have) tc_fence_after();
-    const int kr = x.c * kTile + row;
-    const bool write = kr < p.L && !*abort_flag && (n == 0 || have);
-    const size_t off =
-        ((static_cast<size_t>(x.bb) * p.S + token_at(p.layout, p.L, p.N, x.j, kr < p.L ? kr : 0)) *
-             p.n_kv + x.kh) * D;
+    if (have) {
+      tc_fence_after();
+      const int r0 = x.c * kTile + (warp & 3) * 32;  // this warp's first key row
+      if constexpr (C::kDqTma) {
+        uint8_t *stg = smem + C::kStgOff + (warp & 3) * C::kDqWarpStgBytes;
+        int c2, c3;
+        map_coords(p.layout, p.L, p.N, x.j, r0, c2, c3);
 #pragma unroll
-    for (int which = 0; which < 2; ++which) {
-      const uint32_t col = which == 0 ? C::kColDk : C::kColDv;
-      float *dst = (which == 0 ? p.dk : p.dv) + off;
-      const float mul = which == 0 ? p.scale : 1.f;
+        for (int round = 0; round < 4; ++round) {  // dK cols 0-63, 64-127, then dV
+          const uint32_t col = (round < 2 ? C::kColDk : C::kColDv) + (round & 1) * 64;
+          const float mul = round < 2 ? p.scale : 1.f;
+          uint32_t r[2][32];
+          tmem_ld32_start(tmem + lane_off + col, r[0]);
+          tmem_ld32_start(tmem + lane_off + col + 32, r[1]);
+          tmem_ld_wait_regs(r[0]);
+          tmem_ld_wait_regs(r[1]);
+          if (lane == 0) bulk_wait_group0<true>();  // the slice's previous reads
+          __syncwarp();
 #pragma unroll
-      for (int ch = 0; ch < D / 32; ++ch) {
-        uint32_t r[32];
-        if (have) tmem_ld32(tmem + lane_off + col + ch * 32, r);
-        if (write) {
-          float4 *o4 = reinterpret_cast<float4 *>(dst + ch * 32);
+          for (int bx = 0; bx < 2; ++bx) {
+            uint8_t *rowp = stg + bx * C::kDqBoxBytes + lane * 128;
 #pragma unroll
-          for (int u = 0; u < 8; ++u)
-            o4[u] = have ? make_float4(__uint_as_float(r[u * 4 + 0]) * mul,
-                                       __uint_as_float(r[u * 4 + 1]) * mul,
-                                       __uint_as_float(r[u * 4 + 2]) * mul,
-                                       __uint_as_float(r[u * 4 + 3]) * mul)
-                         : make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int u = 0; u < 8; ++u)
+              *reinterpret_cast<float4 *>(rowp + ((u ^ (lane & 7)) * 16)) =
+                  make_float4(__uint_as_float(r[bx][4 * u + 0]) * mul,
+                              __uint_as_float(r[bx][4 * u + 1]) * mul,
+                              __uint_as_float(r[bx][4 * u + 2]) * mul,
+                              __uint_as_float(r[bx][4 * u + 3]) * mul);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0 && r0 < p.L) {
+#pragma unroll
+            for (int bx = 0; bx < 2; ++bx)
+              tma_reduce_add_5d(round < 2 ? &dkmap : &dvmap, stg + bx * C::kDqBoxBytes,
+                                (round & 1) * 64 + bx * 32, x.kh, c2, c3, x.bb);
+            bulk_commit_group();
+          }
+        }
+        if (lane == 0) bulk_wait_group0<false>();
+      } else {
+        const int kr = x.c * kTile + row;
+        const size_t off =
+            ((static_cast<size_t>(x.bb) * p.S +
+              token_at(p.layout, p.L, p.N, x.j, kr < p.L ? kr : 0)) * p.n_kv + x.kh) * D;
+#pragma unroll
+        for (int which = 0; which < 2; ++which) {
+          const uint32_t col = which == 0 ? C::kColDk : C::kColDv;
+          float *dst = (which == 0 ? p.dk : p.dv) + off;
+          const float mul = which == 0 ? p.scale : 1.f;
+#pragma unroll
+          for (int ch = 0; ch < D / 32; ++ch) {
+            uint32_t r[32];
+            tmem_ld32(tmem + lane_off + col + ch * 32, r);
+            if (kr < p.L) {
+#pragma unroll
+              for (int u = 0; u < 8; ++u)
+                asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(
+                                 dst + ch * 32 + u * 4),
+                             "f"(__uint_as_float(r[u * 4 + 0]) * mul),
+                             "f"(__uint_as_float(r[u * 4 + 1]) * mul),
+                             "f"(__uint_as_float(r[u * 4 + 2]) * mul),
+                             "f"(__uint_as_float(r[u * 4 + 3]) * mul)
+                             : "memory");
+            }
+          }
         }
       }
     }
@@ -800,7 +844,8 @@ template <int D>
 cudaError_t launch_bwd_t(const BwdParams &p, const float *out, const float *lse,
                          const uint16_t *dout, const CUtensorMap &qmap, const CUtensorMap &kmap,
                          const CUtensorMap &vmap, const CUtensorMap &domap,
-                         const CUtensorMap &dqmap, long long n_units, int n_sm,
+                         const CUtensorMap &dqmap, const CUtensorMap &dkmap,
+                         const CUtensorMap &dvmap, long long n_units, int n_sm,
                          cudaStream_t stream) {
   using C = BwdCfg<D>;
   const long long pre_rows = static_cast<long long>(p.b) * p.h * p.N * p.Lpad;
@@ -822,7 +867,7 @@ cudaError_t launch_bwd_t(const BwdParams &p, const float *out, const float *lse,
     if (attr.numRegs != C::kLaunchRegs) return cudaErrorInvalidConfiguration;
   }
   kern<<<dim3(static_cast<unsigned int>(n_units)), dim3(C::kThreads), C::kSmemAlloc, stream>>>(
-      p, qmap, kmap, vmap, domap, dqmap);
+      p, qmap, kmap, vmap, domap, dqmap, dkmap, dvmap);
   return cudaGetLastError();
 }
 
@@ -831,15 +876,16 @@ cudaError_t launch_bwd_t(const BwdParams &p, const float *out, const float *lse,
 cudaError_t launch_bwd(const BwdParams &p, int d, const float *out, const float *lse,
                        const uint16_t *dout, const CUtensorMap &qmap, const CUtensorMap &kmap,
                        const CUtensorMap &vmap, const CUtensorMap &domap,
-                       const CUtensorMap &dqmap, long long n_units, int n_sm,
+                       const CUtensorMap &dqmap, const CUtensorMap &dkmap,
+                       const CUtensorMap &dvmap, long long n_units, int n_sm,
                        cudaStream_t stream) {
   if (n_units <= 0) return cudaSuccess;
   if (d == 128)
-    return launch_bwd_t<128>(p, out, lse, dout, qmap, kmap, vmap, domap, dqmap, n_units, n_sm,
-                             stream);
+    return launch_bwd_t<128>(p, out, lse, dout, qmap, kmap, vmap, domap, dqmap, dkmap, dvmap,
+                             n_units, n_sm, stream);
   if (d == 64)
-    return launch_bwd_t<64>(p, out, lse, dout, qmap, kmap, vmap, domap, dqmap, n_units, n_sm,
-                            stream);
+    return launch_bwd_t<64>(p, out, lse, dout, qmap, kmap, vmap, domap, dqmap, dkmap, dvmap,
+                            n_units, n_sm, stream);
   return cudaErrorInvalidValue;
 }
 

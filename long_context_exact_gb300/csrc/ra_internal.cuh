@@ -147,7 +147,8 @@ cudaError_t launch_fwd(const FwdParams &p, int d, int nq, const CUtensorMap &qma
 cudaError_t launch_bwd(const BwdParams &p, int d, const float *out, const float *lse,
                        const uint16_t *dout, const CUtensorMap &qmap, const CUtensorMap &kmap,
                        const CUtensorMap &vmap, const CUtensorMap &domap,
-                       const CUtensorMap &dqmap, long long n_units, int n_sm,
+                       const CUtensorMap &dqmap, const CUtensorMap &dkmap,
+                       const CUtensorMap &dvmap, long long n_units, int n_sm,
                        cudaStream_t stream);
 
 // Element-wise kernels (ra_small.cu).
