@@ -32,9 +32,13 @@ if ROOT not in sys.path:
 METRIC = "useful attention TFLOP/s fwd & bwd (causal, S=256K GQA) and % of BF16 tensor peak"
 WORKLOAD = "causal256k"
 
-# Per-launch DRAM traffic of the dominant kernels from one ncu capture, valid
-# only while the kernel source hashes match (see profiles/).
-TRAFFIC = {}
+# Per-launch DRAM traffic of the dominant kernels from one ncu capture
+# (dram__bytes_read.sum + dram__bytes_write.sum, one pass, this workload),
+# valid only while the kernel source hashes match (see profiles/).
+TRAFFIC = {
+    "bwd": {"bytes_per_launch": 117758141952 + 80446772480, "src_sha": "ab8df136a2c4b952",
+            "profile": "profiles/traffic_bwd_causal256k.md"},
+}
 
 
 def _args():
