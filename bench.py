@@ -347,6 +347,37 @@ def hbm_kernel_report(w, dev, peaks):
     return out
 
 
+def prefill_report(w, q, k, v, dev):
+    """Chunked prefill at the workload's length: the last Lq tokens of the
+    sequence attend to all S keys (ra_chunked_prefill), with the automatic
+    key split and with a single split."""
+    import torch
+
+    from long_context_exact_gb300 import binding as ra
+
+    res = []
+    kpos = torch.arange(w.S, dtype=torch.int32, device=dev)
+    for Lq in (512, 4096):
+        if Lq > w.S:
+            continue
+        qc = q[:, w.S - Lq:].contiguous()
+        qpos = kpos[w.S - Lq:].contiguous()
+        pairs = Lq * w.S - Lq * (Lq - 1) // 2          # visible (query, key) pairs per head
+        flops = 4.0 * w.b * w.h * w.d * pairs
+        for splits in (0, 1):
+            ws = torch.empty(max(ra.prefill_workspace_size(Lq, w.S, splits, w.b, w.h, w.n_kv,
+                                                           w.d), 16),
+                             dtype=torch.uint8, device=dev)
+            ms = _time_ms(lambda: ra.chunked_prefill(qc, k, v, qpos, kpos, True, n_splits=splits,
+                                                     workspace=ws), reps=3)
+            used = ws.numel() // (w.b * w.h * Lq * (2 + w.d) * 4)
+            res.append({"Lq": Lq, "Lk": w.S, "n_splits": splits, "splits_used": int(used),
+                        "ms": ms, "tflops": flops / (ms / 1e3) / 1e12})
+            del ws
+    ra.stream_check()
+    return res
+
+
 # ---------------------------------------------------------------- our arm
 def run_ours(a, rank, world, local_rank):
     import torch
@@ -515,6 +546,7 @@ def run_ours(a, rank, world, local_rank):
         extras = layout_and_imbalance_report(w, q, k, v, dev)
         extras["exp2_roof"] = exp2_roof_report(w, dev, clk)
         extras["hbm_kernels"] = hbm_kernel_report(w, dev, peaks)
+        extras["chunked_prefill"] = prefill_report(w, q, k, v, dev)
 
     cpu = None
     if rank == 0 and world == 1 and not a.no_cpu_baseline:

@@ -133,6 +133,29 @@ ra_status ra_ring_attention(const uint16_t *q, const uint16_t *k, const uint16_t
                             float *lse, int64_t S, int n_shards, ra_layout layout, int causal,
                             float scale, ra_dims dims, void *stream);
 
+/* Chunked prefill: Lq new query tokens (positions q_pos) attend to Lk
+ * resident keys (positions k_pos) -- the first page's inference remark, a
+ * block step with Lq much smaller than Lk.  The keys are cut into n_splits
+ * ranges of whole 128-key tiles that run as concurrent block steps, each into
+ * its own online-softmax state in the workspace, and the states are combined
+ * with the second page's rescale-merge generalised to n parts:
+ *   M = max_s m_s, L = sum_s l_s e^(m_s - M), out = sum_s e^(m_s - M) O_s / L,
+ *   lse = M + ln L  (rows no key reaches: 0 and -inf).
+ *   q [b, Lq, h, d] bf16; k, v [b, Lk, n_kv, d] bf16; q_pos [Lq], k_pos [Lk]
+ *   int32 (needed when causal: key visible iff k_pos <= q_pos);
+ *   out [b, Lq, h, d] float; lse [b, h, Lq] float (overwritten).
+ *   n_splits: 0 picks enough splits to fill the GPU; at most 64.
+ *   workspace: device memory of ra_prefill_workspace_size() bytes (same
+ *   n_splits), 16-byte aligned, scratch after the call.
+ * Launches three kernels on `stream`; RA_ERR_WORKSPACE if the workspace is
+ * missing or small.  The pages give no kernel for this case; splitting the
+ * keys is this library's way to fill the GPU when Lq is short. */
+size_t ra_prefill_workspace_size(int64_t Lq, int64_t Lk, int n_splits, ra_dims dims);
+ra_status ra_chunked_prefill(const uint16_t *q, const uint16_t *k, const uint16_t *v, float *out,
+                             float *lse, const int32_t *q_pos, const int32_t *k_pos, int64_t Lq,
+                             int64_t Lk, int n_splits, ra_dims dims, int causal, float scale,
+                             void *workspace, size_t workspace_bytes, void *stream);
+
 /* Bytes of device workspace ra_ring_attention_bwd needs: per query row,
  * D = rowsum(dO * O) and the log2-domain LSE, both float, stored per shard
  * with each shard's rows padded to a multiple of 128.  0 if the arguments

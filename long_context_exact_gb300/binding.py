@@ -74,6 +74,11 @@ def load(path: str | None = None):
         lib.ra_ring_attention_bwd_noalloc.argtypes = [P, P, P, P, P, P, P, P, P, I64, I, I, I, F,
                                                       Dims, P]
         lib.ra_ring_attention_bwd_noalloc.restype = I
+        lib.ra_prefill_workspace_size.argtypes = [I64, I64, I, Dims]
+        lib.ra_prefill_workspace_size.restype = ctypes.c_size_t
+        lib.ra_chunked_prefill.argtypes = [P, P, P, P, P, P, P, I64, I64, I, Dims, I, F, P,
+                                           ctypes.c_size_t, P]
+        lib.ra_chunked_prefill.restype = I
         lib.ra_bwd_workspace_size.argtypes = [I64, I, Dims]
         lib.ra_bwd_workspace_size.restype = ctypes.c_size_t
         lib.ra_last_error.argtypes = []
@@ -202,6 +207,36 @@ def merge(o_a, lse_a, o_b, lse_b, o=None, lse=None, stream=None):
 
 
 # ---------------------------------------------------------------- backward
+def prefill_workspace_size(Lq: int, Lk: int, n_splits: int, b: int, h: int, n_kv: int,
+                           d: int) -> int:
+    return int(load().ra_prefill_workspace_size(Lq, Lk, n_splits, _dims(b, h, n_kv, d)))
+
+
+def chunked_prefill(q, k, v, q_pos=None, k_pos=None, causal: bool = True, scale: float = 0.0,
+                    n_splits: int = 0, out=None, lse=None, workspace=None, stream=None):
+    """Lq new queries against Lk resident keys with the keys split over
+    concurrent block steps; returns (out [b,Lq,h,d] float, lse [b,h,Lq])."""
+    lib = load()
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, torch.bfloat16, n)
+    b, Lq, h, d = q.shape
+    Lk, n_kv = k.shape[1], k.shape[2]
+    out = torch.empty((b, Lq, h, d), dtype=torch.float32, device=q.device) if out is None else out
+    lse = torch.empty((b, h, Lq), dtype=torch.float32, device=q.device) if lse is None else lse
+    if workspace is None:
+        nbytes = prefill_workspace_size(Lq, Lk, n_splits, b, h, n_kv, d)
+        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
+    for t, n in ((q_pos, "q_pos"), (k_pos, "k_pos")):
+        if t is not None:
+            _need(t, torch.int32, n)
+    _check(lib.ra_chunked_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse),
+                                  _ptr(q_pos) if q_pos is not None else None,
+                                  _ptr(k_pos) if k_pos is not None else None, Lq, Lk, n_splits,
+                                  _dims(b, h, n_kv, d), 1 if causal else 0, scale,
+                                  _ptr(workspace), workspace.numel(), _stream(stream)))
+    return out, lse
+
+
 def bwd_workspace_size(S: int, n_shards: int, b: int, h: int, n_kv: int, d: int) -> int:
     return int(load().ra_bwd_workspace_size(S, int(n_shards), _dims(b, h, n_kv, d)))
 

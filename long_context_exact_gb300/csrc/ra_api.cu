@@ -2,6 +2,7 @@
 // validation, TMA tensor-map construction, kernel launches and error
 // reporting.  No device memory is allocated here.
 #include <cmath>
+#include <algorithm>
 #include <cstdarg>
 #include <cstdint>
 #include <cstdio>
@@ -207,6 +208,29 @@ ra_status launch_attention(const FwdParams &p, int d, const void *q, const void 
   return RA_OK;
 }
 
+// Key splits for a chunked prefill: n_splits if given (capped by the key
+// tiles and kMaxSplits), else enough splits for about eight waves of CTAs
+// (so the last, partly filled wave costs little) with at least four key
+// tiles each.
+constexpr int kMaxSplits = 64;
+
+int resolve_splits(int64_t Lq, int64_t Lk, int n_splits, const ra_dims &dims) {
+  const int n_ktiles = static_cast<int>((Lk + kTile - 1) / kTile);
+  int s = n_splits;
+  if (s <= 0) {
+    const int g = dims.h / dims.n_kv;
+    const long long units = static_cast<long long>(dims.b) * dims.n_kv * (g % 2 == 0 ? g / 2 : g) *
+                            ((Lq + kTile - 1) / kTile);
+    const long long want = (8LL * sm_count() + units - 1) / units;
+    s = static_cast<int>(want < 1 ? 1 : (want > kMaxSplits ? kMaxSplits : want));
+    s = std::min(s, std::max(1, (n_ktiles + 3) / 4));
+  }
+  s = std::min(std::min(s, kMaxSplits), std::max(1, n_ktiles));
+  // splits of equal whole tiles: the last may be shorter, none empty
+  const int per = (n_ktiles + s - 1) / s;
+  return (n_ktiles + per - 1) / per;
+}
+
 }  // namespace
 
 ra_status report_error(ra_status st, const char *fmt, ...) {
@@ -306,6 +330,83 @@ ra_status ra_merge(const float *o_a, const float *lse_a, const float *o_b, const
   cudaError_t e = counted(launch_merge(o_a, lse_a, o_b, lse_b, o, lse, dims.b, Lq, dims.h, dims.d,
                                        static_cast<cudaStream_t>(stream)));
   return e == cudaSuccess ? RA_OK : cuda_fail(e, "merge launch");
+}
+
+size_t ra_prefill_workspace_size(int64_t Lq, int64_t Lk, int n_splits, ra_dims dims) {
+  if (Lq <= 0 || Lk <= 0 || dims.b <= 0 || dims.h <= 0 || dims.n_kv <= 0 ||
+      dims.h % dims.n_kv != 0 || dims.d <= 0 || Lq >= (1LL << 31) || Lk >= (1LL << 31))
+    return 0;
+  const int s = resolve_splits(Lq, Lk, n_splits, dims);
+  const size_t rows = static_cast<size_t>(dims.b) * dims.h * static_cast<size_t>(Lq);
+  return static_cast<size_t>(s) * rows * (2 + static_cast<size_t>(dims.d)) * sizeof(float);
+}
+
+ra_status ra_chunked_prefill(const uint16_t *q, const uint16_t *k, const uint16_t *v, float *out,
+                             float *lse, const int32_t *q_pos, const int32_t *k_pos, int64_t Lq,
+                             int64_t Lk, int n_splits, ra_dims dims, int causal, float scale,
+                             void *workspace, size_t workspace_bytes, void *stream) {
+  ra_status st;
+  if ((st = check_dims(dims)) != RA_OK) return st;
+  if (Lq < 0 || Lk < 0) return fail(RA_ERR_INVALID_ARG, "negative length Lq=%lld Lk=%lld",
+                                    (long long)Lq, (long long)Lk);
+  if (Lq >= (1LL << 31) || Lk >= (1LL << 31))
+    return fail(RA_ERR_UNSUPPORTED, "Lq/Lk must be below 2^31");
+  if (n_splits < 0 || n_splits > kMaxSplits)
+    return fail(RA_ERR_INVALID_ARG, "n_splits must be 0 (automatic) .. %d", kMaxSplits);
+  if (Lq == 0 || dims.b == 0) return RA_OK;
+  RA_CHECK_PTR(q);
+  RA_CHECK_PTR(out);
+  RA_CHECK_PTR(lse);
+  if (Lk > 0) {
+    RA_CHECK_PTR(k);
+    RA_CHECK_PTR(v);
+  }
+  if (causal && (!q_pos || (Lk > 0 && !k_pos)))
+    return fail(RA_ERR_INVALID_ARG, "causal prefill needs q_pos and k_pos");
+  float sc = 0.f;
+  if ((st = resolve_scale(scale, dims.d, &sc)) != RA_OK) return st;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  const long long rows = static_cast<long long>(dims.b) * dims.h * Lq;
+  if (Lk == 0) {  // nothing to attend to: O = 0, LSE = -inf
+    cudaError_t e = counted(launch_state_init(lse, nullptr, out, rows, dims.d, cs));
+    return e == cudaSuccess ? RA_OK : cuda_fail(e, "empty prefill");
+  }
+  const size_t need = ra_prefill_workspace_size(Lq, Lk, n_splits, dims);
+  if (workspace == nullptr || workspace_bytes < need)
+    return fail(RA_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need,
+                workspace == nullptr ? (size_t)0 : workspace_bytes);
+  if (!aligned16(workspace)) return fail(RA_ERR_INVALID_ARG, "workspace is not 16-byte aligned");
+  const int splits = resolve_splits(Lq, Lk, n_splits, dims);
+  float *m = static_cast<float *>(workspace);
+  float *l = m + static_cast<size_t>(splits) * rows;
+  float *o = l + static_cast<size_t>(splits) * rows;
+  FwdParams p{};
+  p.b = dims.b;
+  p.h = dims.h;
+  p.n_kv = dims.n_kv;
+  p.g = dims.h / dims.n_kv;
+  p.N = 1;
+  p.L = static_cast<int>(Lq);
+  p.Lk = static_cast<int>(Lk);
+  p.S = static_cast<int>(Lq);
+  p.layout = RA_LAYOUT_CONTIGUOUS;
+  p.causal = causal ? 1 : 0;
+  p.scale_log2 = sc * kLog2e;
+  p.n_qtiles = static_cast<int>((Lq + kTile - 1) / kTile);
+  p.n_ktiles = static_cast<int>((Lk + kTile - 1) / kTile);
+  p.split_tiles = (p.n_ktiles + splits - 1) / splits;
+  p.block_mode = 1;
+  p.q_pos = q_pos;
+  p.k_pos = k_pos;
+  p.st_m = m;
+  p.st_l = l;
+  p.st_o = o;
+  cudaError_t e = counted(launch_state_init(m, l, o, static_cast<long long>(splits) * rows,
+                                            dims.d, cs));
+  if (e != cudaSuccess) return cuda_fail(e, "state init");
+  if ((st = launch_attention(p, dims.d, q, k, v, Lq, Lk, cs)) != RA_OK) return st;
+  e = counted(launch_combine(m, l, o, splits, out, lse, dims.b, Lq, dims.h, dims.d, cs));
+  return e == cudaSuccess ? RA_OK : cuda_fail(e, "combine launch");
 }
 
 ra_status ra_ring_attention(const uint16_t *q, const uint16_t *k, const uint16_t *v, float *out,

@@ -99,6 +99,7 @@ enum : unsigned int {
 struct Unit {
   int bb, kh, pr, i, a;
   int qmin, qmax;  // token positions of the tile's first and last existing row
+  int kc0, kc1;    // block mode: key tiles [kc0, kc1) of this CTA's key split
 };
 
 // Work-unit order: groups of (batch, kv head, query shard); inside a group the
@@ -118,6 +119,9 @@ __device__ __forceinline__ Unit decode_unit(const FwdParams &p, long long u) {
   x.bb = static_cast<int>(g2 / p.n_kv);
   x.qmin = 0;
   x.qmax = 0;
+  // block mode with a key split: blockIdx.y selects split_tiles key tiles
+  x.kc0 = p.split_tiles > 0 ? static_cast<int>(blockIdx.y) * p.split_tiles : 0;
+  x.kc1 = p.split_tiles > 0 ? min(p.n_ktiles, x.kc0 + p.split_tiles) : p.n_ktiles;
   return x;
 }
 
@@ -162,7 +166,7 @@ struct KvIter {
   // block mode: a window of 32 key tiles starting at `win`, with bit t of
   // `keep` set when tile win + t holds a key some query of the unit sees,
   // and of `part` when that tile needs the element mask
-  int win = -1;
+  int win = -2;  // -2: not started
   uint32_t keep = 0, part = 0;
 };
 
@@ -197,8 +201,12 @@ __device__ __forceinline__ bool kv_next(const FwdParams &p, const Unit &x, KvIte
     ++it.c;
     return true;
   } else {
+    if (it.win == -2) {  // first call: start at the split's first tile
+      it.c = x.kc0;
+      it.win = -1;
+    }
     if (!p.causal) {
-      if (it.c >= p.n_ktiles) return false;
+      if (it.c >= x.kc1) return false;
       c = it.c++;
       j = 0;
       partial = c >= n_complete;
@@ -207,7 +215,7 @@ __device__ __forceinline__ bool kv_next(const FwdParams &p, const Unit &x, KvIte
     const int lane = threadIdx.x & 31;
     while (true) {
       if (it.win < 0 || it.c >= it.win + 32) {
-        if (it.c >= p.n_ktiles) return false;
+        if (it.c >= x.kc1) return false;
         // Classify the next 32 key tiles from their positions' min and max:
         // eight tiles at a time, every lane loading four positions of each
         // (coalesced), then one warp reduction per tile.
@@ -225,7 +233,7 @@ __device__ __forceinline__ bool kv_next(const FwdParams &p, const Unit &x, KvIte
 #pragma unroll
             for (int e = 0; e < kTile / 32; ++e) {
               const int kr = tile * kTile + e * 32 + lane;
-              if (tile < p.n_ktiles && kr < p.Lk) {
+              if (tile < x.kc1 && kr < p.Lk) {
                 const int v = p.k_pos[kr];
                 lo[t] = min(lo[t], v);
                 hi[t] = max(hi[t], v);
@@ -237,7 +245,7 @@ __device__ __forceinline__ bool kv_next(const FwdParams &p, const Unit &x, KvIte
             lo[t] = warp_min(lo[t]);
             hi[t] = warp_max(hi[t]);
             const int tile = it.win + sb * 8 + t;
-            if (tile < p.n_ktiles && lo[t] <= x.qmax) {  // else every key follows every query
+            if (tile < x.kc1 && lo[t] <= x.qmax) {  // else every key follows every query
               it.keep |= 1u << (sb * 8 + t);
               if (tile >= n_complete || hi[t] > x.qmin) it.part |= 1u << (sb * 8 + t);
             }
@@ -346,6 +354,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::kThreads, 1)
     }
     mbar_init(&bars[C::bDrain], 1);
     *abort_flag = 0;
+    *reinterpret_cast<int *>(smem + C::kMiscOff + 8) = 0;  // block mode: visible-key count
     fence_barrier_init();
   }
   if (warp == C::kMmaWarp) {
@@ -359,7 +368,31 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::kThreads, 1)
 
   Unit x = decode_unit(p, blockIdx.x);
   unit_qrange<kBlock>(p, x);
-  const bool split = kBlock || (p.causal ? (x.qmin + 1 < kSplitKeys) : (p.S < kSplitKeys));
+  // Rows that see fewer than kSplitKeys keys take the hi + lo path.  On the
+  // ring a row at position t sees t + 1 keys.  A block step counts, over the
+  // CTA's key range, the keys its earliest query sees (every row of the tile
+  // sees at least those).
+  bool split;
+  if constexpr (!kBlock) {
+    split = p.causal ? (x.qmin + 1 < kSplitKeys) : (p.S < kSplitKeys);
+  } else {
+    const int k0 = x.kc0 * kTile, k1 = min(p.Lk, x.kc1 * kTile);
+    if (k1 - k0 < kSplitKeys) {
+      split = true;
+    } else if (!p.causal) {
+      split = false;
+    } else {
+      int *cnt = reinterpret_cast<int *>(smem + C::kMiscOff + 8);
+      int mine = 0;
+      for (int kk = k0 + static_cast<int>(threadIdx.x); kk < k1; kk += blockDim.x)
+        mine += p.k_pos[kk] <= x.qmin ? 1 : 0;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mine += __shfl_xor_sync(kFull, mine, o);
+      if (lane == 0) atomicAdd(cnt, mine);
+      __syncthreads();
+      split = *cnt < kSplitKeys;
+    }
+  }
 
   if (warp >= C::kSoftmaxWarps) {
     if constexpr (C::kResplit) regs_set<C::kOtherRegs, C::kLaunchRegs>();
@@ -645,8 +678,12 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::kThreads, 1)
     } else {
       // Fold the block result (shift m_run, sum l_sum, numerator in TMEM)
       // into the caller's state, re-referenced to the exact running max.
-      const size_t si = (static_cast<size_t>(x.bb) * p.h + hq) * p.L + r_cl;
-      const size_t oi = ((static_cast<size_t>(x.bb) * p.L + r_cl) * p.h + hq) * D;
+      // with a key split, each split folds into its own state slice
+      const size_t z = p.split_tiles > 0 ? blockIdx.y : 0;
+      const size_t si = z * p.b * p.h * static_cast<size_t>(p.L) +
+                        (static_cast<size_t>(x.bb) * p.h + hq) * p.L + r_cl;
+      const size_t oi = z * p.b * p.h * static_cast<size_t>(p.L) * D +
+                        ((static_cast<size_t>(x.bb) * p.L + r_cl) * p.h + hq) * D;
       const float m_old2 = row_exists ? p.st_m[si] * kLog2e : -INFINITY;
       const float M = fmaxf(m_old2, have_o ? m_max : -INFINITY);
       const bool write = row_exists && !*abort_flag && have_o && M != -INFINITY;
@@ -700,7 +737,12 @@ cudaError_t launch_fwd_t(const FwdParams &p, const CUtensorMap &qmap, const CUte
     // The re-split assumes each warpgroup starts from exactly kLaunchRegs.
     if (attr.numRegs != C::kLaunchRegs) return cudaErrorInvalidConfiguration;
   }
-  kern<<<dim3(static_cast<unsigned int>(n_units)), dim3(C::kThreads), C::kSmemAlloc, stream>>>(
+  const unsigned int splits = (kBlock && p.split_tiles > 0)
+                                  ? static_cast<unsigned int>((p.n_ktiles + p.split_tiles - 1) /
+                                                              p.split_tiles)
+                                  : 1u;
+  kern<<<dim3(static_cast<unsigned int>(n_units), splits), dim3(C::kThreads), C::kSmemAlloc,
+         stream>>>(
       p, qmap, kmap, vmap);
   return cudaGetLastError();
 }

@@ -113,6 +113,7 @@ struct FwdParams {
   int n_ktiles;             // ceil(Lk / 128)
   int pairs;                // g / NQ query-head groups per KV head
   int block_mode;           // 0: ring + finalize, 1: block step with state merge
+  int split_tiles;          // block mode: key tiles per split (0: one split of all)
   const int32_t *q_pos;     // block mode: [Lq]
   const int32_t *k_pos;     // block mode: [Lk]
   float *out;               // ring: [b, S, h, d]
@@ -161,6 +162,10 @@ cudaError_t launch_position_map(int layout, int S, int N, int32_t *shard_of, int
                                 int32_t *token_of, cudaStream_t stream);
 cudaError_t launch_ring_order(int N, int32_t *order, cudaStream_t stream);
 cudaError_t launch_wait_timeout_selftest(long long budget, cudaStream_t stream);
+cudaError_t launch_state_init(float *m, float *l, float *o, long long m_rows, int d,
+                              cudaStream_t stream);
+cudaError_t launch_combine(const float *m, const float *l, const float *o, int splits, float *out,
+                           float *lse, int b, long long Lq, int h, int d, cudaStream_t stream);
 cudaError_t launch_ex2_probe(long long iters, float *sink, int blocks, int threads,
                              cudaStream_t stream);
 // Record a message for ra_last_error() on this thread and return `st`.

@@ -28,74 +28,178 @@ inline unsigned int ew_grid(long long work) {
   return static_cast<unsigned int>(want < 1 ? 1 : (want < cap ? want : cap));
 }
 
-// One warp per (batch, head, row); lanes stride the d columns with float4.
-// o <- o / l, lse = m + ln l; rows with l == 0 get 0 and -inf.
+// Rows handled per warp and loop trip by the two HBM-bound kernels below:
+// their loads are all issued before any result is formed, so each warp keeps
+// kRowsPerTrip rows of every operand in flight (one float4 per lane and row).
+constexpr int kRowsPerTrip = 4;
+
+// Decompose warp-row index w of [b, h, Lq] into the float offset of its
+// [b, Lq, h, d] row.
+__device__ __forceinline__ size_t row_offset(long long w, long long Lq, int h, int d) {
+  const long long r = w % Lq;
+  const long long bh = w / Lq;
+  const long long hq = bh % h;
+  const long long bb = bh / h;
+  return static_cast<size_t>(((bb * Lq + r) * h + hq) * d);
+}
+
+// One warp per (batch, head, row), lane e holding columns 4e..4e+3 (d = 64
+// uses half the warp).  o <- o / l, lse = m + ln l; rows with l == 0 get 0
+// and -inf.
 __global__ void finalize_kernel(float *o, const float *l, const float *m, float *lse, int b,
                                 long long Lq, int h, int d) {
   const long long rows = static_cast<long long>(b) * h * Lq;
   const int lane = threadIdx.x & 31;
+  const bool col = lane < d / 4;
   const long long warps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
-  for (long long w = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; w < rows;
-       w += warps) {
-    const long long r = w % Lq;
-    const long long bh = w / Lq;
-    const int hq = static_cast<int>(bh % h);
-    const long long bb = bh / h;
-    const float lr = l[w];
-    const bool live = lr > 0.f;
-    const float inv = live ? 1.f / lr : 0.f;
-    if (lane == 0) lse[w] = live ? m[w] + logf(lr) : -INFINITY;
-    float4 *row = reinterpret_cast<float4 *>(o + ((bb * Lq + r) * h + hq) * d);
-    for (int e = lane; e < d / 4; e += 32) {
-      float4 v = row[e];
-      v.x *= inv;
-      v.y *= inv;
-      v.z *= inv;
-      v.w *= inv;
-      row[e] = v;
+  const long long w0 = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  for (long long base = w0; base < rows; base += kRowsPerTrip * warps) {
+    float4 v[kRowsPerTrip];
+    float lr[kRowsPerTrip], mr[kRowsPerTrip];
+#pragma unroll
+    for (int k = 0; k < kRowsPerTrip; ++k) {
+      const long long w = base + k * warps;
+      if (w < rows) {
+        lr[k] = l[w];
+        mr[k] = m[w];
+        if (col) v[k] = reinterpret_cast<const float4 *>(o + row_offset(w, Lq, h, d))[lane];
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < kRowsPerTrip; ++k) {
+      const long long w = base + k * warps;
+      if (w < rows) {
+        const bool live = lr[k] > 0.f;
+        const float inv = live ? 1.f / lr[k] : 0.f;
+        if (lane == 0) lse[w] = live ? mr[k] + logf(lr[k]) : -INFINITY;
+        if (col) {
+          float4 x = v[k];
+          x.x *= inv;
+          x.y *= inv;
+          x.z *= inv;
+          x.w *= inv;
+          reinterpret_cast<float4 *>(o + row_offset(w, Lq, h, d))[lane] = x;
+        }
+      }
     }
   }
 }
 
 // Rescale-merge of two normalised partial results over disjoint keys.
+// o (and lse) may alias side a: each element is read before it is written.
 __global__ void merge_kernel(const float *o_a, const float *lse_a, const float *o_b,
                              const float *lse_b, float *o, float *lse, int b, long long Lq, int h,
                              int d) {
   const long long rows = static_cast<long long>(b) * h * Lq;
   const int lane = threadIdx.x & 31;
+  const bool col = lane < d / 4;
   const long long warps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
-  for (long long w = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; w < rows;
-       w += warps) {
-    const long long r = w % Lq;
-    const long long bh = w / Lq;
-    const int hq = static_cast<int>(bh % h);
-    const long long bb = bh / h;
-    const float la = lse_a[w], lb = lse_b[w];
-    const float mx = fmaxf(la, lb);
-    float wa = 0.f, wb = 0.f, out_lse = -INFINITY;
-    if (mx != -INFINITY) {
-      wa = (la == -INFINITY) ? 0.f : expf(la - mx);
-      wb = (lb == -INFINITY) ? 0.f : expf(lb - mx);
-      const float den = wa + wb;
-      out_lse = mx + logf(den);
-      wa /= den;
-      wb /= den;
+  const long long w0 = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  for (long long base = w0; base < rows; base += kRowsPerTrip * warps) {
+    float4 va[kRowsPerTrip], vb[kRowsPerTrip];
+    float la[kRowsPerTrip], lb[kRowsPerTrip];
+#pragma unroll
+    for (int k = 0; k < kRowsPerTrip; ++k) {
+      const long long w = base + k * warps;
+      if (w < rows) {
+        la[k] = lse_a[w];
+        lb[k] = lse_b[w];
+        if (col) {
+          const size_t off = row_offset(w, Lq, h, d);
+          va[k] = reinterpret_cast<const float4 *>(o_a + off)[lane];
+          vb[k] = reinterpret_cast<const float4 *>(o_b + off)[lane];
+        }
+      }
     }
-    const size_t off = ((bb * Lq + r) * h + hq) * d;
-    const float4 *ra4 = reinterpret_cast<const float4 *>(o_a + off);
-    const float4 *rb4 = reinterpret_cast<const float4 *>(o_b + off);
-    float4 *ro4 = reinterpret_cast<float4 *>(o + off);
-    for (int e = lane; e < d / 4; e += 32) {
-      const float4 a = ra4[e], c = rb4[e];
-      float4 v;
-      v.x = (wa == 0.f ? 0.f : wa * a.x) + (wb == 0.f ? 0.f : wb * c.x);
-      v.y = (wa == 0.f ? 0.f : wa * a.y) + (wb == 0.f ? 0.f : wb * c.y);
-      v.z = (wa == 0.f ? 0.f : wa * a.z) + (wb == 0.f ? 0.f : wb * c.z);
-      v.w = (wa == 0.f ? 0.f : wa * a.w) + (wb == 0.f ? 0.f : wb * c.w);
-      ro4[e] = v;
+#pragma unroll
+    for (int k = 0; k < kRowsPerTrip; ++k) {
+      const long long w = base + k * warps;
+      if (w < rows) {
+        const float mx = fmaxf(la[k], lb[k]);
+        float wa = 0.f, wb = 0.f, out_lse = -INFINITY;
+        if (mx != -INFINITY) {
+          wa = (la[k] == -INFINITY) ? 0.f : expf(la[k] - mx);
+          wb = (lb[k] == -INFINITY) ? 0.f : expf(lb[k] - mx);
+          const float den = wa + wb;
+          out_lse = mx + logf(den);
+          wa /= den;
+          wb /= den;
+        }
+        if (col) {
+          const float4 a = va[k], c = vb[k];
+          float4 x;
+          x.x = (wa == 0.f ? 0.f : wa * a.x) + (wb == 0.f ? 0.f : wb * c.x);
+          x.y = (wa == 0.f ? 0.f : wa * a.y) + (wb == 0.f ? 0.f : wb * c.y);
+          x.z = (wa == 0.f ? 0.f : wa * a.z) + (wb == 0.f ? 0.f : wb * c.z);
+          x.w = (wa == 0.f ? 0.f : wa * a.w) + (wb == 0.f ? 0.f : wb * c.w);
+          reinterpret_cast<float4 *>(o + row_offset(w, Lq, h, d))[lane] = x;
+        }
+        __syncwarp();
+        if (lane == 0) lse[w] = out_lse;
+      }
     }
-    __syncwarp();
-    if (lane == 0) lse[w] = out_lse;
+  }
+}
+
+// Empty online-softmax states for `splits` key splits: m = -inf, l = 0,
+// O = 0 (m_rows = splits * b * h * Lq entries, o_vals = m_rows * d; l may be
+// null).
+__global__ void state_init_kernel(float *m, float *l, float *o, long long m_rows,
+                                  long long o_vals) {
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; t < o_vals / 4;
+       t += stride) {
+    reinterpret_cast<float4 *>(o)[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (t < m_rows) {
+      m[t] = -INFINITY;
+      if (l) l[t] = 0.f;
+    }
+  }
+}
+
+// Combination of the unnormalised states of `splits` disjoint key ranges
+// (the second page's rescale-merge, over any number of parts):
+//   M = max_s m_s,  L = sum_s l_s e^(m_s - M),
+//   out = sum_s e^(m_s - M) O_s / L,  lse = M + ln L;
+// rows no key reaches (L = 0) get 0 and -inf.  One warp per (batch, head,
+// row); lane e holds columns 4e..4e+3.  State slices are split_rows =
+// b * h * Lq rows apart (m, l) and split_rows * d floats apart (O).
+__global__ void combine_kernel(const float *m, const float *l, const float *o, int splits,
+                               float *out, float *lse, int b, long long Lq, int h, int d) {
+  const long long rows = static_cast<long long>(b) * h * Lq;
+  const int lane = threadIdx.x & 31;
+  const bool col = lane < d / 4;
+  const long long warps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
+  for (long long w = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+       w < rows; w += warps) {
+    float mx = -INFINITY;
+    for (int z = lane; z < splits; z += 32) mx = fmaxf(mx, m[z * rows + w]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    float den = 0.f;
+    for (int z = lane; z < splits; z += 32) {
+      const float mz = m[z * rows + w];
+      if (mz != -INFINITY) den += l[z * rows + w] * expf(mz - mx);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
+    const bool live = mx != -INFINITY && den > 0.f;
+    const size_t orow = row_offset(w, Lq, h, d);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (live && col) {
+      for (int z = 0; z < splits; ++z) {
+        const float mz = m[z * rows + w];
+        if (mz == -INFINITY) continue;
+        const float wz = expf(mz - mx) / den;
+        const float4 v = reinterpret_cast<const float4 *>(o + z * rows * d + orow)[lane];
+        acc.x += wz * v.x;
+        acc.y += wz * v.y;
+        acc.z += wz * v.z;
+        acc.w += wz * v.w;
+      }
+    }
+    if (col) reinterpret_cast<float4 *>(out + orow)[lane] = acc;
+    if (lane == 0) lse[w] = live ? mx + logf(den) : -INFINITY;
   }
 }
 
@@ -169,6 +273,23 @@ cudaError_t launch_merge(const float *o_a, const float *lse_a, const float *o_b,
   if (rows == 0) return cudaSuccess;
   merge_kernel<<<ew_grid(rows * 32), kEwThreads, 0, stream>>>(o_a, lse_a, o_b, lse_b, o, lse, b,
                                                               Lq, h, d);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_state_init(float *m, float *l, float *o, long long m_rows, int d,
+                              cudaStream_t stream) {
+  const long long o_vals = m_rows * d;
+  if (o_vals == 0) return cudaSuccess;
+  state_init_kernel<<<ew_grid(o_vals / 4), kEwThreads, 0, stream>>>(m, l, o, m_rows, o_vals);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const float *m, const float *l, const float *o, int splits, float *out,
+                           float *lse, int b, long long Lq, int h, int d, cudaStream_t stream) {
+  const long long rows = static_cast<long long>(b) * h * Lq;
+  if (rows == 0) return cudaSuccess;
+  combine_kernel<<<ew_grid(rows * 32), kEwThreads, 0, stream>>>(m, l, o, splits, out, lse, b, Lq,
+                                                                h, d);
   return cudaGetLastError();
 }
 

@@ -135,6 +135,30 @@ def test_ex2_probe_validation(lib):
     assert lib.ra_ex2_probe(16, FAKE, n - 1, None) == binding.RA_ERR_INVALID_ARG
 
 
+def test_prefill_validation_and_workspace(lib):
+    lib.ra_prefill_workspace_size.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
+                                              binding.Dims]
+    lib.ra_prefill_workspace_size.restype = ctypes.c_size_t
+    d = _dims(b=1, h=8, n_kv=2, d=128)
+    # explicit split counts: n_splits states of (m, l, O) per query row
+    assert lib.ra_prefill_workspace_size(256, 4096, 4, d) == 4 * 8 * 256 * (2 + 128) * 4
+    # never more splits than key tiles, and no empty split
+    assert lib.ra_prefill_workspace_size(256, 300, 8, d) == 3 * 8 * 256 * 130 * 4
+    assert lib.ra_prefill_workspace_size(256, 1280, 4, d) == 4 * 8 * 256 * 130 * 4
+    assert lib.ra_prefill_workspace_size(256, 1280, 6, d) == 5 * 8 * 256 * 130 * 4
+    assert lib.ra_prefill_workspace_size(0, 4096, 4, d) == 0
+    args = [FAKE] * 7
+    assert lib.ra_chunked_prefill(*args, 256, 4096, 65, d, 1, 0.0, FAKE, 1 << 30, None) == \
+        binding.RA_ERR_INVALID_ARG                      # too many splits
+    assert lib.ra_chunked_prefill(*args[:5], None, None, 256, 4096, 0, d, 1, 0.0, FAKE, 1 << 30,
+                                  None) == binding.RA_ERR_INVALID_ARG   # causal without positions
+    assert lib.ra_chunked_prefill(*args, 256, 4096, 4, d, 1, 0.0, None, 0, None) == \
+        binding.RA_ERR_WORKSPACE
+    assert lib.ra_chunked_prefill(*args, 256, 4096, 4, d, 1, 0.0, FAKE, 16, None) == \
+        binding.RA_ERR_WORKSPACE
+    assert lib.ra_chunked_prefill(*args, 0, 4096, 4, d, 1, 0.0, None, 0, None) == binding.RA_OK
+
+
 def test_workspace_size(lib):
     lib.ra_bwd_workspace_size.argtypes = [ctypes.c_int64, ctypes.c_int, binding.Dims]
     n = lib.ra_bwd_workspace_size(65536, 16, _dims(b=2, h=32, n_kv=8))

@@ -187,6 +187,41 @@ def test_block_steps_over_ring_reproduce_full_attention(orc, layout):
     _cmp(out, lse, ref_o, ref_l)
 
 
+@pytest.mark.parametrize("Lq,Lk,causal,g,d,splits", [
+    (256, 4096, True, 4, 128, 0), (256, 4096, True, 4, 128, 1), (256, 4096, True, 4, 128, 5),
+    (200, 1000, True, 2, 64, 3), (128, 2048, False, 1, 128, 0), (384, 640, True, 3, 128, 64),
+    # splits of >= 4096 visible keys per row take the plain bf16 P path
+    (256, 16384, True, 4, 128, 2), (128, 12288, False, 2, 64, 0),
+])
+def test_chunked_prefill_matches_oracle(orc, Lq, Lk, causal, g, d, splits):
+    """The last Lq tokens of an Lk-token sequence attend to all Lk keys
+    (their own included), keys split over concurrent block steps."""
+    n_kv = 2
+    h = g * n_kv
+    q, _, _ = make_inputs(1, Lq, h, n_kv, d, seed=Lq + 5)
+    _, k, v = make_inputs(1, Lk, h, n_kv, d, seed=Lk + 6)
+    q_pos = np.arange(Lk - Lq, Lk, dtype=np.int32)
+    k_pos = np.arange(Lk, dtype=np.int32)
+    st = orc.new_state(1, Lq, h, d)
+    orc.block_update(q, k, v, q_pos, k_pos, causal, 1.0 / np.sqrt(d), st)
+    ref_o, ref_l = orc.finalize(st)
+    qd, kd, vd = _dev(q, k, v)
+    qp, kp = (torch.from_numpy(x).cuda() for x in (q_pos, k_pos))
+    out, lse = ra.chunked_prefill(qd, kd, vd, qp, kp, causal, n_splits=splits)
+    ra.stream_check()
+    _cmp(out, lse, ref_o, ref_l)
+
+
+def test_chunked_prefill_without_keys():
+    q, k, v = _dev(*make_inputs(1, 128, 4, 2, 64, seed=1))
+    pos = torch.arange(128, dtype=torch.int32, device="cuda")
+    out, lse = ra.chunked_prefill(q, k[:, :0].contiguous(), v[:, :0].contiguous(), pos,
+                                  pos[:0].contiguous(), True)
+    ra.stream_check()
+    assert torch.count_nonzero(out).item() == 0
+    assert torch.isneginf(lse).all().item()
+
+
 def test_merge_matches_oracle(orc):
     b, S, h, n_kv, d = 1, 512, 4, 2, 128
     q, k, v = make_inputs(b, S, h, n_kv, d, seed=12)
