@@ -102,6 +102,26 @@ ORC_API void orc_ring_order(int N, int32_t *order)
 }
 
 /* ------------------------------------------------------------------------ */
+/* Keys query token t sees, as the interval [j0, j1).  Without documents all
+ * S keys, or under the causal rule keys 0..t.  Packed documents ([P3 section
+ * 5], "packing" with a block-diagonal mask): doc_start / doc_end [b, S] give
+ * the first token and one past the last token of t's document, and t sees
+ * only keys of its own document (and, causal, not after t).               */
+static void visible_keys(int64_t t, int64_t S, int causal, const int64_t *doc_start,
+                         const int64_t *doc_end, int bb, int64_t *j0, int64_t *j1)
+{
+    int64_t lo = 0, hi = S;
+    if (doc_start) {
+        lo = doc_start[(int64_t)bb * S + t];
+        hi = doc_end[(int64_t)bb * S + t];
+    }
+    if (causal && t + 1 < hi)
+        hi = t + 1;
+    *j0 = lo;
+    *j1 = hi;
+}
+
+/* ------------------------------------------------------------------------ */
 /* Direct definition, [P1 "The Memory and Communication Bottlenecks"] with the
  * causal rule of [P3 section 6] and GQA head sharing of [P3 section 2]:
  *   s_tj  = scale * <q_t, k_j>          for visible keys j
@@ -114,7 +134,8 @@ ORC_API void orc_attn_fwd_rows(const double *q_rows, const double *k,
                                const double *v, int b, int64_t S, int h,
                                int n_kv, int d, int causal, double scale,
                                const int64_t *rows, int64_t R, double *out,
-                               double *lse)
+                               double *lse, const int64_t *doc_start,
+                               const int64_t *doc_end)
 {
     const int g = h / n_kv;
     const int64_t total = (int64_t)b * R * h;
@@ -129,27 +150,28 @@ ORC_API void orc_attn_fwd_rows(const double *q_rows, const double *k,
             const int64_t t = rows[ri];
             const int kh = hq / g;
             const double *qt = q_rows + (((int64_t)bb * R + ri) * h + hq) * d;
-            const int64_t nvis = causal ? (t + 1 < S ? t + 1 : S) : S;
+            int64_t j0, nvis;
+            visible_keys(t, S, causal, doc_start, doc_end, bb, &j0, &nvis);
             double *o = out + (((int64_t)bb * R + ri) * h + hq) * d;
             double *ls = lse + ((int64_t)bb * h + hq) * R + ri;
             for (int e = 0; e < d; ++e)
                 o[e] = 0.0;
-            if (nvis <= 0) {
+            if (nvis <= j0) {
                 *ls = -INFINITY;
                 continue;
             }
             double mx = -INFINITY;
-            for (int64_t j = 0; j < nvis; ++j) {
+            for (int64_t j = j0; j < nvis; ++j) {
                 s[j] = scale * dot(qt, k + (((int64_t)bb * S + j) * n_kv + kh) * d, d);
                 if (s[j] > mx)
                     mx = s[j];
             }
             double sum = 0.0;
-            for (int64_t j = 0; j < nvis; ++j)
+            for (int64_t j = j0; j < nvis; ++j)
                 sum += exp(s[j] - mx);
             const double lse_t = mx + log(sum);
             *ls = lse_t;
-            for (int64_t j = 0; j < nvis; ++j) {
+            for (int64_t j = j0; j < nvis; ++j) {
                 const double p = exp(s[j] - lse_t);
                 const double *vj = v + (((int64_t)bb * S + j) * n_kv + kh) * d;
                 for (int e = 0; e < d; ++e)
@@ -177,7 +199,8 @@ ORC_API void orc_attn_bwd_rows(const double *q_rows, const double *k,
                                const double *v, const double *dout_rows, int b,
                                int64_t S, int h, int n_kv, int d, int causal,
                                double scale, const int64_t *rows, int64_t R,
-                               double *dq_rows, double *dk, double *dv)
+                               double *dq_rows, double *dk, double *dv,
+                               const int64_t *doc_start, const int64_t *doc_end)
 {
     const int g = h / n_kv;
     memset(dk, 0, sizeof(double) * (size_t)b * (size_t)S * n_kv * d);
@@ -194,32 +217,33 @@ ORC_API void orc_attn_bwd_rows(const double *q_rows, const double *k,
                 for (int hq = kh * g; hq < (kh + 1) * g; ++hq)
                     for (int64_t ri = 0; ri < R; ++ri) {
                         const int64_t t = rows[ri];
-                        const int64_t nvis = causal ? (t + 1 < S ? t + 1 : S) : S;
-                        if (nvis <= 0)
+                        int64_t j0, nvis;
+                        visible_keys(t, S, causal, doc_start, doc_end, bb, &j0, &nvis);
+                        if (nvis <= j0)
                             continue;
                         const double *qt = q_rows + (((int64_t)bb * R + ri) * h + hq) * d;
                         const double *gt = dout_rows + (((int64_t)bb * R + ri) * h + hq) * d;
                         double *dq = dq_rows + (((int64_t)bb * R + ri) * h + hq) * d;
                         double mx = -INFINITY;
-                        for (int64_t j = 0; j < nvis; ++j) {
+                        for (int64_t j = j0; j < nvis; ++j) {
                             p[j] = scale * dot(qt, k + (((int64_t)bb * S + j) * n_kv + kh) * d, d);
                             if (p[j] > mx)
                                 mx = p[j];
                         }
                         double sum = 0.0;
-                        for (int64_t j = 0; j < nvis; ++j)
+                        for (int64_t j = j0; j < nvis; ++j)
                             sum += exp(p[j] - mx);
                         const double lse_t = mx + log(sum);
                         for (int e = 0; e < d; ++e)
                             o[e] = 0.0;
-                        for (int64_t j = 0; j < nvis; ++j) {
+                        for (int64_t j = j0; j < nvis; ++j) {
                             p[j] = exp(p[j] - lse_t); /* scores -> weights P_tj */
                             const double *vj = v + (((int64_t)bb * S + j) * n_kv + kh) * d;
                             for (int e = 0; e < d; ++e)
                                 o[e] += p[j] * vj[e];
                         }
                         const double D = dot(gt, o, d);
-                        for (int64_t j = 0; j < nvis; ++j) {
+                        for (int64_t j = j0; j < nvis; ++j) {
                             const int64_t kv_off = (((int64_t)bb * S + j) * n_kv + kh) * d;
                             const double ds = p[j] * (dot(gt, v + kv_off, d) - D);
                             const double *kj = k + kv_off;

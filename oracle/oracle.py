@@ -61,10 +61,10 @@ def _load():
             lib.orc_ring_order.argtypes = [i32, P]
             lib.orc_ring_order.restype = None
             lib.orc_attn_fwd_rows.argtypes = [P, P, P, i32, i64, i32, i32, i32,
-                                              i32, dbl, P, i64, P, P]
+                                              i32, dbl, P, i64, P, P, P, P]
             lib.orc_attn_fwd_rows.restype = None
             lib.orc_attn_bwd_rows.argtypes = [P, P, P, P, i32, i64, i32, i32,
-                                              i32, i32, dbl, P, i64, P, P, P]
+                                              i32, i32, dbl, P, i64, P, P, P, P, P]
             lib.orc_attn_bwd_rows.restype = None
             lib.orc_block_update.argtypes = [P, P, P, P, P, i32, i64, i64, i32,
                                              i32, i32, i32, dbl, P, P, P]
@@ -127,9 +127,39 @@ def ring_order(N: int) -> np.ndarray:
     return out.reshape(N, N)
 
 
-def attn_fwd_rows(q, k, v, causal: bool, scale: float | None = None, rows=None):
+def doc_bounds(cu_seqlens, S: int):
+    """Per-token document bounds from packed-document offsets.
+    cu_seqlens [b, n_docs + 1] (non-decreasing, from 0 to S): token t of
+    batch row bb belongs to the document [cu[d], cu[d+1]) containing it.
+    Returns (doc_start, doc_end) as int64 [b, S]."""
+    cu = np.asarray(cu_seqlens, np.int64)
+    if cu.ndim == 1:
+        cu = cu[None]
+    starts = np.empty((cu.shape[0], S), np.int64)
+    ends = np.empty((cu.shape[0], S), np.int64)
+    for bb in range(cu.shape[0]):
+        assert cu[bb, 0] == 0 and cu[bb, -1] == S and np.all(np.diff(cu[bb]) >= 0)
+        lens = np.diff(cu[bb])
+        starts[bb] = np.repeat(cu[bb, :-1], lens)
+        ends[bb] = np.repeat(cu[bb, 1:], lens)
+    return starts, ends
+
+
+def _docs(cu_seqlens, b: int, S: int):
+    if cu_seqlens is None:
+        return None, None, None, None
+    ds, de = doc_bounds(cu_seqlens, S)
+    if ds.shape[0] == 1 and b > 1:
+        ds, de = np.repeat(ds, b, axis=0), np.repeat(de, b, axis=0)
+    ds, de = np.ascontiguousarray(ds), np.ascontiguousarray(de)
+    return ds, de, _ptr(ds), _ptr(de)
+
+
+def attn_fwd_rows(q, k, v, causal: bool, scale: float | None = None, rows=None,
+                  cu_seqlens=None):
     """Direct definition softmax(scale*QK^T)V with the causal rule and GQA
-    sharing, on the listed query rows (natural token order).
+    sharing, on the listed query rows (natural token order).  With
+    cu_seqlens (packed documents) a token sees only keys of its document.
 
     q [b,S,h,d], k/v [b,S,n_kv,d] (bf16 tensors or float arrays).
     Returns out [b,R,h,d], lse [b,h,R] as float64."""
@@ -144,13 +174,15 @@ def attn_fwd_rows(q, k, v, causal: bool, scale: float | None = None, rows=None):
     qr, kd, vd = _gather_rows(q, rows), _f64(k), _f64(v)
     out = np.empty((b, R, h, d), np.float64)
     lse = np.empty((b, h, R), np.float64)
+    ds, de, pds, pde = _docs(cu_seqlens, b, S)
     lib.orc_attn_fwd_rows(_ptr(qr), _ptr(kd), _ptr(vd), b, S, h, n_kv, d,
                           int(bool(causal)), float(scale), _ptr(rows), R,
-                          _ptr(out), _ptr(lse))
+                          _ptr(out), _ptr(lse), pds, pde)
     return out, lse
 
 
-def attn_bwd_rows(q, k, v, dout, causal: bool, scale: float | None = None, rows=None):
+def attn_bwd_rows(q, k, v, dout, causal: bool, scale: float | None = None, rows=None,
+                  cu_seqlens=None):
     """Analytic gradient of the direct definition with dO restricted to the
     listed rows.  Returns dq_rows [b,R,h,d], dk [b,S,n_kv,d], dv [b,S,n_kv,d]."""
     lib = _load()
@@ -165,9 +197,10 @@ def attn_bwd_rows(q, k, v, dout, causal: bool, scale: float | None = None, rows=
     dq = np.empty((b, R, h, d), np.float64)
     dk = np.empty((b, S, n_kv, d), np.float64)
     dv = np.empty((b, S, n_kv, d), np.float64)
+    ds, de, pds, pde = _docs(cu_seqlens, b, S)
     lib.orc_attn_bwd_rows(_ptr(qr), _ptr(kd), _ptr(vd), _ptr(gr), b, S, h, n_kv,
                           d, int(bool(causal)), float(scale), _ptr(rows), R,
-                          _ptr(dq), _ptr(dk), _ptr(dv))
+                          _ptr(dq), _ptr(dk), _ptr(dv), pds, pde)
     return dq, dk, dv
 
 

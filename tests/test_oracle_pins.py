@@ -354,3 +354,75 @@ def test_gradient_sum_invariants(orc):
     np.testing.assert_allclose(dk.sum(1), 0.0, atol=1e-11)
     gd = do.to(torch.float64).numpy().reshape(b, S, n_kv, h // n_kv, d)
     np.testing.assert_allclose(dv.sum(1), gd.sum(axis=(1, 3)), atol=1e-11)
+
+
+# ---------------------------------------------------------------- packed documents
+# The third page's section 5: documents packed end to end into one window, a
+# block-diagonal mask keeping every document to itself.
+PACKS = [
+    # S, cu_seqlens per batch row
+    (96, [[0, 17, 40, 40, 96], [0, 96, 96, 96, 96]]),   # an empty document; one spanning all
+    (64, [[0, 1, 2, 3, 64], [0, 30, 31, 63, 64]]),      # one-token documents
+]
+
+
+def _per_document(q, k, v, do, cu, causal, fn):
+    """Run fn on every document slice of every batch row separately."""
+    res = []
+    for bb, offs in enumerate(cu):
+        parts = []
+        for s0, s1 in zip(offs[:-1], offs[1:]):
+            if s1 > s0:
+                sl = slice(s0, s1)
+                args = [x[bb:bb + 1, sl] for x in (q, k, v)] + ([do[bb:bb + 1, sl]] if do is not None else [])
+                parts.append(((s0, s1), fn(*args, causal)))
+        res.append(parts)
+    return res
+
+
+@pytest.mark.parametrize("S,cu", PACKS)
+@pytest.mark.parametrize("causal", [True, False])
+def test_packed_forward_equals_independent_documents(orc, S, cu, causal):
+    q, k, v = make_inputs(2, S, 4, 2, 16, seed=S)
+    o, l = orc.attn_fwd_rows(q, k, v, causal, cu_seqlens=cu)
+    for bb, parts in enumerate(_per_document(q, k, v, None, cu, causal, orc.attn_fwd_rows)):
+        for (s0, s1), (od, ld) in parts:
+            np.testing.assert_array_equal(o[bb, s0:s1], od[0])
+            np.testing.assert_array_equal(l[bb, :, s0:s1], ld[0])
+
+
+@pytest.mark.parametrize("S,cu", PACKS)
+@pytest.mark.parametrize("causal", [True, False])
+def test_packed_backward_equals_independent_documents(orc, S, cu, causal):
+    q, k, v, do = make_inputs(2, S, 4, 2, 16, seed=S + 1, with_dout=True)
+    dq, dk, dv = orc.attn_bwd_rows(q, k, v, do, causal, cu_seqlens=cu)
+    for bb, parts in enumerate(_per_document(q, k, v, do, cu, causal, orc.attn_bwd_rows)):
+        for (s0, s1), (dqd, dkd, dvd) in parts:
+            np.testing.assert_array_equal(dq[bb, s0:s1], dqd[0])
+            np.testing.assert_array_equal(dk[bb, s0:s1], dkd[0])
+            np.testing.assert_array_equal(dv[bb, s0:s1], dvd[0])
+
+
+def test_packed_mask_matches_brute_force(orc):
+    """An explicit S x S mask from document ids (same document, and key <=
+    query) with scipy's softmax, against the oracle's interval rule."""
+    S, cu = 40, [0, 7, 19, 40]
+    q, k, v = make_inputs(1, S, 2, 1, 8, seed=3)
+    doc = np.repeat(np.arange(3), np.diff(cu))
+    mask = (doc[:, None] == doc[None, :]) & (np.arange(S)[None, :] <= np.arange(S)[:, None])
+    qd, kd, vd = (x.double().numpy() for x in (q, k, v))
+    o, l = orc.attn_fwd_rows(q, k, v, True, cu_seqlens=[cu])
+    for hq in range(2):
+        s = qd[0, :, hq] @ kd[0, :, 0].T / np.sqrt(8)
+        s = np.where(mask, s, -np.inf)
+        np.testing.assert_allclose(l[0, hq], logsumexp(s, axis=1), atol=1e-12)
+        np.testing.assert_allclose(o[0, :, hq], softmax(s, axis=1) @ vd[0, :, 0], atol=1e-12)
+
+
+def test_single_document_is_the_unpacked_definition(orc):
+    q, k, v = make_inputs(1, 50, 2, 2, 8, seed=4)
+    for causal in (True, False):
+        o1, l1 = orc.attn_fwd_rows(q, k, v, causal)
+        o2, l2 = orc.attn_fwd_rows(q, k, v, causal, cu_seqlens=[[0, 50]])
+        np.testing.assert_array_equal(o1, o2)
+        np.testing.assert_array_equal(l1, l2)
