@@ -133,6 +133,27 @@ ra_status ra_ring_attention(const uint16_t *q, const uint16_t *k, const uint16_t
                             float *lse, int64_t S, int n_shards, ra_layout layout, int causal,
                             float scale, ra_dims dims, void *stream);
 
+/* Packed documents (the third page's section 5: documents packed end to end
+ * into one window, a block-diagonal mask keeping each to itself): as
+ * ra_ring_attention / ra_ring_attention_bwd, but a query sees only keys of
+ * its own document (and, causal, none after itself).  Key tiles no query of
+ * a tile can see are skipped, as causal ones are.
+ *   cu_seqlens: device int32 [b][n_docs + 1], document offsets of each batch
+ *   row, from 0 to S, non-decreasing (empty documents allowed); the contents
+ *   are not checked on the host.  n_docs >= 1.
+ * Precision: query tiles with a row that sees fewer than 4096 keys (a row
+ * near the start of a document) take the hi + lo bf16 path. */
+ra_status ra_ring_attention_packed(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                                   float *out, float *lse, int64_t S, int n_shards,
+                                   ra_layout layout, int causal, float scale, ra_dims dims,
+                                   const int32_t *cu_seqlens, int n_docs, void *stream);
+ra_status ra_ring_attention_packed_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                                       const float *out, const float *lse, const uint16_t *dout,
+                                       float *dq, float *dk, float *dv, void *workspace,
+                                       size_t workspace_bytes, int64_t S, int n_shards,
+                                       ra_layout layout, int causal, float scale, ra_dims dims,
+                                       const int32_t *cu_seqlens, int n_docs, void *stream);
+
 /* Chunked prefill: Lq new query tokens (positions q_pos) attend to Lk
  * resident keys (positions k_pos) -- the first page's inference remark, a
  * block step with Lq much smaller than Lk.  The keys are cut into n_splits

@@ -60,6 +60,9 @@ def load(path: str | None = None):
             "ra_finalize": [P, P, P, P, I64, Dims, P],
             "ra_merge": [P, P, P, P, P, P, I64, Dims, P],
             "ra_ring_attention": [P, P, P, P, P, I64, I, I, I, F, Dims, P],
+            "ra_ring_attention_packed": [P, P, P, P, P, I64, I, I, I, F, Dims, P, I, P],
+            "ra_ring_attention_packed_bwd": [P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, I64,
+                                             I, I, I, F, Dims, P, I, P],
             "ra_ring_attention_bwd": [P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, I64, I, I, I,
                                       F, Dims, P],
             "ra_position_map": [I, I64, I, P, P, P, P],
@@ -129,10 +132,23 @@ def _bits(t):
 
 
 # ---------------------------------------------------------------- forward
+def _docs(cu_seqlens, b):
+    """(pointer, n_docs) of packed-document offsets as int32 [b, n_docs + 1]."""
+    if cu_seqlens is None:
+        return None, 0, None
+    _need(cu_seqlens, torch.int32, "cu_seqlens")
+    cu = cu_seqlens if cu_seqlens.dim() == 2 else cu_seqlens.unsqueeze(0).expand(b, -1)
+    cu = cu.contiguous()
+    if cu.shape[0] != b:
+        raise RAError(RA_ERR_INVALID_ARG, "cu_seqlens needs one row per batch row")
+    return _ptr(cu), cu.shape[1] - 1, cu
+
+
 def ring_attention(q, k, v, n_shards: int, layout: int = STRIPED, causal: bool = True,
-                   scale: float = 0.0, out=None, lse=None, stream=None):
+                   scale: float = 0.0, out=None, lse=None, stream=None, cu_seqlens=None):
     """Exact attention over N virtual shards in ring order (one fused launch).
     q [b,S,h,d], k/v [b,S,n_kv,d] bf16 CUDA tensors in natural token order.
+    cu_seqlens (int32 [b, n_docs+1] or [n_docs+1]): packed documents.
     Returns (out [b,S,h,d] float32, lse [b,h,S] float32)."""
     lib = load()
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
@@ -145,9 +161,16 @@ def ring_attention(q, k, v, n_shards: int, layout: int = STRIPED, causal: bool =
         lse = torch.empty((b, h, S), dtype=torch.float32, device=q.device)
     _need(out, torch.float32, "out")
     _need(lse, torch.float32, "lse")
-    _check(lib.ra_ring_attention(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), S,
-                                 int(n_shards), int(layout), int(bool(causal)), float(scale),
-                                 _dims(b, h, n_kv, d), _stream(stream)))
+    cu_p, n_docs, _keep = _docs(cu_seqlens, b)
+    if cu_p is None:
+        _check(lib.ra_ring_attention(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), S,
+                                     int(n_shards), int(layout), int(bool(causal)), float(scale),
+                                     _dims(b, h, n_kv, d), _stream(stream)))
+    else:
+        _check(lib.ra_ring_attention_packed(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), S,
+                                            int(n_shards), int(layout), int(bool(causal)),
+                                            float(scale), _dims(b, h, n_kv, d), cu_p, n_docs,
+                                            _stream(stream)))
     return out, lse
 
 
@@ -243,7 +266,7 @@ def bwd_workspace_size(S: int, n_shards: int, b: int, h: int, n_kv: int, d: int)
 
 def ring_attention_bwd(q, k, v, out, lse, dout, n_shards: int, layout: int = STRIPED,
                        causal: bool = True, scale: float = 0.0, dq=None, dk=None, dv=None,
-                       workspace=None, stream=None):
+                       workspace=None, stream=None, cu_seqlens=None):
     """Gradients (dq, dk, dv) as float32, recomputing P from the saved LSE."""
     lib = load()
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (dout, "dout")):
@@ -258,11 +281,14 @@ def ring_attention_bwd(q, k, v, out, lse, dout, n_shards: int, layout: int = STR
     ws_bytes = bwd_workspace_size(S, n_shards, b, h, n_kv, d)
     if workspace is None:
         workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=q.device)
-    _check(lib.ra_ring_attention_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout),
-                                     _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace),
-                                     workspace.numel() * workspace.element_size(), S,
-                                     int(n_shards), int(layout), int(bool(causal)), float(scale),
-                                     _dims(b, h, n_kv, d), _stream(stream)))
+    cu_p, n_docs, _keep = _docs(cu_seqlens, b)
+    args = (_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
+            _ptr(dv), _ptr(workspace), workspace.numel() * workspace.element_size(), S,
+            int(n_shards), int(layout), int(bool(causal)), float(scale), _dims(b, h, n_kv, d))
+    if cu_p is None:
+        _check(lib.ra_ring_attention_bwd(*args, _stream(stream)))
+    else:
+        _check(lib.ra_ring_attention_packed_bwd(*args, cu_p, n_docs, _stream(stream)))
     return dq, dk, dv
 
 

@@ -65,6 +65,15 @@ bool known_layout(int layout) {
          layout == RA_LAYOUT_ZIGZAG;
 }
 
+// Packed documents: offsets [b][n_docs + 1] on the device (contents are the
+// caller's contract and are not read on the host).
+ra_status check_docs(const int32_t *cu, int n_docs) {
+  if (cu == nullptr) return n_docs == 0 ? RA_OK : fail(RA_ERR_INVALID_ARG, "n_docs without cu_seqlens");
+  if (n_docs < 1 || n_docs > (1 << 30))
+    return fail(RA_ERR_INVALID_ARG, "n_docs must be in 1 .. 2^30 (got %d)", n_docs);
+  return RA_OK;
+}
+
 // Zig-zag shards are two half-blocks of S / 2N tokens each; the attention
 // kernels need every 128-row tile inside one half-block.
 ra_status check_zigzag_tiles(int layout, int64_t S, int n_shards) {
@@ -409,9 +418,10 @@ ra_status ra_chunked_prefill(const uint16_t *q, const uint16_t *k, const uint16_
   return e == cudaSuccess ? RA_OK : cuda_fail(e, "combine launch");
 }
 
-ra_status ra_ring_attention(const uint16_t *q, const uint16_t *k, const uint16_t *v, float *out,
-                            float *lse, int64_t S, int n_shards, ra_layout layout, int causal,
-                            float scale, ra_dims dims, void *stream) {
+ra_status ra_ring_attention_packed(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                                   float *out, float *lse, int64_t S, int n_shards,
+                                   ra_layout layout, int causal, float scale, ra_dims dims,
+                                   const int32_t *cu_seqlens, int n_docs, void *stream) {
   ra_status st;
   if ((st = check_dims(dims)) != RA_OK) return st;
   if (!known_layout(layout)) return fail(RA_ERR_INVALID_ARG, "unknown layout %d", (int)layout);
@@ -427,6 +437,7 @@ ra_status ra_ring_attention(const uint16_t *q, const uint16_t *k, const uint16_t
   RA_CHECK_PTR(v);
   RA_CHECK_PTR(out);
   RA_CHECK_PTR(lse);
+  if ((st = check_docs(cu_seqlens, n_docs)) != RA_OK) return st;
   float sc = 0.f;
   if ((st = resolve_scale(scale, dims.d, &sc)) != RA_OK) return st;
   const long long L = S / n_shards;
@@ -447,7 +458,16 @@ ra_status ra_ring_attention(const uint16_t *q, const uint16_t *k, const uint16_t
   p.block_mode = 0;
   p.out = out;
   p.lse = lse;
+  p.cu = cu_seqlens;
+  p.n_docs = n_docs;
   return launch_attention(p, dims.d, q, k, v, L, L, static_cast<cudaStream_t>(stream));
+}
+
+ra_status ra_ring_attention(const uint16_t *q, const uint16_t *k, const uint16_t *v, float *out,
+                            float *lse, int64_t S, int n_shards, ra_layout layout, int causal,
+                            float scale, ra_dims dims, void *stream) {
+  return ra_ring_attention_packed(q, k, v, out, lse, S, n_shards, layout, causal, scale, dims,
+                                  nullptr, 0, stream);
 }
 
 size_t ra_bwd_workspace_size(int64_t S, int n_shards, ra_dims dims) {
@@ -458,11 +478,12 @@ size_t ra_bwd_workspace_size(int64_t S, int n_shards, ra_dims dims) {
          static_cast<size_t>(Lpad) * sizeof(float);
 }
 
-ra_status ra_ring_attention_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
-                                const float *out, const float *lse, const uint16_t *dout,
-                                float *dq, float *dk, float *dv, void *workspace,
-                                size_t workspace_bytes, int64_t S, int n_shards, ra_layout layout,
-                                int causal, float scale, ra_dims dims, void *stream) {
+ra_status ra_ring_attention_packed_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                                       const float *out, const float *lse, const uint16_t *dout,
+                                       float *dq, float *dk, float *dv, void *workspace,
+                                       size_t workspace_bytes, int64_t S, int n_shards,
+                                       ra_layout layout, int causal, float scale, ra_dims dims,
+                                       const int32_t *cu_seqlens, int n_docs, void *stream) {
   ra_status st;
   if ((st = check_dims(dims)) != RA_OK) return st;
   if (!known_layout(layout)) return fail(RA_ERR_INVALID_ARG, "unknown layout %d", (int)layout);
@@ -482,6 +503,7 @@ ra_status ra_ring_attention_bwd(const uint16_t *q, const uint16_t *k, const uint
   RA_CHECK_PTR(dq);
   RA_CHECK_PTR(dk);
   RA_CHECK_PTR(dv);
+  if ((st = check_docs(cu_seqlens, n_docs)) != RA_OK) return st;
   const size_t need = ra_bwd_workspace_size(S, n_shards, dims);
   if (workspace == nullptr || workspace_bytes < need)
     return fail(RA_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need,
@@ -491,6 +513,8 @@ ra_status ra_ring_attention_bwd(const uint16_t *q, const uint16_t *k, const uint
   if ((st = resolve_scale(scale, dims.d, &sc)) != RA_OK) return st;
   const int64_t L = S / n_shards;
   BwdParams p{};
+  p.cu = cu_seqlens;
+  p.n_docs = n_docs;
   p.b = dims.b;
   p.h = dims.h;
   p.n_kv = dims.n_kv;
@@ -533,6 +557,16 @@ ra_status ra_ring_attention_bwd(const uint16_t *q, const uint16_t *k, const uint
   e = counted(launch_bwd(p, dims.d, out, lse, dout, qm, km, vm, dom, dqm, dkm, dvm, n_units,
                          sm_count(), cs), 2);
   return e == cudaSuccess ? RA_OK : cuda_fail(e, "backward launch");
+}
+
+ra_status ra_ring_attention_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                                const float *out, const float *lse, const uint16_t *dout,
+                                float *dq, float *dk, float *dv, void *workspace,
+                                size_t workspace_bytes, int64_t S, int n_shards, ra_layout layout,
+                                int causal, float scale, ra_dims dims, void *stream) {
+  return ra_ring_attention_packed_bwd(q, k, v, out, lse, dout, dq, dk, dv, workspace,
+                                      workspace_bytes, S, n_shards, layout, causal, scale, dims,
+                                      nullptr, 0, stream);
 }
 
 ra_status ra_position_map(ra_layout layout, int64_t S, int n_shards, int32_t *shard_of,

@@ -137,7 +137,8 @@ struct KvUnit {
   int bb, kh, j, c;   // batch, kv head, kv shard, kv tile
   int i, hq;          // the query shard and query head it meets
   int kmin, kmax;     // token positions of the tile's first and last existing key
-  int a_lo, a_full;   // visible query tiles a >= a_lo; unmasked ones a >= a_full
+  int a_lo, a_hi;     // query tiles [a_lo, a_hi) have a row that sees a key of the tile
+  int a_flo, a_fhi;   // query tiles [a_flo, a_fhi): every row sees every key (no mask)
 };
 
 // Units: one 128-key tile against one query shard and one query head of its
@@ -146,6 +147,7 @@ struct KvUnit {
 // tiles innermost, so the CTAs resident together read the same Q / dO tiles
 // and add their dQ partials into the same 64 KB dq tiles: one group's dq
 // rows (n_qtiles x 64 KB) stay in L2 while every key tile adds to them.
+template <bool kDocs>
 __device__ __forceinline__ KvUnit decode_kv_unit(const BwdParams &p, long long u) {
   KvUnit x;
   x.c = static_cast<int>(u % p.n_ktiles);
@@ -163,38 +165,101 @@ __device__ __forceinline__ KvUnit decode_kv_unit(const BwdParams &p, long long u
   const int r1 = min(r0 + kTile, p.L) - 1;
   x.kmin = token_at(p.layout, p.L, p.N, x.j, r0);
   x.kmax = token_at(p.layout, p.L, p.N, x.j, r1);
-  if (!p.causal) {
-    x.a_lo = 0;
-    x.a_full = 0;
-  } else {
-    // visible query tiles: those whose last row sees the tile's first key
-    const int r_vis = max(0, first_row_at_or_after(p.layout, p.L, p.N, x.i, x.kmin));
-    x.a_lo = r_vis >= p.L ? p.n_qtiles : r_vis / kTile;
-    // unmasked query tiles: every row sees the tile's last key
-    const int r_full = max(0, first_row_at_or_after(p.layout, p.L, p.N, x.i, x.kmax));
-    x.a_full = min(p.n_qtiles, (r_full + kTile - 1) / kTile);
+  if constexpr (!kDocs) {
+    x.a_hi = p.n_qtiles;
+    x.a_fhi = p.n_qtiles;
+    if (!p.causal) {
+      x.a_lo = 0;
+      x.a_flo = 0;
+    } else {
+      // visible query tiles: those whose last row sees the tile's first key
+      const int r_vis = max(0, first_row_at_or_after(p.layout, p.L, p.N, x.i, x.kmin));
+      x.a_lo = r_vis >= p.L ? p.n_qtiles : r_vis / kTile;
+      // unmasked query tiles: every row sees the tile's last key
+      const int r_full = max(0, first_row_at_or_after(p.layout, p.L, p.N, x.i, x.kmax));
+      x.a_flo = min(p.n_qtiles, (r_full + kTile - 1) / kTile);
+    }
+    return x;
   }
+  // A query at t sees key kp iff kp lies in t's document [ds, de) and, causal,
+  // kp <= t: iff t >= (causal ? kp : ds(kp)) and t < de(kp).  Query rows of
+  // shard i are increasing positions, so the rows that see some key of the
+  // tile and those that see all of them are row ranges.
+  int ds0, de0, ds1, de1;
+  doc_of(p.cu, p.n_docs, x.bb, p.S, x.kmin, ds0, de0);
+  doc_of(p.cu, p.n_docs, x.bb, p.S, x.kmax, ds1, de1);
+  const int r_vis = max(0, first_row_at_or_after(p.layout, p.L, p.N, x.i, p.causal ? x.kmin : ds0));
+  const int r_end = min(p.L, first_row_at_or_after(p.layout, p.L, p.N, x.i, de1));
+  const int r_flo = max(0, first_row_at_or_after(p.layout, p.L, p.N, x.i, p.causal ? x.kmax : ds1));
+  const int r_fhi = min(p.L, first_row_at_or_after(p.layout, p.L, p.N, x.i, de0));
+  x.a_lo = r_vis >= r_end ? p.n_qtiles : r_vis / kTile;
+  x.a_hi = r_vis >= r_end ? p.n_qtiles : (r_end + kTile - 1) / kTile;
+  x.a_flo = (r_flo + kTile - 1) / kTile;
+  x.a_fhi = r_fhi >= p.L ? p.n_qtiles : r_fhi / kTile;
   return x;
 }
 
 struct QIter {
   int a = INT_MAX;
+  int d0 = -1, d1 = -1;  // packed documents: documents of the tile's first and last rows
 };
+
+// Document index of position t, starting from a document index at or after
+// it (the query tiles are visited in decreasing position order).
+__device__ __forceinline__ int doc_walk(const int32_t *c, int n_docs, int d, int t) {
+  if (d < 0 || d >= n_docs) {  // first use: binary search
+    int lo = 0, hi = n_docs - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (c[mid] <= t)
+        lo = mid;
+      else
+        hi = mid - 1;
+    }
+    return lo;
+  }
+  while (d > 0 && c[d] > t) --d;
+  return d;
+}
 
 // Next query tile of the unit, from the last down to the first visible one
 // (every key tile of a group starts on the same query tile).  `partial` marks
-// steps that need the causal element mask; `split` steps whose query tile
-// has a row seeing fewer than kSplitKeys keys.
+// steps that need the element mask; `split` steps whose query tile has a row
+// seeing fewer than kSplitKeys keys.
+template <bool kDocs>
 __device__ __forceinline__ bool q_next(const BwdParams &p, const KvUnit &x, QIter &it, int &i,
                                        int &a, int &hq, bool &partial, bool &split) {
-  it.a = it.a == INT_MAX ? p.n_qtiles - 1 : it.a - 1;
+  if constexpr (!kDocs) {
+    it.a = it.a == INT_MAX ? p.n_qtiles - 1 : it.a - 1;
+    if (it.a < x.a_lo) return false;
+    i = x.i;
+    a = it.a;
+    hq = x.hq;
+    partial = it.a < x.a_flo;
+    split = p.causal ? (token_at(p.layout, p.L, p.N, x.i, it.a * kTile) + 1 < kSplitKeys)
+                     : (p.S < kSplitKeys);
+    return true;
+  }
+  it.a = it.a == INT_MAX ? x.a_hi - 1 : it.a - 1;
   if (it.a < x.a_lo) return false;
   i = x.i;
   a = it.a;
   hq = x.hq;
-  partial = it.a < x.a_full;
-  split = p.causal ? (token_at(p.layout, p.L, p.N, x.i, it.a * kTile) + 1 < kSplitKeys)
-                   : (p.S < kSplitKeys);
+  partial = it.a < x.a_flo || it.a >= x.a_fhi;
+  const int t0 = token_at(p.layout, p.L, p.N, x.i, it.a * kTile);
+  int minvis;
+  {
+    const int t1 = token_at(p.layout, p.L, p.N, x.i, min(it.a * kTile + kTile, p.L) - 1);
+    const int32_t *cb = p.cu + static_cast<size_t>(x.bb) * (p.n_docs + 1);
+    it.d0 = doc_walk(cb, p.n_docs, it.d0, t0);
+    it.d1 = doc_walk(cb, p.n_docs, it.d1, t1);
+    const int ds0 = cb[it.d0], de0 = cb[it.d0 + 1], ds1 = cb[it.d1], de1 = cb[it.d1 + 1];
+    if (p.causal)
+      minvis = ds1 > t0 ? 1 : t0 - ds0 + 1;  // a document starting inside: 1
+    else
+      minvis = de0 < ds1 ? 1 : min(de0 - ds0, de1 - ds1);
+  }
+  split = minvis < kSplitKeys;
   return true;
 }
 
@@ -264,7 +329,7 @@ __device__ __forceinline__ void store_p_half(const float (&pf)[64], uint32_t tS,
   }
 }
 
-template <int D>
+template <int D, bool kDocs>
 __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     bwd_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUtensorMap qmap,
                const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
@@ -273,8 +338,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                const __grid_constant__ CUtensorMap dkmap,
                const __grid_constant__ CUtensorMap dvmap) {
   using C = BwdCfg<D>;
-  const KvUnit x = decode_kv_unit(p, blockIdx.x);
-  if (x.a_lo >= p.n_qtiles) return;  // no query of this shard sees the tile: nothing to add
+  const KvUnit x = decode_kv_unit<kDocs>(p, blockIdx.x);
+  if (x.a_lo >= x.a_hi) return;  // no query of this shard sees the tile: nothing to add
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   if (pad > static_cast<uint32_t>(C::kSlack)) {  // uniform: never touch smem beyond the allocation
@@ -344,7 +409,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       QIter it;
       int i, a, hq, n = 0;
       bool partial, split;
-      while (q_next(p, x, it, i, a, hq, partial, split)) {
+      while (q_next<kDocs>(p, x, it, i, a, hq, partial, split)) {
         if (lane == 0) {
           int c2, c3;
           map_coords(p.layout, p.L, p.N, i, a * kTile, c2, c3);
@@ -401,7 +466,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         QIter it;
         int i, a, hq, n = 0;
         bool partial, split;
-        bool has = q_next(p, x, it, i, a, hq, partial, split);
+        bool has = q_next<kDocs>(p, x, it, i, a, hq, partial, split);
         if (has && lane == 0) {
           if (mbar_wait(&bars[C::bQFull + 0], 0, abort_flag, kSiteBMmaQ)) {
             tc_fence_after();
@@ -412,7 +477,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         __syncwarp();
         while (has && !*abort_flag) {
           const bool cur_split = split;
-          const bool has_next = q_next(p, x, it, i, a, hq, partial, split);
+          const bool has_next = q_next<kDocs>(p, x, it, i, a, hq, partial, split);
           if (lane == 0) {
             const int st = n % C::kQSt;
             const uint32_t q_s = sbase + C::kQOff + st * C::kTileBytes;
@@ -500,6 +565,16 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     const int kr = x.c * kTile + row;
     const bool key_exists = kr < p.L;
     const int kp = token_at(p.layout, p.L, p.N, x.j, key_exists ? kr : p.L - 1);
+    // this key is seen by the query rows [qr_lo, qr_hi) of shard x.i
+    int qr_lo = 0, qr_hi = 0;
+    if constexpr (kDocs) {
+      int kds, kde;
+      doc_of(p.cu, p.n_docs, x.bb, p.S, kp, kds, kde);
+      qr_lo = first_row_at_or_after(p.layout, p.L, p.N, x.i, p.causal ? kp : kds);
+      qr_hi = first_row_at_or_after(p.layout, p.L, p.N, x.i, kde);
+    } else {
+      qr_lo = first_row_at_or_after(p.layout, p.L, p.N, x.i, kp);
+    }
     const float sl2 = p.scale_log2;
     // this warpgroup's 64 query columns are one 128-byte-swizzled half of dS^T
     uint8_t *ds_row = smem + C::kDsOff + half * (kTile * 128) + row * 128;
@@ -507,15 +582,18 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     QIter it;
     int i, a, hq, n = 0;
     bool partial, split;
-    while (q_next(p, x, it, i, a, hq, partial, split)) {
+    while (q_next<kDocs>(p, x, it, i, a, hq, partial, split)) {
       // this step's LSE2 and D rows, staged by the producer with the Q tile
       const float4 *lse4 = reinterpret_cast<const float4 *>(
                                smem + C::kStatOff + (n % C::kQSt) * 2 * C::kRowStatBytes) +
                            cb / 4;
       const float4 *d4 = lse4 + kTile / 4;
-      // query columns cb + c with c < c0 are masked for this key
-      int c0 = 0;
-      if (partial) c0 = first_row_at_or_after(p.layout, p.L, p.N, i, kp) - a * kTile - cb;
+      // query columns cb + c with c < c0 or c >= c1 are masked for this key
+      int c0 = 0, c1 = C::kHalfCols;
+      if (partial) {
+        c0 = qr_lo - a * kTile - cb;
+        if constexpr (kDocs) c1 = qr_hi - a * kTile - cb;
+      }
       if (!key_exists) {
         c0 = C::kHalfCols;
         partial = true;
@@ -544,7 +622,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       if (partial) {  // causal diagonal: columns before c0 do not see this key
 #pragma unroll
         for (int c = 0; c < C::kHalfCols; ++c)
-          if (c < c0) pf[c] = 0.f;
+          if (c < c0 || (kDocs && c >= c1)) pf[c] = 0.f;
       }
       if (split)
         store_p_half<true>(pf, tS, cb);
@@ -633,7 +711,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     int i, a, hq, n = 0;
     bool partial, split;
     bool aborted = false;
-    while (q_next(p, x, it, i, a, hq, partial, split)) {
+    while (q_next<kDocs>(p, x, it, i, a, hq, partial, split)) {
       if (!__all_sync(kFull, mbar_wait(&bars[C::bDqFull], n & 1, abort_flag, kSiteBDq))) {
         aborted = true;
         break;
@@ -855,7 +933,7 @@ cudaError_t launch_bwd_t(const BwdParams &p, const float *out, const float *lse,
   bwd_pre_kernel<D><<<static_cast<unsigned int>(pre_blocks), 256, 0, stream>>>(p, out, lse, dout);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  auto kern = bwd_kernel<D>;
+  auto kern = p.cu != nullptr ? bwd_kernel<D, true> : bwd_kernel<D, false>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemAlloc);
   if (e != cudaSuccess) return e;
   {

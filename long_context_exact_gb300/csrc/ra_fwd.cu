@@ -100,6 +100,9 @@ struct Unit {
   int bb, kh, pr, i, a;
   int qmin, qmax;  // token positions of the tile's first and last existing row
   int kc0, kc1;    // block mode: key tiles [kc0, kc1) of this CTA's key split
+  // ring mode: key positions some row of the tile sees form [wlo, whi]; keys
+  // in [flo, fhi] are seen by every row; minvis = fewest keys any row sees
+  int wlo, whi, flo, fhi, minvis;
 };
 
 // Work-unit order: groups of (batch, kv head, query shard); inside a group the
@@ -138,13 +141,31 @@ __device__ __forceinline__ int warp_max(int v) {
 
 // Token positions covered by the unit's query tile.  Warp-collective in
 // block mode (positions come from q_pos).
-template <bool kBlock>
+template <bool kBlock, bool kDocs>
 __device__ __forceinline__ void unit_qrange(const FwdParams &p, Unit &x) {
   const int r0 = x.a * kTile;
   const int r1 = min(r0 + kTile, p.L) - 1;
   if constexpr (!kBlock) {
     x.qmin = token_at(p.layout, p.L, p.N, x.i, r0);
     x.qmax = token_at(p.layout, p.L, p.N, x.i, r1);
+    if constexpr (!kDocs) {
+      x.minvis = p.causal ? x.qmin + 1 : p.S;
+      return;
+    }
+    // Rows are increasing positions and document starts do not decrease
+    // with the position, so the tile's windows follow from its first and
+    // last rows.
+    int ds0, de0, ds1, de1;
+    doc_of(p.cu, p.n_docs, x.bb, p.S, x.qmin, ds0, de0);
+    doc_of(p.cu, p.n_docs, x.bb, p.S, x.qmax, ds1, de1);
+    x.wlo = ds0;
+    x.whi = p.causal ? x.qmax : de1 - 1;
+    x.flo = ds1;
+    x.fhi = p.causal ? x.qmin : de0 - 1;
+    if (p.causal)
+      x.minvis = ds1 > x.qmin ? 1 : x.qmin - ds0 + 1;  // a document starting inside: 1
+    else
+      x.minvis = de0 < ds1 ? 1 : min(de0 - ds0, de1 - ds1);  // a whole document inside: short
     return;
   }
   int lo = INT_MAX, hi = INT_MIN;
@@ -162,7 +183,7 @@ __device__ __forceinline__ void unit_qrange(const FwdParams &p, Unit &x) {
 }
 
 struct KvIter {
-  int s = -1, j = 0, c = 0, c_end = 0, c_full = 0;
+  int s = -1, j = 0, c = 0, c_end = 0, c_fbeg = 0, c_full = 0;
   // block mode: a window of 32 key tiles starting at `win`, with bit t of
   // `keep` set when tile win + t holds a key some query of the unit sees,
   // and of `part` when that tile needs the element mask
@@ -173,7 +194,7 @@ struct KvIter {
 // Next key/value tile of the unit in ring order.  Returns false at the end.
 // `partial` marks tiles that need an element mask (causal diagonal or the
 // ragged last tile).  Warp-collective in block mode.
-template <bool kBlock>
+template <bool kBlock, bool kDocs>
 __device__ __forceinline__ bool kv_next(const FwdParams &p, const Unit &x, KvIter &it, int &j,
                                         int &c, bool &partial) {
   const int n_complete = p.Lk / kTile;
@@ -181,23 +202,39 @@ __device__ __forceinline__ bool kv_next(const FwdParams &p, const Unit &x, KvIte
     while (it.c >= it.c_end) {
       if (++it.s >= p.N) return false;
       it.j = kv_shard_at(x.i, it.s, p.N);
-      it.c = 0;
-      if (!p.causal) {
-        it.c_end = p.n_ktiles;
-        it.c_full = n_complete;
-      } else {
-        // keys visible to the latest query form a prefix [0, lim] of the shard;
-        // keys visible to the earliest query form [0, limf].
-        const int lim = last_visible_row(p.layout, p.L, p.N, it.j, x.qmax);
-        const int limf = last_visible_row(p.layout, p.L, p.N, it.j, x.qmin);
+      if constexpr (kDocs) {
+        // Shard rows are increasing positions, so the keys some row sees are
+        // the rows [lo, lim] of the shard and those every row sees
+        // [flo, limf].
+        const int lo = max(0, first_row_at_or_after(p.layout, p.L, p.N, it.j, x.wlo));
+        const int lim = last_visible_row(p.layout, p.L, p.N, it.j, x.whi);
+        const int flo = max(0, first_row_at_or_after(p.layout, p.L, p.N, it.j, x.flo));
+        const int limf = last_visible_row(p.layout, p.L, p.N, it.j, x.fhi);
+        it.c = lo >= p.L ? p.n_ktiles : lo / kTile;
         it.c_end = lim < 0 ? 0 : min(p.n_ktiles, lim / kTile + 1);
+        it.c_fbeg = (flo + kTile - 1) / kTile;
         it.c_full = limf < kTile - 1 ? 0 : min(n_complete, (limf - (kTile - 1)) / kTile + 1);
         it.c_full = min(it.c_full, it.c_end);
+      } else {
+        it.c = 0;
+        it.c_fbeg = 0;
+        if (!p.causal) {
+          it.c_end = p.n_ktiles;
+          it.c_full = n_complete;
+        } else {
+          // keys visible to the latest query form a prefix [0, lim] of the
+          // shard; keys visible to the earliest query form [0, limf].
+          const int lim = last_visible_row(p.layout, p.L, p.N, it.j, x.qmax);
+          const int limf = last_visible_row(p.layout, p.L, p.N, it.j, x.qmin);
+          it.c_end = lim < 0 ? 0 : min(p.n_ktiles, lim / kTile + 1);
+          it.c_full = limf < kTile - 1 ? 0 : min(n_complete, (limf - (kTile - 1)) / kTile + 1);
+          it.c_full = min(it.c_full, it.c_end);
+        }
       }
     }
     j = it.j;
     c = it.c;
-    partial = it.c >= it.c_full;
+    partial = it.c < it.c_fbeg || it.c >= it.c_full;
     ++it.c;
     return true;
   } else {
@@ -322,7 +359,7 @@ __device__ __forceinline__ void exp_pack_store(const float (&s)[kTile], uint64_t
   }
 }
 
-template <int D, int NQ, bool kBlock>
+template <int D, int NQ, bool kBlock, bool kDocs>
 __global__ void __launch_bounds__(FwdCfg<D, NQ>::kThreads, 1)
     fwd_kernel(const __grid_constant__ FwdParams p, const __grid_constant__ CUtensorMap qmap,
                const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap) {
@@ -367,14 +404,14 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::kThreads, 1)
   const uint32_t tmem = *tmem_holder;
 
   Unit x = decode_unit(p, blockIdx.x);
-  unit_qrange<kBlock>(p, x);
+  unit_qrange<kBlock, kDocs>(p, x);
   // Rows that see fewer than kSplitKeys keys take the hi + lo path.  On the
   // ring a row at position t sees t + 1 keys.  A block step counts, over the
   // CTA's key range, the keys its earliest query sees (every row of the tile
   // sees at least those).
   bool split;
   if constexpr (!kBlock) {
-    split = p.causal ? (x.qmin + 1 < kSplitKeys) : (p.S < kSplitKeys);
+    split = x.minvis < kSplitKeys;
   } else {
     const int k0 = x.kc0 * kTile, k1 = min(p.Lk, x.kc1 * kTile);
     if (k1 - k0 < kSplitKeys) {
@@ -420,7 +457,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::kThreads, 1)
     KvIter it;
     int j, c, n = 0;
     bool partial;
-    while (kv_next<kBlock>(p, x, it, j, c, partial)) {
+    while (kv_next<kBlock, kDocs>(p, x, it, j, c, partial)) {
       if (lane == 0) {
         map_coords(p.layout, p.L, p.N, j, c * kTile, c2, c3);
         const int ks = n % C::kKSt;
@@ -469,7 +506,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::kThreads, 1)
       KvIter it;
       int j, c, n = 0;
       bool partial;
-      bool has = kv_next<kBlock>(p, x, it, j, c, partial);
+      bool has = kv_next<kBlock, kDocs>(p, x, it, j, c, partial);
       if (has && lane == 0) {
         if (mbar_wait(&bars[C::bKFull + 0], 0, abort_flag, kSiteMmaK)) {
           tc_fence_after();
@@ -483,7 +520,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::kThreads, 1)
       }
       __syncwarp();
       while (has && !*abort_flag) {
-        const bool has_next = kv_next<kBlock>(p, x, it, j, c, partial);
+        const bool has_next = kv_next<kBlock, kDocs>(p, x, it, j, c, partial);
         if (lane == 0) {
           const int vs = n % C::kVSt;
           const uint32_t vph = (n / C::kVSt) & 1;
@@ -544,6 +581,9 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::kThreads, 1)
     const int r_cl = row_exists ? r_abs : p.L - 1;
     const int qp = kBlock ? (p.causal ? p.q_pos[r_cl] : 0)
                                 : token_at(p.layout, p.L, p.N, x.i, r_cl);
+    // ring mode: this row sees key positions [q_wlo, q_whi]
+    int q_wlo = 0, q_whi = 0;
+    if constexpr (kDocs) key_window(p.cu, p.n_docs, x.bb, p.S, p.causal, qp, q_wlo, q_whi);
     const float sl2 = p.scale_log2;
 
     float m_run = -INFINITY;  // exponent shift (log2 units of the scaled logits)
@@ -557,7 +597,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::kThreads, 1)
     // the hot loop carries no branch on it.
     auto tile_loop = [&](auto split_tag) {
     constexpr bool kSplit = decltype(split_tag)::value;
-    while (kv_next<kBlock>(p, x, it, j, c, partial)) {
+    while (kv_next<kBlock, kDocs>(p, x, it, j, c, partial)) {
       const bool got = mbar_wait(&bars[C::bSFull + t], n & 1, abort_flag, kSiteSmS);
       if (!__all_sync(kFull, got)) {  // tcgen05.ld/st below are warp-collective
         aborted = true;
@@ -571,12 +611,22 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::kThreads, 1)
       for (int e = 0; e < kTile; ++e) s[e] = __uint_as_float(sr[e]);
       if (partial) {
         if constexpr (!kBlock) {
-          int lim = p.Lk - 1;
-          if (p.causal) lim = min(lim, last_visible_row(p.layout, p.L, p.N, j, qp));
-          const int climit = lim - c * kTile;
+          if constexpr (kDocs) {
+            const int lim = min(p.Lk - 1, last_visible_row(p.layout, p.L, p.N, j, q_whi));
+            const int lo = first_row_at_or_after(p.layout, p.L, p.N, j, q_wlo);
+            const int climit = lim - c * kTile;
+            const int cbase = lo - c * kTile;
 #pragma unroll
-          for (int e = 0; e < kTile; ++e)
-            if (e > climit) s[e] = -INFINITY;
+            for (int e = 0; e < kTile; ++e)
+              if (e > climit || e < cbase) s[e] = -INFINITY;
+          } else {
+            int lim = p.Lk - 1;
+            if (p.causal) lim = min(lim, last_visible_row(p.layout, p.L, p.N, j, qp));
+            const int climit = lim - c * kTile;
+#pragma unroll
+            for (int e = 0; e < kTile; ++e)
+              if (e > climit) s[e] = -INFINITY;
+          }
         } else {
 #pragma unroll
           for (int e = 0; e < kTile; ++e) {
@@ -721,11 +771,11 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::kThreads, 1)
   }
 }
 
-template <int D, int NQ, bool kBlock>
+template <int D, int NQ, bool kBlock, bool kDocs = false>
 cudaError_t launch_fwd_t(const FwdParams &p, const CUtensorMap &qmap, const CUtensorMap &kmap,
                          const CUtensorMap &vmap, long long n_units, cudaStream_t stream) {
   using C = FwdCfg<D, NQ>;
-  auto kern = fwd_kernel<D, NQ, kBlock>;
+  auto kern = fwd_kernel<D, NQ, kBlock, kDocs>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemAlloc);
   if (e != cudaSuccess) return e;
@@ -754,18 +804,23 @@ cudaError_t launch_fwd(const FwdParams &p, int d, int nq, const CUtensorMap &qma
                        cudaStream_t stream) {
   if (n_units <= 0) return cudaSuccess;
   const bool blk = p.block_mode != 0;
+  const bool docs = !blk && p.cu != nullptr;
   if (d == 128 && nq == 2)
     return blk ? launch_fwd_t<128, 2, true>(p, qmap, kmap, vmap, n_units, stream)
-               : launch_fwd_t<128, 2, false>(p, qmap, kmap, vmap, n_units, stream);
+           : docs ? launch_fwd_t<128, 2, false, true>(p, qmap, kmap, vmap, n_units, stream)
+                  : launch_fwd_t<128, 2, false>(p, qmap, kmap, vmap, n_units, stream);
   if (d == 128 && nq == 1)
     return blk ? launch_fwd_t<128, 1, true>(p, qmap, kmap, vmap, n_units, stream)
-               : launch_fwd_t<128, 1, false>(p, qmap, kmap, vmap, n_units, stream);
+           : docs ? launch_fwd_t<128, 1, false, true>(p, qmap, kmap, vmap, n_units, stream)
+                  : launch_fwd_t<128, 1, false>(p, qmap, kmap, vmap, n_units, stream);
   if (d == 64 && nq == 2)
     return blk ? launch_fwd_t<64, 2, true>(p, qmap, kmap, vmap, n_units, stream)
-               : launch_fwd_t<64, 2, false>(p, qmap, kmap, vmap, n_units, stream);
+           : docs ? launch_fwd_t<64, 2, false, true>(p, qmap, kmap, vmap, n_units, stream)
+                  : launch_fwd_t<64, 2, false>(p, qmap, kmap, vmap, n_units, stream);
   if (d == 64 && nq == 1)
     return blk ? launch_fwd_t<64, 1, true>(p, qmap, kmap, vmap, n_units, stream)
-               : launch_fwd_t<64, 1, false>(p, qmap, kmap, vmap, n_units, stream);
+           : docs ? launch_fwd_t<64, 1, false, true>(p, qmap, kmap, vmap, n_units, stream)
+                  : launch_fwd_t<64, 1, false>(p, qmap, kmap, vmap, n_units, stream);
   return cudaErrorInvalidValue;
 }
 

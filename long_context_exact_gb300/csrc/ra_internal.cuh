@@ -99,6 +99,43 @@ __host__ __device__ __forceinline__ void map_coords(int layout, int L, int N, in
   }
 }
 
+// ------------------------------------------------------------ packed documents
+// Documents packed end to end into one sequence (the third page's section
+// 5): cu [b][n_docs + 1] holds each batch row's document offsets, from 0 to
+// S, non-decreasing.  A query sees only keys of its own document (and, under
+// the causal rule, none after itself), so the keys a query at position t
+// sees are the positions [ds, causal ? t : de - 1] of its document [ds, de).
+// Without documents (cu == nullptr) the document is the whole sequence.
+__device__ __forceinline__ void doc_of(const int32_t *cu, int n_docs, int bb, int S, int t,
+                                       int &ds, int &de) {
+  if (cu == nullptr) {
+    ds = 0;
+    de = S;
+    return;
+  }
+  const int32_t *c = cu + static_cast<size_t>(bb) * (n_docs + 1);
+  int lo = 0, hi = n_docs - 1;  // the last document that starts at or before t
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (c[mid] <= t)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  ds = c[lo];
+  de = c[lo + 1];
+}
+
+// Keys visible to the query at position t form the position window
+// [win_lo, win_hi] (inclusive).
+__device__ __forceinline__ void key_window(const int32_t *cu, int n_docs, int bb, int S,
+                                           int causal, int t, int &win_lo, int &win_hi) {
+  int ds, de;
+  doc_of(cu, n_docs, bb, S, t, ds, de);
+  win_lo = ds;
+  win_hi = causal ? t : de - 1;
+}
+
 // ------------------------------------------------------------ parameters
 struct FwdParams {
   int b, h, n_kv, g;        // g = h / n_kv
@@ -114,6 +151,8 @@ struct FwdParams {
   int pairs;                // g / NQ query-head groups per KV head
   int block_mode;           // 0: ring + finalize, 1: block step with state merge
   int split_tiles;          // block mode: key tiles per split (0: one split of all)
+  const int32_t *cu;        // ring: packed-document offsets [b][n_docs + 1], or null
+  int n_docs;
   const int32_t *q_pos;     // block mode: [Lq]
   const int32_t *k_pos;     // block mode: [Lk]
   float *out;               // ring: [b, S, h, d]
@@ -125,6 +164,8 @@ struct FwdParams {
 
 struct BwdParams {
   int b, h, n_kv, g;
+  const int32_t *cu;        // packed-document offsets [b][n_docs + 1], or null
+  int n_docs;
   int N, L, S;              // shards, rows per shard, tokens per sequence
   int layout, causal;
   float scale;              // dQ, dK multiplier

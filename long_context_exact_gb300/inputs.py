@@ -58,6 +58,9 @@ WORKLOADS = {
     # profiling-size case: inputs still larger than L2, ~2 GB on the device
     "causal32k": Workload("causal GQA fwd+bwd b1 h32 kv8 d128 S32768 N8 striped", 1, 32768, 32,
                           8, 128, 8, True, (STRIPED,), 5, rows_per_head=128, backward=True),
+    # packed documents (log-uniform lengths 1K..64K) in one causal window
+    "packed64k": Workload("packed causal GQA b1 h32 kv8 d128 S65536 N8 striped", 1, 65536, 32,
+                          8, 128, 8, True, (STRIPED,), 6, rows_per_head=256),
     "bwd64k": Workload("causal GQA fwd+bwd b2 h32 kv8 d128 S65536 N16 striped", 2, 65536,
                        32, 8, 128, 16, True, (STRIPED,), 4, rows_per_head=128,
                        backward=True),
@@ -79,6 +82,24 @@ def make_inputs(b: int, S: int, h: int, n_kv: int, d: int, seed: int,
 
 def workload_inputs(w: Workload):
     return make_inputs(w.b, w.S, w.h, w.n_kv, w.d, w.seed, w.amplitude, w.backward)
+
+
+def packed_offsets(S: int, seed: int, min_len: int = 1024, max_len: int = 65536,
+                   b: int = 1) -> np.ndarray:
+    """Document offsets [b, n_docs + 1] (int32) of a packed window of S
+    tokens: document lengths drawn log-uniformly in [min_len, max_len]
+    (seeded numpy Generator), the last one cut at S; every batch row gets its
+    own draw and rows are padded with empty documents to a common count."""
+    rng = np.random.default_rng(seed + 2000)
+    rows = []
+    for _ in range(b):
+        offs = [0]
+        while offs[-1] < S:
+            n = int(np.exp(rng.uniform(np.log(min_len), np.log(max_len))))
+            offs.append(min(S, offs[-1] + max(1, n)))
+        rows.append(offs)
+    n = max(len(r) for r in rows)
+    return np.array([r + [S] * (n - len(r)) for r in rows], dtype=np.int32)
 
 
 def sample_rows(S: int, n_shards: int, count: int | None, seed: int) -> np.ndarray:

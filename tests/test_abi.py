@@ -159,6 +159,16 @@ def test_prefill_validation_and_workspace(lib):
     assert lib.ra_chunked_prefill(*args, 0, 4096, 4, d, 1, 0.0, None, 0, None) == binding.RA_OK
 
 
+def test_packed_validation(lib):
+    d = _dims()
+    assert lib.ra_ring_attention_packed(FAKE, FAKE, FAKE, FAKE, FAKE, 1024, 4, 1, 1, 0.0, d, FAKE,
+                                        0, None) == binding.RA_ERR_INVALID_ARG   # no documents
+    assert lib.ra_ring_attention_packed(FAKE, FAKE, FAKE, FAKE, FAKE, 1024, 4, 1, 1, 0.0, d, None,
+                                        3, None) == binding.RA_ERR_INVALID_ARG   # offsets missing
+    assert lib.ra_ring_attention_packed_bwd(*([FAKE] * 9), FAKE, 1 << 30, 1024, 4, 1, 1, 0.0, d,
+                                            FAKE, -1, None) == binding.RA_ERR_INVALID_ARG
+
+
 def test_workspace_size(lib):
     lib.ra_bwd_workspace_size.argtypes = [ctypes.c_int64, ctypes.c_int, binding.Dims]
     n = lib.ra_bwd_workspace_size(65536, 16, _dims(b=2, h=32, n_kv=8))
