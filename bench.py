@@ -378,6 +378,37 @@ def prefill_report(w, q, k, v, dev):
     return res
 
 
+def packed_report(w, q, k, v, do, layout, dev):
+    """Packed documents in the workload's window (the third page's section 5,
+    branch two: a kernel that skips the masked blocks): document lengths
+    drawn log-uniformly in [1K, 64K] tokens (seeded), forward and backward
+    with the block-diagonal causal mask.  Useful FLOPs count each document's
+    own causal triangle: 2 b h d n^2 per document of n tokens forward, 2.5x
+    that backward."""
+    import numpy as np
+    import torch
+
+    from long_context_exact_gb300 import binding as ra
+    from long_context_exact_gb300.inputs import packed_offsets
+
+    cu_np = packed_offsets(w.S, w.seed, b=w.b)
+    cu = torch.from_numpy(cu_np).to(dev)
+    lens = (cu_np[:, 1:] - cu_np[:, :-1]).astype(np.float64)
+    f_fwd = float(2.0 * w.h * w.d * (lens ** 2).sum())
+    out = torch.empty((w.b, w.S, w.h, w.d), dtype=torch.float32, device=dev)
+    lse = torch.empty((w.b, w.h, w.S), dtype=torch.float32, device=dev)
+    fwd_ms = _time_ms(lambda: ra.ring_attention(q, k, v, w.n_shards, layout, True, out=out,
+                                                lse=lse, cu_seqlens=cu), reps=2)
+    bwd_ms = _time_ms(lambda: ra.ring_attention_bwd(q, k, v, out, lse, do, w.n_shards, layout,
+                                                    True, cu_seqlens=cu), reps=2)
+    ra.stream_check()
+    return {"n_docs": int((lens > 0).sum()), "doc_len_min": int(lens[lens > 0].min()),
+            "doc_len_max": int(lens.max()), "fwd_ms": fwd_ms,
+            "fwd_tflops": f_fwd / (fwd_ms / 1e3) / 1e12, "bwd_ms": bwd_ms,
+            "bwd_tflops": 2.5 * f_fwd / (bwd_ms / 1e3) / 1e12,
+            "useful_fraction_of_unpacked_causal": f_fwd / (2.0 * w.b * w.S * w.S * w.h * w.d)}
+
+
 # ---------------------------------------------------------------- our arm
 def run_ours(a, rank, world, local_rank):
     import torch
@@ -547,6 +578,8 @@ def run_ours(a, rank, world, local_rank):
         extras["exp2_roof"] = exp2_roof_report(w, dev, clk)
         extras["hbm_kernels"] = hbm_kernel_report(w, dev, peaks)
         extras["chunked_prefill"] = prefill_report(w, q, k, v, dev)
+        if have_bwd:
+            extras["packed_documents"] = packed_report(w, q, k, v, do, layout, dev)
 
     cpu = None
     if rank == 0 and world == 1 and not a.no_cpu_baseline:
