@@ -36,7 +36,7 @@ WORKLOAD = "causal256k"
 # (dram__bytes_read.sum + dram__bytes_write.sum, one pass, this workload),
 # valid only while the kernel source hashes match (see profiles/).
 TRAFFIC = {
-    "bwd": {"bytes_per_launch": 117758141952 + 80446772480, "src_sha": "ab8df136a2c4b952",
+    "bwd": {"bytes_per_launch": 118393900544 + 80786313984, "src_sha": "424f43924557fbc3",
             "profile": "profiles/traffic_bwd_causal256k.md"},
 }
 
