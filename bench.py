@@ -172,8 +172,28 @@ def _cpu_oracle_sample(w, fwd_rows: int, bwd_rows: int, seed: int):
         oracle.attn_bwd_rows(q, k, v, do, w.causal, rows=rows_b)
         flops += 2.5 * per_row_fwd * bwd_rows
     t2 = time.perf_counter()
-    threads = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    threads = oracle.max_threads()
     return flops, (t1 - t0), (t2 - t0), threads, torch
+
+
+def _cpu_oracle_single_thread_tiny():
+    """The oracle on the tiny configuration (b1 h2 kv2 d64 S1024 N4,
+    non-causal), every row, forward, on one thread: (seconds, TFLOP/s)."""
+    from long_context_exact_gb300 import accounting
+    from long_context_exact_gb300.inputs import WORKLOADS, workload_inputs
+    from oracle import oracle
+
+    w = WORKLOADS["tiny"]
+    q, k, v = workload_inputs(w)[:3]
+    n = oracle.max_threads()
+    oracle.set_threads(1)
+    try:
+        t0 = time.perf_counter()
+        oracle.attn_fwd_rows(q, k, v, w.causal)
+        secs = time.perf_counter() - t0
+    finally:
+        oracle.set_threads(n)
+    return secs, accounting.fwd_useful_flops(w.b, w.S, w.h, w.d, w.causal) / secs / 1e12
 
 
 def run_reference(a, rank, world):
@@ -585,10 +605,17 @@ def run_ours(a, rank, world, local_rank):
     if rank == 0 and world == 1 and not a.no_cpu_baseline:
         fwd_rows, bwd_rows = 16, 4
         flops, _, secs, threads, _ = _cpu_oracle_sample(w, fwd_rows, bwd_rows, seed=123)
+        st_secs, st_tflops = _cpu_oracle_single_thread_tiny()
         cpu = {"value": flops / secs / 1e12, "unit": "TFLOP/s", "cores": threads,
-               "kind": "oracle",
+               "host_cpus": os.cpu_count(), "kind": "oracle",
                "sample": f"fp64 oracle, {fwd_rows} forward + {bwd_rows} backward random query "
-                         f"rows x {w.h} heads of this workload, {secs:.1f} s"}
+                         f"rows x {w.h} heads of this workload, {secs:.1f} s",
+               "extrapolated_full_step_s": secs * step_flops / flops,
+               "extrapolated_note": "measured seconds x (useful FLOPs of a whole forward + "
+                                    "backward step / FLOPs of the sample); not measured",
+               "single_thread_tiny": {"seconds": st_secs, "tflops": st_tflops,
+                                      "workload": "tiny non-causal b1 h2 kv2 d64 S1024, "
+                                                  "every row, forward"}}
 
     if rank == 0:
         line = {

@@ -34,6 +34,9 @@
  * LSE = -inf.
  */
 #include <math.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
@@ -99,6 +102,28 @@ ORC_API void orc_ring_order(int N, int32_t *order)
     for (int i = 0; i < N; ++i)
         for (int s = 0; s < N; ++s)
             order[i * N + s] = (int32_t)(((i - s) % N + N) % N);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Thread control for timing the oracle (no arithmetic): the number of
+ * OpenMP threads a parallel region uses, and a way to set it.             */
+ORC_API int orc_max_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+ORC_API void orc_set_threads(int n)
+{
+#ifdef _OPENMP
+    if (n > 0)
+        omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
 }
 
 /* ------------------------------------------------------------------------ */

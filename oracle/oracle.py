@@ -73,6 +73,10 @@ def _load():
             lib.orc_finalize.restype = None
             lib.orc_merge.argtypes = [P, P, P, P, i32, i64, i32, i32, P, P]
             lib.orc_merge.restype = None
+            lib.orc_max_threads.argtypes = []
+            lib.orc_max_threads.restype = i32
+            lib.orc_set_threads.argtypes = [i32]
+            lib.orc_set_threads.restype = None
             _lib = lib
     return _lib
 
@@ -125,6 +129,16 @@ def ring_order(N: int) -> np.ndarray:
     out = np.empty(N * N, np.int32)
     lib.orc_ring_order(N, _ptr(out))
     return out.reshape(N, N)
+
+
+def max_threads() -> int:
+    """OpenMP threads the oracle's parallel loops use."""
+    return int(_load().orc_max_threads())
+
+
+def set_threads(n: int) -> None:
+    """Set the OpenMP thread count of later oracle calls (timing only)."""
+    _load().orc_set_threads(int(n))
 
 
 def doc_bounds(cu_seqlens, S: int):
