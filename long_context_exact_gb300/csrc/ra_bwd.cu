@@ -640,33 +640,30 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         go = mbar_wait(&bars[C::bStgEmpty], (n - 1) & 1, abort_flag, kSiteBSmStg);
       if (!__all_sync(kFull, go)) break;
       tc_fence_after();
-      // 16 query columns at a time; the next group's dP^T and D in flight
-      uint32_t rc[16], rn[16];
-      float4 dc[4], dn[4];
-      tmem_ld16_start(tDp, rc);
+      // all 64 dP^T columns of this half in one round of loads; dS = P (dP - D)
+      // on f32x2 pairs
+      uint32_t r4[4][16];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) dc[e] = d4[e];
-      tmem_ld_wait_regs16(rc);
+      for (int ch = 0; ch < 4; ++ch) tmem_ld16_start(tDp + ch * 16, r4[ch]);
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) tmem_ld_wait_regs16(r4[ch]);
 #pragma unroll
       for (int ch = 0; ch < 4; ++ch) {
-        if (ch < 3) {
-          tmem_ld16_start(tDp + (ch + 1) * 16, rn);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) dn[e] = d4[(ch + 1) * 4 + e];
-        }
         float sv[16];
 #pragma unroll
         for (int e4 = 0; e4 < 4; ++e4) {
+          const float4 dd = d4[ch * 4 + e4];
           const int c = ch * 16 + e4 * 4;
-          sv[e4 * 4 + 0] = pf[c + 0] * (__uint_as_float(rc[e4 * 4 + 0]) - dc[e4].x);
-          sv[e4 * 4 + 1] = pf[c + 1] * (__uint_as_float(rc[e4 * 4 + 1]) - dc[e4].y);
-          sv[e4 * 4 + 2] = pf[c + 2] * (__uint_as_float(rc[e4 * 4 + 2]) - dc[e4].z);
-          sv[e4 * 4 + 3] = pf[c + 3] * (__uint_as_float(rc[e4 * 4 + 3]) - dc[e4].w);
+          const uint64_t t0 = fadd2(f2pack(__uint_as_float(r4[ch][e4 * 4 + 0]), __uint_as_float(r4[ch][e4 * 4 + 1])),
+                                    f2pack(-dd.x, -dd.y));
+          const uint64_t t1 = fadd2(f2pack(__uint_as_float(r4[ch][e4 * 4 + 2]), __uint_as_float(r4[ch][e4 * 4 + 3])),
+                                    f2pack(-dd.z, -dd.w));
+          f2unpack(fmul2(f2pack(pf[c + 0], pf[c + 1]), t0), sv[e4 * 4 + 0], sv[e4 * 4 + 1]);
+          f2unpack(fmul2(f2pack(pf[c + 2], pf[c + 3]), t1), sv[e4 * 4 + 2], sv[e4 * 4 + 3]);
         }
         uint32_t whi[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) whi[e] = pack_bf16x2(sv[2 * e], sv[2 * e + 1]);
-        // 16 queries = two 16-byte chunks of this key's row, 128-byte swizzled
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
           const int chunk = (ch * 2 + u) ^ (row & 7);
@@ -685,13 +682,6 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
             *reinterpret_cast<uint4 *>(dslo_row + chunk * 16) =
                 make_uint4(wlo[u * 4 + 0], wlo[u * 4 + 1], wlo[u * 4 + 2], wlo[u * 4 + 3]);
           }
-        }
-        if (ch < 3) {
-          tmem_ld_wait_regs16(rn);
-#pragma unroll
-          for (int e = 0; e < 16; ++e) rc[e] = rn[e];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) dc[e] = dn[e];
         }
       }
       fence_proxy_async_smem();
