@@ -610,13 +610,21 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         for (int e = 0; e < 16; ++e) l4[e] = lse4[e];
         tmem_ld_wait_regs(sr[0]);
         tmem_ld_wait_regs(sr[1]);
+        const uint64_t sl2x2 = f2pack(sl2, sl2);
 #pragma unroll
         for (int e4 = 0; e4 < 16; ++e4) {
           const int c = e4 * 4;
-          pf[c + 0] = ex2(fmaf(__uint_as_float(sr[c >> 5][(c + 0) & 31]), sl2, -l4[e4].x));
-          pf[c + 1] = ex2(fmaf(__uint_as_float(sr[c >> 5][(c + 1) & 31]), sl2, -l4[e4].y));
-          pf[c + 2] = ex2(fmaf(__uint_as_float(sr[c >> 5][(c + 2) & 31]), sl2, -l4[e4].z));
-          pf[c + 3] = ex2(fmaf(__uint_as_float(sr[c >> 5][(c + 3) & 31]), sl2, -l4[e4].w));
+          float x0, x1, x2, x3;
+          f2unpack(ffma2(f2pack(__uint_as_float(sr[c >> 5][(c + 0) & 31]),
+                                __uint_as_float(sr[c >> 5][(c + 1) & 31])),
+                         sl2x2, f2pack(l4[e4].x, l4[e4].y)), x0, x1);
+          f2unpack(ffma2(f2pack(__uint_as_float(sr[c >> 5][(c + 2) & 31]),
+                                __uint_as_float(sr[c >> 5][(c + 3) & 31])),
+                         sl2x2, f2pack(l4[e4].z, l4[e4].w)), x2, x3);
+          pf[c + 0] = ex2(x0);
+          pf[c + 1] = ex2(x1);
+          pf[c + 2] = ex2(x2);
+          pf[c + 3] = ex2(x3);
         }
       }
       if (partial) {  // causal diagonal: columns before c0 do not see this key
@@ -655,9 +663,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
           const float4 dd = d4[ch * 4 + e4];
           const int c = ch * 16 + e4 * 4;
           const uint64_t t0 = fadd2(f2pack(__uint_as_float(r4[ch][e4 * 4 + 0]), __uint_as_float(r4[ch][e4 * 4 + 1])),
-                                    f2pack(-dd.x, -dd.y));
+                                    f2pack(dd.x, dd.y));
           const uint64_t t1 = fadd2(f2pack(__uint_as_float(r4[ch][e4 * 4 + 2]), __uint_as_float(r4[ch][e4 * 4 + 3])),
-                                    f2pack(-dd.z, -dd.w));
+                                    f2pack(dd.z, dd.w));
           f2unpack(fmul2(f2pack(pf[c + 0], pf[c + 1]), t0), sv[e4 * 4 + 0], sv[e4 * 4 + 1]);
           f2unpack(fmul2(f2pack(pf[c + 2], pf[c + 3]), t1), sv[e4 * 4 + 2], sv[e4 * 4 + 3]);
         }
@@ -867,9 +875,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
   }
 }
 
-// D = rowsum(dO * O) and LSE2 = LSE * log2(e) per (batch, head, query row),
+// -D = -rowsum(dO * O) and -LSE2 = -LSE * log2(e) per (batch, head, query
+// row), stored negated so the main kernel adds them with f32x2 arithmetic,
 // written in shard-local order [b, h, N, Lpad]; padding rows get D = 0 and
-// LSE2 = +inf (their P is exactly 0).  One warp per row.
+// -LSE2 = -inf (their P is exactly 0).  One warp per row.
 template <int D>
 __global__ void bwd_pre_kernel(BwdParams p, const float *out, const float *lse,
                                const uint16_t *dout) {
@@ -902,8 +911,8 @@ __global__ void bwd_pre_kernel(BwdParams p, const float *out, const float *lse,
       l2 = (lv == -INFINITY) ? INFINITY : lv * kLog2e;
     }
     if (lane == 0) {
-      p.dvec[w] = dsum;
-      p.lse2[w] = l2;
+      p.dvec[w] = -dsum;
+      p.lse2[w] = -l2;
     }
   }
 }

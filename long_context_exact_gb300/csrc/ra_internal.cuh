@@ -172,8 +172,8 @@ struct BwdParams {
   float scale_log2;         // scale * log2(e)
   int n_qtiles, n_ktiles;   // ceil(L / 128)
   int Lpad;                 // n_qtiles * 128
-  float *dvec;              // [b, h, N, Lpad] rowsum(dO * O), shard-local order
-  float *lse2;              // [b, h, N, Lpad] LSE * log2(e), +inf on padding rows
+  float *dvec;              // [b, h, N, Lpad] -rowsum(dO * O), shard-local order
+  float *lse2;              // [b, h, N, Lpad] -LSE * log2(e), -inf on padding rows
   float *dq;                // [b, S, h, d], accumulated (zeroed before the launch)
   float *dk, *dv;           // [b, S, n_kv, d]
 };
