@@ -36,7 +36,7 @@ WORKLOAD = "causal256k"
 # (dram__bytes_read.sum + dram__bytes_write.sum, one pass, this workload),
 # valid only while the kernel source hashes match (see profiles/).
 TRAFFIC = {
-    "bwd": {"bytes_per_launch": 118393900544 + 80786313984, "src_sha": "424f43924557fbc3",
+    "bwd": {"bytes_per_launch": 119864092928 + 82170674944, "src_sha": "a39e63d6501ff63b",
             "profile": "profiles/traffic_bwd_causal256k.md"},
 }
 
