@@ -135,18 +135,24 @@ enum : unsigned int {
 
 struct KvUnit {
   int bb, kh, j, c;   // batch, kv head, kv shard, kv tile
-  int i, hq;          // the query shard and query head it meets
+  int i, hq;          // unpacked: the query shard and query head it meets
   int kmin, kmax;     // token positions of the tile's first and last existing key
-  int a_lo, a_hi;     // query tiles [a_lo, a_hi) have a row that sees a key of the tile
-  int a_flo, a_fhi;   // query tiles [a_flo, a_fhi): every row sees every key (no mask)
+  int a_lo, a_hi;     // unpacked: query tiles [a_lo, a_hi) see a key of the tile
+  int a_flo;          // unpacked: query tiles a >= a_flo see every key (no mask)
+  int ds0, de0, ds1, de1;  // packed: documents of the first and last key
 };
 
-// Units: one 128-key tile against one query shard and one query head of its
-// group; dK and dV of the tile are summed over its units with reductions.
-// Units run grouped by (batch, kv head, query shard, query head) with the key
-// tiles innermost, so the CTAs resident together read the same Q / dO tiles
-// and add their dQ partials into the same 64 KB dq tiles: one group's dq
-// rows (n_qtiles x 64 KB) stay in L2 while every key tile adds to them.
+// Units (unpacked): one 128-key tile against one query shard and one query
+// head of its group; dK and dV of the tile are summed over its units with
+// reductions.  Units run grouped by (batch, kv head, query shard, query head)
+// with the key tiles innermost, so the CTAs resident together read the same
+// Q / dO tiles and add their dQ partials into the same 64 KB dq tiles: one
+// group's dq rows (n_qtiles x 64 KB) stay in L2 while every key tile adds
+// to them.
+// Units (packed documents): one 128-key tile against every query shard and
+// head, like the key/value block of the pages: a tile sees only the query
+// tiles of its own documents, so per-shard units would be a few steps long,
+// and the dq rows it adds into are those few tiles anyway.
 template <bool kDocs>
 __device__ __forceinline__ KvUnit decode_kv_unit(const BwdParams &p, long long u) {
   KvUnit x;
@@ -154,20 +160,26 @@ __device__ __forceinline__ KvUnit decode_kv_unit(const BwdParams &p, long long u
   long long g = u / p.n_ktiles;
   x.j = static_cast<int>(g % p.N);
   g /= p.N;
-  const int hh = static_cast<int>(g % p.g);
-  g /= p.g;
-  x.i = static_cast<int>(g % p.N);
-  g /= p.N;
-  x.kh = static_cast<int>(g % p.n_kv);
-  x.bb = static_cast<int>(g / p.n_kv);
-  x.hq = x.kh * p.g + hh;
+  if constexpr (!kDocs) {
+    const int hh = static_cast<int>(g % p.g);
+    g /= p.g;
+    x.i = static_cast<int>(g % p.N);
+    g /= p.N;
+    x.kh = static_cast<int>(g % p.n_kv);
+    x.bb = static_cast<int>(g / p.n_kv);
+    x.hq = x.kh * p.g + hh;
+  } else {
+    x.kh = static_cast<int>(g % p.n_kv);
+    x.bb = static_cast<int>(g / p.n_kv);
+    x.i = -1;
+    x.hq = -1;
+  }
   const int r0 = x.c * kTile;
   const int r1 = min(r0 + kTile, p.L) - 1;
   x.kmin = token_at(p.layout, p.L, p.N, x.j, r0);
   x.kmax = token_at(p.layout, p.L, p.N, x.j, r1);
   if constexpr (!kDocs) {
     x.a_hi = p.n_qtiles;
-    x.a_fhi = p.n_qtiles;
     if (!p.causal) {
       x.a_lo = 0;
       x.a_flo = 0;
@@ -179,29 +191,20 @@ __device__ __forceinline__ KvUnit decode_kv_unit(const BwdParams &p, long long u
       const int r_full = max(0, first_row_at_or_after(p.layout, p.L, p.N, x.i, x.kmax));
       x.a_flo = min(p.n_qtiles, (r_full + kTile - 1) / kTile);
     }
-    return x;
+  } else {
+    doc_of(p.cu, p.n_docs, x.bb, p.S, x.kmin, x.ds0, x.de0);
+    doc_of(p.cu, p.n_docs, x.bb, p.S, x.kmax, x.ds1, x.de1);
   }
-  // A query at t sees key kp iff kp lies in t's document [ds, de) and, causal,
-  // kp <= t: iff t >= (causal ? kp : ds(kp)) and t < de(kp).  Query rows of
-  // shard i are increasing positions, so the rows that see some key of the
-  // tile and those that see all of them are row ranges.
-  int ds0, de0, ds1, de1;
-  doc_of(p.cu, p.n_docs, x.bb, p.S, x.kmin, ds0, de0);
-  doc_of(p.cu, p.n_docs, x.bb, p.S, x.kmax, ds1, de1);
-  const int r_vis = max(0, first_row_at_or_after(p.layout, p.L, p.N, x.i, p.causal ? x.kmin : ds0));
-  const int r_end = min(p.L, first_row_at_or_after(p.layout, p.L, p.N, x.i, de1));
-  const int r_flo = max(0, first_row_at_or_after(p.layout, p.L, p.N, x.i, p.causal ? x.kmax : ds1));
-  const int r_fhi = min(p.L, first_row_at_or_after(p.layout, p.L, p.N, x.i, de0));
-  x.a_lo = r_vis >= r_end ? p.n_qtiles : r_vis / kTile;
-  x.a_hi = r_vis >= r_end ? p.n_qtiles : (r_end + kTile - 1) / kTile;
-  x.a_flo = (r_flo + kTile - 1) / kTile;
-  x.a_fhi = r_fhi >= p.L ? p.n_qtiles : r_fhi / kTile;
   return x;
 }
 
 struct QIter {
   int a = INT_MAX;
-  int d0 = -1, d1 = -1;  // packed documents: documents of the tile's first and last rows
+  // packed documents: shard step, query shard, its visible and unmasked tile
+  // ranges, query head, and the documents of the current tile's first and
+  // last rows
+  int s = -1, i = 0, a_lo = 0, a_flo = 0, a_fhi = 0, hh = 0;
+  int d0 = -1, d1 = -1;
 };
 
 // Document index of position t, starting from a document index at or after
@@ -240,16 +243,47 @@ __device__ __forceinline__ bool q_next(const BwdParams &p, const KvUnit &x, QIte
                      : (p.S < kSplitKeys);
     return true;
   }
-  it.a = it.a == INT_MAX ? x.a_hi - 1 : it.a - 1;
-  if (it.a < x.a_lo) return false;
-  i = x.i;
+  // Query shards in ring order (j + s) mod N; inside a shard the visible
+  // query tiles from the last down; then the g query heads.  A query at t
+  // sees key kp iff kp lies in t's document [ds, de) and, causal, kp <= t:
+  // iff t >= (causal ? kp : ds(kp)) and t < de(kp).  Query rows of a shard
+  // are increasing positions, so the rows that see some key of the tile and
+  // those that see all of them are row ranges.
+  bool next_shard = false;
+  if (it.a == INT_MAX) {
+    next_shard = true;
+  } else if (++it.hh >= p.g) {
+    it.hh = 0;
+    next_shard = --it.a < it.a_lo;
+  }
+  if (next_shard) {
+    for (;;) {
+      if (++it.s >= p.N) return false;
+      it.i = (x.j + it.s) % p.N;
+      const int r_vis = max(0, first_row_at_or_after(p.layout, p.L, p.N, it.i,
+                                                     p.causal ? x.kmin : x.ds0));
+      const int r_end = min(p.L, first_row_at_or_after(p.layout, p.L, p.N, it.i, x.de1));
+      if (r_vis >= r_end) continue;
+      const int r_flo = max(0, first_row_at_or_after(p.layout, p.L, p.N, it.i,
+                                                     p.causal ? x.kmax : x.ds1));
+      const int r_fhi = min(p.L, first_row_at_or_after(p.layout, p.L, p.N, it.i, x.de0));
+      it.a_lo = r_vis / kTile;
+      it.a = (r_end + kTile - 1) / kTile - 1;
+      it.a_flo = (r_flo + kTile - 1) / kTile;
+      it.a_fhi = r_fhi >= p.L ? p.n_qtiles : r_fhi / kTile;
+      it.hh = 0;
+      it.d0 = it.d1 = -1;
+      break;
+    }
+  }
+  i = it.i;
   a = it.a;
-  hq = x.hq;
-  partial = it.a < x.a_flo || it.a >= x.a_fhi;
-  const int t0 = token_at(p.layout, p.L, p.N, x.i, it.a * kTile);
+  hq = x.kh * p.g + it.hh;
+  partial = it.a < it.a_flo || it.a >= it.a_fhi;
+  const int t0 = token_at(p.layout, p.L, p.N, it.i, it.a * kTile);
   int minvis;
   {
-    const int t1 = token_at(p.layout, p.L, p.N, x.i, min(it.a * kTile + kTile, p.L) - 1);
+    const int t1 = token_at(p.layout, p.L, p.N, it.i, min(it.a * kTile + kTile, p.L) - 1);
     const int32_t *cb = p.cu + static_cast<size_t>(x.bb) * (p.n_docs + 1);
     it.d0 = doc_walk(cb, p.n_docs, it.d0, t0);
     it.d1 = doc_walk(cb, p.n_docs, it.d1, t1);
@@ -339,7 +373,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                const __grid_constant__ CUtensorMap dvmap) {
   using C = BwdCfg<D>;
   const KvUnit x = decode_kv_unit<kDocs>(p, blockIdx.x);
-  if (x.a_lo >= x.a_hi) return;  // no query of this shard sees the tile: nothing to add
+  if constexpr (!kDocs) {
+    if (x.a_lo >= x.a_hi) return;  // no query of this shard sees the tile: nothing to add
+  }
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   if (pad > static_cast<uint32_t>(C::kSlack)) {  // uniform: never touch smem beyond the allocation
@@ -565,15 +601,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     const int kr = x.c * kTile + row;
     const bool key_exists = kr < p.L;
     const int kp = token_at(p.layout, p.L, p.N, x.j, key_exists ? kr : p.L - 1);
-    // this key is seen by the query rows [qr_lo, qr_hi) of shard x.i
-    int qr_lo = 0, qr_hi = 0;
+    // this key is seen by the query positions [kq_lo, kq_hi)
+    int kq_lo = kp, kq_hi = p.S;
     if constexpr (kDocs) {
-      int kds, kde;
-      doc_of(p.cu, p.n_docs, x.bb, p.S, kp, kds, kde);
-      qr_lo = first_row_at_or_after(p.layout, p.L, p.N, x.i, p.causal ? kp : kds);
-      qr_hi = first_row_at_or_after(p.layout, p.L, p.N, x.i, kde);
-    } else {
-      qr_lo = first_row_at_or_after(p.layout, p.L, p.N, x.i, kp);
+      int kds;
+      doc_of(p.cu, p.n_docs, x.bb, p.S, kp, kds, kq_hi);
+      if (!p.causal) kq_lo = kds;
     }
     const float sl2 = p.scale_log2;
     // this warpgroup's 64 query columns are one 128-byte-swizzled half of dS^T
@@ -591,8 +624,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       // query columns cb + c with c < c0 or c >= c1 are masked for this key
       int c0 = 0, c1 = C::kHalfCols;
       if (partial) {
-        c0 = qr_lo - a * kTile - cb;
-        if constexpr (kDocs) c1 = qr_hi - a * kTile - cb;
+        c0 = first_row_at_or_after(p.layout, p.L, p.N, i, kq_lo) - a * kTile - cb;
+        if constexpr (kDocs)
+          c1 = first_row_at_or_after(p.layout, p.L, p.N, i, kq_hi) - a * kTile - cb;
       }
       if (!key_exists) {
         c0 = C::kHalfCols;
