@@ -14,8 +14,10 @@
  *    Context Scaling": "Blockwise Attention and Online Softmax Formulations"
  *    (the update of m, l, O and the final division by l), "The Ring Attention
  *    Protocol" (query block resident, key/value blocks rotate), "Causal
- *    Masking Dynamics" (striped placement t -> t mod N), "The Backward Pass and
- *    Gradient Exchange" (P recomputed from saved statistics).
+ *    Masking Dynamics" (striped placement t -> t mod N; zig-zag half-blocks
+ *    p and 2N-1-p), "The Backward Pass and Gradient Exchange" (P recomputed
+ *    from saved statistics), and its closing remark on inference (a short
+ *    query chunk against a long resident key/value cache).
  *  - "Ring Attention for Infinite Context": "FlashAttention Integration" (the
  *    rescale-merge of a running output with a block output).
  *  - summary of "Ring Attention with Blockwise Transformers for Near-Infinite
@@ -24,13 +26,15 @@
  *    Operation".
  *  - the magicnetworld.com article on ring attention's communication budget,
  *    causal triangle and load imbalance: section 2 (symbols, GQA with h query
- *    heads sharing n_kv KV heads), section 6 (causal mask; contiguous versus
+ *    heads sharing n_kv KV heads), section 5 (documents packed into one window
+ *    with a block-diagonal mask), section 6 (causal mask; contiguous versus
  *    striped placement).
  *
  * Conventions for every call:
  *  - Tensors are dense, row-major, in DEVICE memory, and owned by the caller.
- *    The library allocates no device memory.  Base pointers must be 16-byte
- *    aligned.
+ *    The library allocates no device memory (the allocation-free backward
+ *    uses one fixed array in the library's own device memory).  Base pointers
+ *    must be 16-byte aligned.
  *  - bf16 tensors are passed as raw 16-bit patterns (uint16_t).
  *  - Query-side tensors are [b, rows, h, d]; key/value-side tensors are
  *    [b, rows, n_kv, d].  Per-row statistics are [b, h, rows] float.
@@ -47,7 +51,11 @@
  *  - Device-side waits are bounded; a wait that runs out sets a device error
  *    word, and the kernel unwinds.  ra_stream_check() reports it.
  *  - Supported: d in {64, 128}; h % n_kv == 0; the row counts of one call
- *    below 2^31; n_shards >= 1 with S % n_shards == 0.
+ *    below 2^31; n_shards >= 1 with S % n_shards == 0 (zig-zag: S / 2N a
+ *    multiple of 128).
+ *  - Accumulated outputs (dq, dk, dv; the split states of the chunked
+ *    prefill) are sums of fp32 partial tiles added in arrival order: two
+ *    runs agree to fp32 rounding, not bit for bit.
  */
 #ifndef RA_H
 #define RA_H
