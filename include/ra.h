@@ -53,9 +53,9 @@
  *  - Supported: d in {64, 128}; h % n_kv == 0; the row counts of one call
  *    below 2^31; n_shards >= 1 with S % n_shards == 0 (zig-zag: S / 2N a
  *    multiple of 128).
- *  - Accumulated outputs (dq, dk, dv; the split states of the chunked
- *    prefill) are sums of fp32 partial tiles added in arrival order: two
- *    runs agree to fp32 rounding, not bit for bit.
+ *  - The backward's dq, dk and dv are sums of fp32 partial tiles added in
+ *    arrival order: two runs agree to fp32 rounding, not bit for bit.  The
+ *    forward calls are deterministic.
  */
 #ifndef RA_H
 #define RA_H
