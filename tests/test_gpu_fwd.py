@@ -212,6 +212,40 @@ def test_chunked_prefill_matches_oracle(orc, Lq, Lk, causal, g, d, splits):
     _cmp(out, lse, ref_o, ref_l)
 
 
+def test_chunked_prefill_batch_of_two(orc):
+    """b = 2: the split states and their combination are per batch row."""
+    b, Lq, Lk, h, n_kv, d = 2, 200, 1500, 4, 2, 128
+    q, _, _ = make_inputs(b, Lq, h, n_kv, d, seed=61)
+    _, k, v = make_inputs(b, Lk, h, n_kv, d, seed=62)
+    q_pos = np.arange(Lk - Lq, Lk, dtype=np.int32)
+    k_pos = np.arange(Lk, dtype=np.int32)
+    st = orc.new_state(b, Lq, h, d)
+    orc.block_update(q, k, v, q_pos, k_pos, True, 1.0 / np.sqrt(d), st)
+    ref_o, ref_l = orc.finalize(st)
+    qd, kd, vd = _dev(q, k, v)
+    qp, kp = (torch.from_numpy(x).cuda() for x in (q_pos, k_pos))
+    out, lse = ra.chunked_prefill(qd, kd, vd, qp, kp, True, n_splits=4)
+    ra.stream_check()
+    _cmp(out, lse, ref_o, ref_l)
+
+
+def test_block_step_batch_of_two_non_causal(orc):
+    b, Lq, Lk, h, n_kv, d = 2, 256, 384, 8, 2, 64
+    q, _, _ = make_inputs(b, Lq, h, n_kv, d, seed=71)
+    _, k, v = make_inputs(b, Lk, h, n_kv, d, seed=72)
+    pos_q = np.arange(Lq, dtype=np.int32)
+    pos_k = np.arange(Lk, dtype=np.int32)
+    st_ref = orc.new_state(b, Lq, h, d)
+    orc.block_update(q, k, v, pos_q, pos_k, False, 1.0 / np.sqrt(d), st_ref)
+    qd, kd, vd = _dev(q, k, v)
+    st = ra.new_state(b, Lq, h, d, "cuda")
+    ra.block_step(qd, kd, vd, st, causal=False)
+    out, lse = ra.finalize(st)
+    ra.stream_check()
+    r_out, r_lse = orc.finalize(st_ref)
+    _cmp(out, lse, r_out, r_lse)
+
+
 def test_chunked_prefill_without_keys():
     q, k, v = _dev(*make_inputs(1, 128, 4, 2, 64, seed=1))
     pos = torch.arange(128, dtype=torch.int32, device="cuda")
