@@ -562,7 +562,9 @@ def run_ours(a, rank, world, local_rank):
         # Two device buffer sets and two copy streams: step s+1's inputs go up
         # and step s's results come down while step s computes.  Every step
         # still copies its own inputs from pinned host memory and reads its
-        # own results back inside the timed region.
+        # own results back inside the timed region.  Within a step, dO goes up
+        # after Q, K, V (the forward does not read it) and out, lse come down
+        # as soon as the forward has written them, while the backward runs.
         sets = [dict(q=q, k=k, v=v, do=do, out=out, lse=lse, dq=dq, dk=dk, dv=dv)]
         sets.append({name: torch.empty_like(t) for name, t in sets[0].items()})
         up = torch.cuda.Stream(device=dev)
@@ -580,28 +582,36 @@ def run_ours(a, rank, world, local_rank):
                 bs["q"].copy_(hq_, non_blocking=True)
                 bs["k"].copy_(hk_, non_blocking=True)
                 bs["v"].copy_(hv_, non_blocking=True)
+                qkv_ev = _event(up)
+                do_ev = None
                 if have_bwd:
                     bs["do"].copy_(hdo, non_blocking=True)
-                return _event(up)
+                    do_ev = _event(up)
+                return qkv_ev, do_ev
 
-        def compute(bs, inputs_ready, outputs_free):
-            stream.wait_event(inputs_ready)
+        def compute(bs, ready, outputs_free):
+            qkv_ev, do_ev = ready
+            stream.wait_event(qkv_ev)
             if outputs_free is not None:
                 stream.wait_event(outputs_free)
             ra.ring_attention(bs["q"], bs["k"], bs["v"], w.n_shards, layout, w.causal,
                               out=bs["out"], lse=bs["lse"])
+            fwd_ev = _event(stream)
             if have_bwd:
+                stream.wait_event(do_ev)
                 ra.ring_attention_bwd(bs["q"], bs["k"], bs["v"], bs["out"], bs["lse"], bs["do"],
                                       w.n_shards, layout, w.causal, dq=bs["dq"], dk=bs["dk"],
                                       dv=bs["dv"], workspace=ws)
-            return _event(stream)
+            return fwd_ev, _event(stream)
 
         def d2h_from(bs, done):
+            fwd_ev, all_ev = done
             with torch.cuda.stream(down):
-                down.wait_event(done)
+                down.wait_event(fwd_ev)
                 h_out.copy_(bs["out"], non_blocking=True)
                 h_lse.copy_(bs["lse"], non_blocking=True)
                 if have_bwd:
+                    down.wait_event(all_ev)
                     h_dq.copy_(bs["dq"], non_blocking=True)
                     h_dk.copy_(bs["dk"], non_blocking=True)
                     h_dv.copy_(bs["dv"], non_blocking=True)
@@ -615,7 +625,7 @@ def run_ours(a, rank, world, local_rank):
                 cur, nxt = s_ % 2, (s_ + 1) % 2
                 comp_ev[cur] = compute(sets[cur], ready, down_ev[cur])
                 if s_ + 1 < n_steps:
-                    ready = h2d_into(sets[nxt], comp_ev[nxt])
+                    ready = h2d_into(sets[nxt], None if comp_ev[nxt] is None else comp_ev[nxt][1])
                 down_ev[cur] = d2h_from(sets[cur], comp_ev[cur])
 
         e2e_run(2)
@@ -634,11 +644,25 @@ def run_ours(a, rank, world, local_rank):
         ra.stream_check()
         e2e_ms = s0.elapsed_time(s1)
         e2e_ms = max_over_ranks(e2e_ms, world, dev)
+        # The host link's copy rate on this machine, one direction at a time,
+        # to read the end-to-end figure against.
+        link = {}
+        for name, (dst, src, st) in {"h2d_gbs": (q, hq_, up), "d2h_gbs": (h_dq, dq, down)}.items():
+            c0 = torch.cuda.Event(enable_timing=True)
+            c1 = torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(st):
+                c0.record(st)
+                dst.copy_(src, non_blocking=True)
+                c1.record(st)
+            c1.synchronize()
+            link[name] = src.numel() * src.element_size() / (c0.elapsed_time(c1) * 1e6)
         e2e = {"value": job_rate(step_flops, a.steps, world, e2e_ms), "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": e2e_ms / a.steps,
+               "host_link": {k_: round(v_, 1) for k_, v_ in link.items()},
                "schedule": "two device buffer sets; step s+1's H2D and step s's D2H on "
-                           "their own streams, overlapping step s's compute"}
+                           "their own streams, overlapping compute; dO goes up after Q, K, V "
+                           "and out, lse come down while the backward runs"}
 
     extras = None
     if rank == 0 and not a.no_extras:

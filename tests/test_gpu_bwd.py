@@ -115,3 +115,28 @@ def test_workload_bwd64k_sampled_rows(orc):
     rq, rk, rv = orc.attn_bwd_rows(q, k, v, do, True, rows=rows)
     errs = (_err(dq[:, rows], rq), _err(dk, rk), _err(dv, rv))
     assert max(errs) <= G_TOL, errs
+
+
+def test_workload_causal256k_bwd_sampled_rows(orc):
+    """The timed configuration (b1 S262,144 h32 kv8 d128, N=8 striped,
+    amplitude 0.5, dO drawn after Q, K, V from the same seed) through the
+    same calls: dO is kept on a sample of rows, so dK and dV over all 262,144
+    keys are exactly those rows' contributions and dQ on the sampled rows is
+    the full-run dQ.  Only the sampled dQ rows leave the device."""
+    w = WORKLOADS["causal256k"]
+    q, k, v, do = make_inputs(w.b, w.S, w.h, w.n_kv, w.d, w.seed, w.amplitude, with_dout=True)
+    rows = sample_rows(w.S, w.n_shards, 24, w.seed)
+    mask = torch.zeros(w.S, dtype=torch.bool)
+    mask[torch.from_numpy(rows)] = True
+    do_m = torch.where(mask[None, :, None, None], do, torch.zeros_like(do))
+    qd, kd, vd, dod = (t.cuda() for t in (q, k, v, do_m))
+    out, lse = ra.ring_attention(qd, kd, vd, w.n_shards, STRIPED, True)
+    dq, dk, dv = ra.ring_attention_bwd(qd, kd, vd, out, lse, dod, w.n_shards, STRIPED, True)
+    ra.stream_check()
+    idx = torch.from_numpy(rows).cuda()
+    dq_rows = dq.index_select(1, idx).double().cpu().numpy()
+    dk, dv = dk.double().cpu().numpy(), dv.double().cpu().numpy()
+    del qd, kd, vd, dod, out, lse, dq
+    rq, rk, rv = orc.attn_bwd_rows(q, k, v, do, True, rows=rows)
+    errs = (_err(dq_rows, rq), _err(dk, rk), _err(dv, rv))
+    assert max(errs) <= G_TOL, errs
