@@ -543,126 +543,48 @@ def run_ours(a, rank, world, local_rank):
                 "peak_note": f"{peaks['source']} bf16 sustained; frac of burst "
                              f"{achieved / peaks['bf16']:.3f}"}
 
-    # end to end through the public API with host buffers
+    # end to end through the C ABI's host-buffer pipeline (ra_pipeline_*):
+    # every step copies its inputs up from pinned host memory and its results
+    # back inside the timed region
     e2e = None
     if not a.no_e2e:
-        hq_ = q.cpu().pin_memory()
-        hk_ = k.cpu().pin_memory()
-        hv_ = v.cpu().pin_memory()
-        hdo = do.cpu().pin_memory()
-        h_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
-        h_lse = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
-        h_dq = torch.empty(dq.shape, dtype=dq.dtype, pin_memory=True)
-        h_dk = torch.empty(dk.shape, dtype=dk.dtype, pin_memory=True)
-        h_dv = torch.empty(dv.shape, dtype=dv.dtype, pin_memory=True)
-        h2d = sum(t.numel() * t.element_size() for t in (hq_, hk_, hv_) + ((hdo,) if have_bwd else ()))
-        d2h = sum(t.numel() * t.element_size() for t in (h_out, h_lse) +
-                  ((h_dq, h_dk, h_dv) if have_bwd else ()))
-
-        # Two device buffer sets and two copy streams: step s+1's inputs go up
-        # and step s's results come down while step s computes.  Every step
-        # still copies its own inputs from pinned host memory and reads its
-        # own results back inside the timed region.  Within a step, dO goes up
-        # after Q, K, V (the forward does not read it) and out, lse come down
-        # as soon as the forward has written them, while the backward runs.
-        sets = [dict(q=q, k=k, v=v, do=do, out=out, lse=lse, dq=dq, dk=dk, dv=dv)]
-        sets.append({name: torch.empty_like(t) for name, t in sets[0].items()})
-        up = torch.cuda.Stream(device=dev)
-        down = torch.cuda.Stream(device=dev)
-
-        def _event(st):
-            ev = torch.cuda.Event()
-            ev.record(st)
-            return ev
-
-        def h2d_into(bs, after):
-            with torch.cuda.stream(up):
-                if after is not None:
-                    up.wait_event(after)
-                bs["q"].copy_(hq_, non_blocking=True)
-                bs["k"].copy_(hk_, non_blocking=True)
-                bs["v"].copy_(hv_, non_blocking=True)
-                qkv_ev = _event(up)
-                do_ev = None
-                if have_bwd:
-                    bs["do"].copy_(hdo, non_blocking=True)
-                    do_ev = _event(up)
-                return qkv_ev, do_ev
-
-        def compute(bs, ready, outputs_free):
-            qkv_ev, do_ev = ready
-            stream.wait_event(qkv_ev)
-            if outputs_free is not None:
-                stream.wait_event(outputs_free)
-            ra.ring_attention(bs["q"], bs["k"], bs["v"], w.n_shards, layout, w.causal,
-                              out=bs["out"], lse=bs["lse"])
-            fwd_ev = _event(stream)
-            if have_bwd:
-                stream.wait_event(do_ev)
-                ra.ring_attention_bwd(bs["q"], bs["k"], bs["v"], bs["out"], bs["lse"], bs["do"],
-                                      w.n_shards, layout, w.causal, dq=bs["dq"], dk=bs["dk"],
-                                      dv=bs["dv"], workspace=ws)
-            return fwd_ev, _event(stream)
-
-        def d2h_from(bs, done):
-            fwd_ev, all_ev = done
-            with torch.cuda.stream(down):
-                down.wait_event(fwd_ev)
-                h_out.copy_(bs["out"], non_blocking=True)
-                h_lse.copy_(bs["lse"], non_blocking=True)
-                if have_bwd:
-                    down.wait_event(all_ev)
-                    h_dq.copy_(bs["dq"], non_blocking=True)
-                    h_dk.copy_(bs["dk"], non_blocking=True)
-                    h_dv.copy_(bs["dv"], non_blocking=True)
-                return _event(down)
+        host = {}
+        for name, t in (("q", q), ("k", k), ("v", v)) + ((("do", do),) if have_bwd else ()):
+            host[name] = ra.HostBuffer(t.shape, t.dtype)
+            host[name].tensor.copy_(t.cpu())
+        outs = [("out", out), ("lse", lse)] + ([("dq", dq), ("dk", dk), ("dv", dv)]
+                                               if have_bwd else [])
+        for name, t in outs:
+            host[name] = ra.HostBuffer(t.shape, t.dtype)
+        h2d = sum(host[n].nbytes for n in ("q", "k", "v", "do") if n in host)
+        d2h = sum(host[n].nbytes for n, _ in outs)
+        pl = ra.Pipeline(w.S, w.n_shards, layout, w.causal, w.b, w.h, w.n_kv, w.d,
+                         backward=have_bwd)
 
         def e2e_run(n_steps):
-            comp_ev = [None, None]     # last compute on each set (its inputs are read)
-            down_ev = [None, None]     # last read-back of each set (its outputs are free)
-            ready = h2d_into(sets[0], None)
-            for s_ in range(n_steps):
-                cur, nxt = s_ % 2, (s_ + 1) % 2
-                comp_ev[cur] = compute(sets[cur], ready, down_ev[cur])
-                if s_ + 1 < n_steps:
-                    ready = h2d_into(sets[nxt], None if comp_ev[nxt] is None else comp_ev[nxt][1])
-                down_ev[cur] = d2h_from(sets[cur], comp_ev[cur])
+            for _ in range(n_steps):
+                pl.submit(host["q"], host["k"], host["v"], host.get("do"), host["out"],
+                          host["lse"], host.get("dq"), host.get("dk"), host.get("dv"))
+            pl.sync()
 
         e2e_run(2)
-        torch.cuda.synchronize()
         if world > 1:
             torch.distributed.barrier()
-        s0 = torch.cuda.Event(enable_timing=True)
-        s1 = torch.cuda.Event(enable_timing=True)
-        s0.record(up)
-        stream.wait_event(_event(up))
+        t0 = time.perf_counter()
         e2e_run(a.steps)
-        down.wait_stream(stream)
-        down.wait_stream(up)
-        s1.record(down)
-        torch.cuda.synchronize()
-        ra.stream_check()
-        e2e_ms = s0.elapsed_time(s1)
+        e2e_ms = (time.perf_counter() - t0) * 1e3
         e2e_ms = max_over_ranks(e2e_ms, world, dev)
-        # The host link's copy rate on this machine, one direction at a time,
-        # to read the end-to-end figure against.
-        link = {}
-        for name, (dst, src, st) in {"h2d_gbs": (q, hq_, up), "d2h_gbs": (h_dq, dq, down)}.items():
-            c0 = torch.cuda.Event(enable_timing=True)
-            c1 = torch.cuda.Event(enable_timing=True)
-            with torch.cuda.stream(st):
-                c0.record(st)
-                dst.copy_(src, non_blocking=True)
-                c1.record(st)
-            c1.synchronize()
-            link[name] = src.numel() * src.element_size() / (c0.elapsed_time(c1) * 1e6)
+        pl.close()
+        for hb in host.values():
+            hb.free()
         e2e = {"value": job_rate(step_flops, a.steps, world, e2e_ms), "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": e2e_ms / a.steps,
-               "host_link": {k_: round(v_, 1) for k_, v_ in link.items()},
-               "schedule": "two device buffer sets; step s+1's H2D and step s's D2H on "
-                           "their own streams, overlapping compute; dO goes up after Q, K, V "
-                           "and out, lse come down while the backward runs"}
+               "host_numa_node": ra.host_numa_node(),
+               "api": "ra_pipeline_submit x steps, then ra_pipeline_sync (host wall clock)",
+               "schedule": "two device buffer sets, copy streams up and down: step s+1's "
+                           "inputs go up and step s's results come down while step s "
+                           "computes; out, lse leave while the backward runs"}
 
     extras = None
     if rank == 0 and not a.no_extras:

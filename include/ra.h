@@ -239,6 +239,56 @@ ra_status ra_ring_attention_bwd_noalloc(const uint16_t *q, const uint16_t *k, co
                                         ra_layout layout, int causal, float scale, ra_dims dims,
                                         void *stream);
 
+/* ---- Host buffers.  The pages have no counterpart to these calls: on one
+ * GPU there is no ring transfer, and they are the host-side plumbing that
+ * moves a step's inputs in and its results out. */
+
+/* Pinned (page-locked) host memory of `bytes`, allocated while the calling
+ * thread runs on the CPUs of the NUMA node nearest the current device
+ * (cudaDevAttrHostNumaId), so copies do not cross a CPU socket link.  *ptr is
+ * NULL for bytes == 0.  Free with ra_host_free.  RA_ERR_CUDA if the pinned
+ * allocation fails. */
+ra_status ra_host_alloc(size_t bytes, void **ptr);
+ra_status ra_host_free(void *ptr);
+/* NUMA node nearest the current device, or -1 when unknown. */
+int ra_host_numa_node(void);
+
+/* A pipeline of ring-attention steps on host buffers: each submitted step
+ * copies q, k, v (and dout) in, runs ra_ring_attention (and
+ * ra_ring_attention_bwd), and copies out, lse (and dq, dk, dv) back.  Two
+ * device buffer sets and three streams overlap step n+1's input copies and
+ * step n's result copies with step n's compute; out and lse leave while the
+ * backward runs.  Shapes, dtypes and layouts are those of ra_ring_attention
+ * and ra_ring_attention_bwd, in host memory (pinned memory from
+ * ra_host_alloc overlaps; pageable memory works but its copies do not).
+ * Opaque; one pipeline serves one thread at a time. */
+typedef struct ra_pipeline ra_pipeline;
+
+/* Allocates both buffer sets and the backward workspace on the current
+ * device (about 2 x (2 + 2 + 4 + 4) x b S h d bytes with the backward).
+ * RA_ERR_UNSUPPORTED for dims the kernels do not take, RA_ERR_CUDA if the
+ * device allocation fails. */
+ra_status ra_pipeline_create(int64_t S, int n_shards, ra_layout layout, int causal, float scale,
+                             ra_dims dims, int backward, ra_pipeline **pipeline);
+
+/* Enqueue one step and return.  Inputs: q [b,S,h,d], k, v [b,S,n_kv,d],
+ * dout [b,S,h,d] bf16 (dout only with the backward).  Outputs (any may be
+ * NULL to skip that copy): out [b,S,h,d], lse [b,h,S], dq [b,S,h,d],
+ * dk, dv [b,S,n_kv,d] float.  Every host buffer must stay valid, and the
+ * inputs unchanged, until ra_pipeline_sync returns.  Errors of the attention
+ * calls are returned as they are; after a non-OK status destroy the
+ * pipeline. */
+ra_status ra_pipeline_submit(ra_pipeline *pipeline, const uint16_t *q, const uint16_t *k,
+                             const uint16_t *v, const uint16_t *dout, float *out, float *lse,
+                             float *dq, float *dk, float *dv);
+
+/* Wait for every submitted step (its results are then in the host buffers);
+ * reports device timeouts and CUDA errors as ra_stream_check does. */
+ra_status ra_pipeline_sync(ra_pipeline *pipeline);
+
+/* Wait, then free the pipeline's device memory, streams and events. */
+ra_status ra_pipeline_destroy(ra_pipeline *pipeline);
+
 /* Token placement maps (the third page's section 6 example; "Striped
  * Attention" and "Zig-Zag Ring Attention" on the first page), computed on the
  * device by the same functions the attention kernels use:

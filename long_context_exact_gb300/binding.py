@@ -94,6 +94,20 @@ def load(path: str | None = None):
         lib.ra_ex2_probe_threads.restype = I64
         lib.ra_launch_count.argtypes = []
         lib.ra_launch_count.restype = ctypes.c_uint64
+        lib.ra_host_alloc.argtypes = [ctypes.c_size_t, ctypes.POINTER(P)]
+        lib.ra_host_alloc.restype = I
+        lib.ra_host_free.argtypes = [P]
+        lib.ra_host_free.restype = I
+        lib.ra_host_numa_node.argtypes = []
+        lib.ra_host_numa_node.restype = I
+        lib.ra_pipeline_create.argtypes = [I64, I, I, I, F, Dims, I, ctypes.POINTER(P)]
+        lib.ra_pipeline_create.restype = I
+        lib.ra_pipeline_submit.argtypes = [P, P, P, P, P, P, P, P, P, P]
+        lib.ra_pipeline_submit.restype = I
+        lib.ra_pipeline_sync.argtypes = [P]
+        lib.ra_pipeline_sync.restype = I
+        lib.ra_pipeline_destroy.argtypes = [P]
+        lib.ra_pipeline_destroy.restype = I
         _lib = lib
         return lib
 
@@ -353,3 +367,90 @@ def ex2_probe(iters: int, sink=None, stream=None):
 
 def selftest_wait_timeout(budget_cycles: int, stream=None):
     _check(load().ra_selftest_wait_timeout(int(budget_cycles), _stream(stream)))
+
+
+# ------------------------------------------------------------------ host buffers
+class HostBuffer:
+    """Pinned host memory from ``ra_host_alloc`` (on the NUMA node nearest the
+    current GPU), viewed as a CPU tensor ``.tensor`` of the given shape and
+    dtype.  The memory is freed by ``free()`` or when this object is
+    collected; keep the object alive while ``.tensor`` (or a view) is used."""
+
+    def __init__(self, shape, dtype):
+        lib = load()
+        shape = tuple(int(x) for x in shape)
+        nbytes = torch.Size(shape).numel() * torch.empty((), dtype=dtype).element_size()
+        ptr = ctypes.c_void_p()
+        _check(lib.ra_host_alloc(nbytes, ctypes.byref(ptr)))
+        self._ptr = ptr.value
+        self.nbytes = nbytes
+        if nbytes == 0:
+            self.tensor = torch.empty(shape, dtype=dtype)
+        else:
+            raw = (ctypes.c_uint8 * nbytes).from_address(self._ptr)
+            self.tensor = torch.frombuffer(raw, dtype=torch.uint8).view(dtype).view(shape)
+
+    def data_ptr(self) -> int:
+        return self._ptr or 0
+
+    def free(self):
+        if getattr(self, "_ptr", None):
+            self.tensor = None
+            _check(load().ra_host_free(ctypes.c_void_p(self._ptr)))
+            self._ptr = None
+
+    def __del__(self):
+        try:
+            self.free()
+        except Exception:
+            pass
+
+
+def host_numa_node() -> int:
+    return int(load().ra_host_numa_node())
+
+
+class Pipeline:
+    """``ra_pipeline``: ring-attention steps on host buffers, each step's
+    copies overlapped with its neighbours' compute (two device buffer sets,
+    three streams).  ``submit`` takes CPU tensors (or ``HostBuffer``s) and
+    returns at once; ``sync`` waits for every submitted step."""
+
+    def __init__(self, S: int, n_shards: int, layout: int, causal: bool, b: int, h: int,
+                 n_kv: int, d: int, backward: bool = True, scale: float = 0.0):
+        lib = load()
+        handle = ctypes.c_void_p()
+        _check(lib.ra_pipeline_create(S, n_shards, layout, int(bool(causal)), scale,
+                                      _dims(b, h, n_kv, d), int(bool(backward)),
+                                      ctypes.byref(handle)))
+        self._h = handle.value
+        self.backward = backward
+
+    @staticmethod
+    def _hp(x):
+        if x is None:
+            return None
+        if isinstance(x, HostBuffer):
+            return ctypes.c_void_p(x.data_ptr())
+        if x.is_cuda or not x.is_contiguous():
+            raise RAError(RA_ERR_INVALID_ARG, "pipeline buffers are contiguous host tensors")
+        return ctypes.c_void_p(x.data_ptr())
+
+    def submit(self, q, k, v, dout=None, out=None, lse=None, dq=None, dk=None, dv=None):
+        hp = self._hp
+        _check(load().ra_pipeline_submit(ctypes.c_void_p(self._h), hp(q), hp(k), hp(v), hp(dout),
+                                         hp(out), hp(lse), hp(dq), hp(dk), hp(dv)))
+
+    def sync(self):
+        _check(load().ra_pipeline_sync(ctypes.c_void_p(self._h)))
+
+    def close(self):
+        if getattr(self, "_h", None):
+            load().ra_pipeline_destroy(ctypes.c_void_p(self._h))
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

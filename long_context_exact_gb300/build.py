@@ -19,7 +19,7 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libra.so")
 ROOT = os.path.dirname(HERE)
 
-SOURCES = ["ra_api.cu", "ra_fwd.cu", "ra_bwd.cu", "ra_small.cu", "ra_noalloc.cu"]
+SOURCES = ["ra_api.cu", "ra_fwd.cu", "ra_bwd.cu", "ra_small.cu", "ra_noalloc.cu", "ra_host.cu"]
 HEADERS = ["ra_ptx.cuh", "ra_internal.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",

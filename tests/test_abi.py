@@ -199,3 +199,28 @@ def test_binding_refuses_cpu_tensors(lib):
     q = torch.zeros((1, 128, 2, 64), dtype=torch.bfloat16)
     with pytest.raises(binding.RAError):
         binding.ring_attention(q, q, q, 1)
+
+
+def test_host_buffer_and_pipeline_validation(lib):
+    """Argument checks of the host-buffer calls, all before any CUDA call."""
+    P = ctypes.c_void_p
+    out = P()
+    assert lib.ra_host_alloc(0, ctypes.byref(out)) == binding.RA_OK and out.value is None
+    assert lib.ra_host_alloc(16, None) == binding.RA_ERR_INVALID_ARG
+    assert lib.ra_host_free(None) == binding.RA_OK
+    h = P()
+    create = lib.ra_pipeline_create
+    assert create(1024, 4, 1, 1, 0.0, _dims(), 1, None) == binding.RA_ERR_INVALID_ARG
+    assert create(0, 4, 1, 1, 0.0, _dims(), 1, ctypes.byref(h)) == binding.RA_ERR_INVALID_ARG
+    assert create(1024, 0, 1, 1, 0.0, _dims(), 1, ctypes.byref(h)) == binding.RA_ERR_INVALID_ARG
+    assert create(8, 16, 1, 1, 0.0, _dims(), 1, ctypes.byref(h)) == binding.RA_ERR_INVALID_ARG
+    assert create(1024, 4, 1, 1, 0.0, _dims(d=96), 1, ctypes.byref(h)) == \
+        binding.RA_ERR_UNSUPPORTED
+    assert create(1024, 4, 1, 1, 0.0, _dims(h=6, n_kv=4), 1, ctypes.byref(h)) == \
+        binding.RA_ERR_UNSUPPORTED
+    assert create(1024, 4, 7, 1, 0.0, _dims(), 1, ctypes.byref(h)) == binding.RA_ERR_INVALID_ARG
+    assert h.value is None
+    assert lib.ra_pipeline_submit(None, FAKE, FAKE, FAKE, FAKE, None, None, None, None,
+                                  None) == binding.RA_ERR_INVALID_ARG
+    assert lib.ra_pipeline_sync(None) == binding.RA_ERR_INVALID_ARG
+    assert lib.ra_pipeline_destroy(None) == binding.RA_OK
