@@ -62,3 +62,45 @@ def test_noalloc_rejects_problems_beyond_its_scratch(lib):
                                            S, 8, STRIPED, 1, 0.0, ra.Dims(b, h, n_kv, d), None)
     assert st == ra.RA_ERR_WORKSPACE
     assert b"allocation-free" in lib.ra_last_error()
+
+
+def test_forward_and_noalloc_backward_replay_as_a_cuda_graph(lib):
+    """A whole step (ring forward, allocation-free backward) captured once as
+    a CUDA graph and replayed on new inputs copied into the same buffers
+    gives the eager results: no call in the path allocates or synchronises."""
+    b, S, h, n_kv, d, N, layout = 1, 2048, 8, 2, 128, 4, STRIPED
+    first = [t.cuda() for t in make_inputs(b, S, h, n_kv, d, seed=21, with_dout=True)]
+    second = [t.cuda() for t in make_inputs(b, S, h, n_kv, d, seed=22, with_dout=True)]
+    q, k, v, do = (t.clone() for t in first)
+    out = torch.empty((b, S, h, d), dtype=torch.float32, device="cuda")
+    lse = torch.empty((b, h, S), dtype=torch.float32, device="cuda")
+    dq = torch.empty((b, S, h, d), dtype=torch.float32, device="cuda")
+    dk = torch.empty((b, S, n_kv, d), dtype=torch.float32, device="cuda")
+    dv = torch.empty_like(dk)
+
+    def step():
+        ra.ring_attention(q, k, v, N, layout, True, out=out, lse=lse)
+        ra.ring_attention_bwd_noalloc(q, k, v, out, lse, do, N, layout, True, dq=dq, dk=dk, dv=dv)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step()                      # warm-up outside the capture (scratch address lookup)
+    torch.cuda.current_stream().wait_stream(side)
+    ra.stream_check()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    for inputs in (second, first):
+        for dst, src in zip((q, k, v, do), inputs):
+            dst.copy_(src)
+        for t in (out, lse, dq, dk, dv):
+            t.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        ra.stream_check()
+        e_out, e_lse = ra.ring_attention(*inputs[:3], N, layout, True)
+        e_grads = ra.ring_attention_bwd(*inputs[:3], e_out, e_lse, inputs[3], N, layout, True)
+        assert torch.equal(out, e_out) and torch.equal(lse, e_lse)
+        for got, want in zip((dq, dk, dv), e_grads):
+            assert float((got - want).abs().max()) <= 1e-5
