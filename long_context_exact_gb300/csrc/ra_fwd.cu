@@ -27,6 +27,9 @@
 // max used as the exponent shift is only raised when a row's max grows by
 // more than 8 (log2 units), so most tiles skip the O rescale; P stays
 // <= 2^8 and the result is unchanged because O and l share the same shift.
+// Once every row of a warp has a shift, P is formed against it before the
+// tile's row max is known (the max is taken while the P stores drain); the
+// rare tile whose max passes a row's shift by more than 8 is formed again.
 // The exact running max is tracked alongside for the block-step state.
 //
 // Precision: tiles whose rows see fewer than kSplitKeys keys (and every
@@ -637,28 +640,22 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::kThreads, 1)
         }
       }
       // row max as eight short 3-input-max chains, then a small tree
-      float pm[8];
+      auto row_max = [&]() {
+        float pm[8];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) pm[k] = s[k];
+        for (int k = 0; k < 8; ++k) pm[k] = s[k];
 #pragma unroll
-      for (int e = 8; e + 16 <= kTile; e += 16)
+        for (int e = 8; e + 16 <= kTile; e += 16)
 #pragma unroll
-        for (int k = 0; k < 8; ++k) pm[k] = fmax3(pm[k], s[e + k], s[e + 8 + k]);
+          for (int k = 0; k < 8; ++k) pm[k] = fmax3(pm[k], s[e + k], s[e + 8 + k]);
 #pragma unroll
-      for (int k = 0; k < 8; ++k) pm[k] = fmaxf(pm[k], s[kTile - 8 + k]);
-      const float mx = fmax3(fmax3(pm[0], pm[1], pm[2]), fmax3(pm[3], pm[4], pm[5]),
-                             fmaxf(pm[6], pm[7]));
-      const float mx2 = mx * sl2;
-      m_max = fmaxf(m_max, mx2);
-      const bool need = mx2 > m_run + kRescaleThreshold;
-      float alpha = 1.f;
-      if (need) {
-        alpha = ex2(m_run - mx2);  // 0 when m_run is still -inf
-        m_run = mx2;
-      }
-      if (n > 0 && __any_sync(kFull, need)) {
-        // O_t row *= alpha.  The previous PV into O_t is complete: it was
-        // issued before this tile's S MMA, whose commit we waited on.
+        for (int k = 0; k < 8; ++k) pm[k] = fmaxf(pm[k], s[kTile - 8 + k]);
+        return fmax3(fmax3(pm[0], pm[1], pm[2]), fmax3(pm[3], pm[4], pm[5]),
+                     fmaxf(pm[6], pm[7]));
+      };
+      // O_t row *= alpha.  The previous PV into O_t is complete: it was
+      // issued before this tile's S MMA, whose commit we waited on.
+      auto rescale_o = [&](float alpha) {
 #pragma unroll
         for (int ch = 0; ch < D / 32; ++ch) {
           uint32_t r[32];
@@ -667,14 +664,45 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::kThreads, 1)
           for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
           tmem_st32(tO + ch * 32, r);
         }
-      }
-      l_sum *= alpha;
-      const float base = (m_run == -INFINITY) ? 0.f : m_run;
+      };
       // P = 2^(s * scale * log2 e - shift): paired FMAs, four paired sums
       const uint64_t sl2x2 = f2pack(sl2, sl2);
-      const uint64_t nbx2 = f2pack(-base, -base);
       uint64_t acc[4];
-      exp_pack_store<kSplit>(s, sl2x2, nbx2, acc, tS);
+      // When every row of the warp already has a shift, P is formed against
+      // it while the row max is computed alongside; a row whose max passed
+      // its shift by more than the threshold (rare after the first tiles)
+      // takes a new shift and the warp forms the tile's P again.
+      bool spec = __all_sync(kFull, m_run != -INFINITY);
+      if (!spec) {
+        const float mx2 = row_max() * sl2;
+        m_max = fmaxf(m_max, mx2);
+        const bool need = mx2 > m_run + kRescaleThreshold;
+        float alpha = 1.f;
+        if (need) {
+          alpha = ex2(m_run - mx2);  // 0 when m_run is still -inf
+          m_run = mx2;
+        }
+        if (n > 0 && __any_sync(kFull, need)) rescale_o(alpha);
+        l_sum *= alpha;
+      }
+      for (;;) {
+        const float base = (m_run == -INFINITY) ? 0.f : m_run;
+        exp_pack_store<kSplit>(s, sl2x2, f2pack(-base, -base), acc, tS);
+        if (!spec) break;
+        spec = false;
+        const float mx2 = row_max() * sl2;
+        m_max = fmaxf(m_max, mx2);
+        const bool need = mx2 > m_run + kRescaleThreshold;
+        if (!__any_sync(kFull, need)) break;
+        float alpha = 1.f;
+        if (need) {
+          alpha = ex2(m_run - mx2);
+          m_run = mx2;
+        }
+        rescale_o(alpha);
+        l_sum *= alpha;
+        tmem_st_wait();  // the first P stores have landed before they are overwritten
+      }
       float a0, a1, a2, a3, a4, a5, a6, a7;
       f2unpack(acc[0], a0, a1);
       f2unpack(acc[1], a2, a3);
