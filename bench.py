@@ -36,7 +36,7 @@ WORKLOAD = "causal256k"
 # (dram__bytes_read.sum + dram__bytes_write.sum, one pass, this workload),
 # valid only while the kernel source hashes match (see profiles/).
 TRAFFIC = {
-    "bwd": {"bytes_per_launch": 118881081088 + 81189988864, "src_sha": "31a652306f118ddb",
+    "bwd": {"bytes_per_launch": 118902303488 + 81194302464, "src_sha": "fdd987cd1d197d82",
             "profile": "profiles/traffic_bwd_causal256k.md"},
 }
 

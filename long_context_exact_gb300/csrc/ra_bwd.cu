@@ -912,41 +912,60 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
 // -D = -rowsum(dO * O) and -LSE2 = -LSE * log2(e) per (batch, head, query
 // row), stored negated so the main kernel adds them with f32x2 arithmetic,
 // written in shard-local order [b, h, N, Lpad]; padding rows get D = 0 and
-// -LSE2 = -inf (their P is exactly 0).  One warp per row.
+// -LSE2 = -inf (their P is exactly 0).  One warp per row, four rows in flight.
 template <int D>
 __global__ void bwd_pre_kernel(BwdParams p, const float *out, const float *lse,
                                const uint16_t *dout) {
-  const long long rows = static_cast<long long>(p.b) * p.h * p.N * p.Lpad;
+  // blockIdx.y walks the (batch, head, shard) row groups of the workspace,
+  // blockIdx.x the rows of a group, four rows in flight per warp.
+  constexpr int kRows = 4;
   const int lane = threadIdx.x & 31;
   const long long warps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
-  for (long long w = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; w < rows;
-       w += warps) {
-    const int r = static_cast<int>(w % p.Lpad);
-    long long t = w / p.Lpad;
-    const int i = static_cast<int>(t % p.N);
-    t /= p.N;
-    const int hq = static_cast<int>(t % p.h);
-    const long long bb = t / p.h;
-    float dsum = 0.f, l2 = INFINITY;
-    if (r < p.L) {
-      const int tok = token_at(p.layout, p.L, p.N, i, r);
-      const size_t row = ((bb * p.S + tok) * p.h + hq) * D;
-      const float4 *o4 = reinterpret_cast<const float4 *>(out + row);
-      const uint2 *g4 = reinterpret_cast<const uint2 *>(dout + row);
-      for (int e = lane; e < D / 4; e += 32) {
-        const float4 o = o4[e];
-        const uint2 gg = g4[e];
-        dsum += o.x * __uint_as_float(gg.x << 16) + o.y * __uint_as_float(gg.x & 0xffff0000u) +
-                o.z * __uint_as_float(gg.y << 16) + o.w * __uint_as_float(gg.y & 0xffff0000u);
+  const long long r0 = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const long long groups = static_cast<long long>(p.b) * p.h * p.N;
+  for (long long g = blockIdx.y; g < groups; g += gridDim.y) {
+    const int i = static_cast<int>(g % p.N);
+    const long long bh = g / p.N;
+    const int hq = static_cast<int>(bh % p.h);
+    const long long bb = bh / p.h;
+    for (long long base = r0; base < p.Lpad; base += kRows * warps) {
+      // lane e holds columns 4e..4e+3 of each row (d = 64 uses half the warp)
+      float4 o[kRows];
+      uint2 gg[kRows];
+      float lv[kRows];
+#pragma unroll
+      for (int k = 0; k < kRows; ++k) {
+        const long long r = base + k * warps;
+        if (r < p.L) {
+          const int tok = token_at(p.layout, p.L, p.N, i, static_cast<int>(r));
+          const size_t row = ((bb * p.S + tok) * p.h + hq) * D;
+          if (lane < D / 4) {
+            o[k] = reinterpret_cast<const float4 *>(out + row)[lane];
+            gg[k] = reinterpret_cast<const uint2 *>(dout + row)[lane];
+          }
+          lv[k] = lse[(bb * p.h + hq) * p.S + tok];
+        }
       }
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) dsum += __shfl_xor_sync(kFull, dsum, o);
-      const float lv = lse[(bb * p.h + hq) * p.S + tok];
-      l2 = (lv == -INFINITY) ? INFINITY : lv * kLog2e;
-    }
-    if (lane == 0) {
-      p.dvec[w] = -dsum;
-      p.lse2[w] = -l2;
+      for (int k = 0; k < kRows; ++k) {
+        const long long r = base + k * warps;
+        if (r >= p.Lpad) continue;
+        float dsum = 0.f, l2 = INFINITY;  // padding rows: D = 0, P = 0
+        if (r < p.L) {
+          if (lane < D / 4)
+            dsum = o[k].x * __uint_as_float(gg[k].x << 16) +
+                   o[k].y * __uint_as_float(gg[k].x & 0xffff0000u) +
+                   o[k].z * __uint_as_float(gg[k].y << 16) +
+                   o[k].w * __uint_as_float(gg[k].y & 0xffff0000u);
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1) dsum += __shfl_xor_sync(kFull, dsum, off);
+          l2 = (lv[k] == -INFINITY) ? INFINITY : lv[k] * kLog2e;
+        }
+        if (lane == 0) {
+          p.dvec[g * p.Lpad + r] = -dsum;
+          p.lse2[g * p.Lpad + r] = -l2;
+        }
+      }
     }
   }
 }
@@ -959,11 +978,16 @@ cudaError_t launch_bwd_t(const BwdParams &p, const float *out, const float *lse,
                          const CUtensorMap &dvmap, long long n_units, int n_sm,
                          cudaStream_t stream) {
   using C = BwdCfg<D>;
-  const long long pre_rows = static_cast<long long>(p.b) * p.h * p.N * p.Lpad;
-  long long pre_blocks = (pre_rows * 32 + 255) / 256;
-  if (pre_blocks > static_cast<long long>(n_sm) * 8) pre_blocks = static_cast<long long>(n_sm) * 8;
-  if (pre_blocks < 1) pre_blocks = 1;
-  bwd_pre_kernel<D><<<static_cast<unsigned int>(pre_blocks), 256, 0, stream>>>(p, out, lse, dout);
+  // about eight CTAs of 256 threads per SM: y over the (batch, head, shard)
+  // row groups, x over the rows of a group (32 rows per CTA and trip)
+  const long long groups = static_cast<long long>(p.b) * p.h * p.N;
+  const long long gy = groups < 65535 ? (groups < 1 ? 1 : groups) : 65535;
+  long long gx = (p.Lpad + 31) / 32;
+  const long long cap = (static_cast<long long>(n_sm) * 8 + gy - 1) / gy;
+  if (gx > cap) gx = cap;
+  if (gx < 1) gx = 1;
+  bwd_pre_kernel<D><<<dim3(static_cast<unsigned int>(gx), static_cast<unsigned int>(gy)), 256, 0,
+                      stream>>>(p, out, lse, dout);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   auto kern = p.cu != nullptr ? bwd_kernel<D, true> : bwd_kernel<D, false>;

@@ -28,57 +28,67 @@ inline unsigned int ew_grid(long long work) {
   return static_cast<unsigned int>(want < 1 ? 1 : (want < cap ? want : cap));
 }
 
+// Grid for the row kernels below: blockIdx.y walks the (batch, head) pairs,
+// blockIdx.x the rows of one pair, so no thread divides a row index; about
+// eight CTAs per SM in all.
+inline dim3 rows_grid(long long pairs, long long rows_per_pair, int rows_per_warp) {
+  const long long ctas = static_cast<long long>(ew_grid(1LL << 40));
+  const long long gy = pairs < 65535 ? pairs : 65535;
+  const long long per_cta = static_cast<long long>(kEwThreads / 32) * rows_per_warp;
+  long long gx = (rows_per_pair + per_cta - 1) / per_cta;
+  const long long cap = (ctas + gy - 1) / gy;
+  if (gx > cap) gx = cap;
+  if (gx < 1) gx = 1;
+  return dim3(static_cast<unsigned int>(gx), static_cast<unsigned int>(gy < 1 ? 1 : gy));
+}
+
 // Rows handled per warp and loop trip by the two HBM-bound kernels below:
 // their loads are all issued before any result is formed, so each warp keeps
 // kRowsPerTrip rows of every operand in flight (one float4 per lane and row).
 constexpr int kRowsPerTrip = 4;
-
-// Decompose warp-row index w of [b, h, Lq] into the float offset of its
-// [b, Lq, h, d] row.
-__device__ __forceinline__ size_t row_offset(long long w, long long Lq, int h, int d) {
-  const long long r = w % Lq;
-  const long long bh = w / Lq;
-  const long long hq = bh % h;
-  const long long bb = bh / h;
-  return static_cast<size_t>(((bb * Lq + r) * h + hq) * d);
-}
 
 // One warp per (batch, head, row), lane e holding columns 4e..4e+3 (d = 64
 // uses half the warp).  o <- o / l, lse = m + ln l; rows with l == 0 get 0
 // and -inf.
 __global__ void finalize_kernel(float *o, const float *l, const float *m, float *lse, int b,
                                 long long Lq, int h, int d) {
-  const long long rows = static_cast<long long>(b) * h * Lq;
   const int lane = threadIdx.x & 31;
   const bool col = lane < d / 4;
   const long long warps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
   const long long w0 = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  for (long long base = w0; base < rows; base += kRowsPerTrip * warps) {
-    float4 v[kRowsPerTrip];
-    float lr[kRowsPerTrip], mr[kRowsPerTrip];
+  const size_t ostride = static_cast<size_t>(h) * d;  // floats between rows of one head
+  for (long long bh = blockIdx.y; bh < static_cast<long long>(b) * h; bh += gridDim.y) {
+    const long long bb = bh / h;
+    float *orow = o + (static_cast<size_t>(bb) * Lq * h + (bh - bb * h)) * d;
+    const float *lrow = l + bh * Lq, *mrow = m + bh * Lq;
+    float *lserow = lse + bh * Lq;
+    for (long long base = w0; base < Lq; base += kRowsPerTrip * warps) {
+      float4 v[kRowsPerTrip];
+      float lr[kRowsPerTrip], mr[kRowsPerTrip];
 #pragma unroll
-    for (int k = 0; k < kRowsPerTrip; ++k) {
-      const long long w = base + k * warps;
-      if (w < rows) {
-        lr[k] = l[w];
-        mr[k] = m[w];
-        if (col) v[k] = reinterpret_cast<const float4 *>(o + row_offset(w, Lq, h, d))[lane];
+      for (int k = 0; k < kRowsPerTrip; ++k) {
+        const long long r = base + k * warps;
+        if (r < Lq) {
+          lr[k] = lrow[r];
+          mr[k] = mrow[r];
+          if (col) v[k] = reinterpret_cast<const float4 *>(orow + r * ostride)[lane];
+        }
       }
-    }
 #pragma unroll
-    for (int k = 0; k < kRowsPerTrip; ++k) {
-      const long long w = base + k * warps;
-      if (w < rows) {
-        const bool live = lr[k] > 0.f;
-        const float inv = live ? 1.f / lr[k] : 0.f;
-        if (lane == 0) lse[w] = live ? mr[k] + logf(lr[k]) : -INFINITY;
-        if (col) {
-          float4 x = v[k];
-          x.x *= inv;
-          x.y *= inv;
-          x.z *= inv;
-          x.w *= inv;
-          reinterpret_cast<float4 *>(o + row_offset(w, Lq, h, d))[lane] = x;
+      for (int k = 0; k < kRowsPerTrip; ++k) {
+        const long long r = base + k * warps;
+        if (r < Lq) {
+          const bool live = lr[k] > 0.f;
+          const float inv = live ? 1.f / lr[k] : 0.f;
+          if (lane == 0) lserow[r] = live ? mr[k] + logf(lr[k]) : -INFINITY;
+          if (col) {
+            float4 x = v[k];
+            x.x *= inv;
+            x.y *= inv;
+            x.z *= inv;
+            x.w *= inv;
+            reinterpret_cast<float4 *>(orow + r * ostride)[lane] = x;
+          }
         }
       }
     }
@@ -90,52 +100,56 @@ __global__ void finalize_kernel(float *o, const float *l, const float *m, float 
 __global__ void merge_kernel(const float *o_a, const float *lse_a, const float *o_b,
                              const float *lse_b, float *o, float *lse, int b, long long Lq, int h,
                              int d) {
-  const long long rows = static_cast<long long>(b) * h * Lq;
   const int lane = threadIdx.x & 31;
   const bool col = lane < d / 4;
   const long long warps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
   const long long w0 = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  for (long long base = w0; base < rows; base += kRowsPerTrip * warps) {
-    float4 va[kRowsPerTrip], vb[kRowsPerTrip];
-    float la[kRowsPerTrip], lb[kRowsPerTrip];
+  const size_t ostride = static_cast<size_t>(h) * d;  // floats between rows of one head
+  for (long long bh = blockIdx.y; bh < static_cast<long long>(b) * h; bh += gridDim.y) {
+    const long long bb = bh / h;
+    const size_t obase = (static_cast<size_t>(bb) * Lq * h + (bh - bb * h)) * d;
+    for (long long base = w0; base < Lq; base += kRowsPerTrip * warps) {
+      float4 va[kRowsPerTrip], vb[kRowsPerTrip];
+      float la[kRowsPerTrip], lb[kRowsPerTrip];
 #pragma unroll
-    for (int k = 0; k < kRowsPerTrip; ++k) {
-      const long long w = base + k * warps;
-      if (w < rows) {
-        la[k] = lse_a[w];
-        lb[k] = lse_b[w];
-        if (col) {
-          const size_t off = row_offset(w, Lq, h, d);
-          va[k] = reinterpret_cast<const float4 *>(o_a + off)[lane];
-          vb[k] = reinterpret_cast<const float4 *>(o_b + off)[lane];
+      for (int k = 0; k < kRowsPerTrip; ++k) {
+        const long long r = base + k * warps;
+        if (r < Lq) {
+          la[k] = lse_a[bh * Lq + r];
+          lb[k] = lse_b[bh * Lq + r];
+          if (col) {
+            const size_t off = obase + r * ostride;
+            va[k] = reinterpret_cast<const float4 *>(o_a + off)[lane];
+            vb[k] = reinterpret_cast<const float4 *>(o_b + off)[lane];
+          }
         }
       }
-    }
 #pragma unroll
-    for (int k = 0; k < kRowsPerTrip; ++k) {
-      const long long w = base + k * warps;
-      if (w < rows) {
-        const float mx = fmaxf(la[k], lb[k]);
-        float wa = 0.f, wb = 0.f, out_lse = -INFINITY;
-        if (mx != -INFINITY) {
-          wa = (la[k] == -INFINITY) ? 0.f : expf(la[k] - mx);
-          wb = (lb[k] == -INFINITY) ? 0.f : expf(lb[k] - mx);
-          const float den = wa + wb;
-          out_lse = mx + logf(den);
-          wa /= den;
-          wb /= den;
+      for (int k = 0; k < kRowsPerTrip; ++k) {
+        const long long r = base + k * warps;
+        if (r < Lq) {
+          const float mx = fmaxf(la[k], lb[k]);
+          float wa = 0.f, wb = 0.f, out_lse = -INFINITY;
+          if (mx != -INFINITY) {
+            wa = (la[k] == -INFINITY) ? 0.f : expf(la[k] - mx);
+            wb = (lb[k] == -INFINITY) ? 0.f : expf(lb[k] - mx);
+            const float den = wa + wb;
+            out_lse = mx + logf(den);
+            wa /= den;
+            wb /= den;
+          }
+          if (col) {
+            const float4 a = va[k], c = vb[k];
+            float4 x;
+            x.x = (wa == 0.f ? 0.f : wa * a.x) + (wb == 0.f ? 0.f : wb * c.x);
+            x.y = (wa == 0.f ? 0.f : wa * a.y) + (wb == 0.f ? 0.f : wb * c.y);
+            x.z = (wa == 0.f ? 0.f : wa * a.z) + (wb == 0.f ? 0.f : wb * c.z);
+            x.w = (wa == 0.f ? 0.f : wa * a.w) + (wb == 0.f ? 0.f : wb * c.w);
+            reinterpret_cast<float4 *>(o + obase + r * ostride)[lane] = x;
+          }
+          __syncwarp();
+          if (lane == 0) lse[bh * Lq + r] = out_lse;
         }
-        if (col) {
-          const float4 a = va[k], c = vb[k];
-          float4 x;
-          x.x = (wa == 0.f ? 0.f : wa * a.x) + (wb == 0.f ? 0.f : wb * c.x);
-          x.y = (wa == 0.f ? 0.f : wa * a.y) + (wb == 0.f ? 0.f : wb * c.y);
-          x.z = (wa == 0.f ? 0.f : wa * a.z) + (wb == 0.f ? 0.f : wb * c.z);
-          x.w = (wa == 0.f ? 0.f : wa * a.w) + (wb == 0.f ? 0.f : wb * c.w);
-          reinterpret_cast<float4 *>(o + row_offset(w, Lq, h, d))[lane] = x;
-        }
-        __syncwarp();
-        if (lane == 0) lse[w] = out_lse;
       }
     }
   }
@@ -170,36 +184,43 @@ __global__ void combine_kernel(const float *m, const float *l, const float *o, i
   const int lane = threadIdx.x & 31;
   const bool col = lane < d / 4;
   const long long warps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
-  for (long long w = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-       w < rows; w += warps) {
-    float mx = -INFINITY;
-    for (int z = lane; z < splits; z += 32) mx = fmaxf(mx, m[z * rows + w]);
+  const long long r0 = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const size_t ostride = static_cast<size_t>(h) * d;  // floats between rows of one head
+  for (long long bh = blockIdx.y; bh < static_cast<long long>(b) * h; bh += gridDim.y) {
+    const long long bb = bh / h;
+    const size_t obase = (static_cast<size_t>(bb) * Lq * h + (bh - bb * h)) * d;
+    for (long long r = r0; r < Lq; r += warps) {
+      const long long w = bh * Lq + r;
+      float mx = -INFINITY;
+      for (int z = lane; z < splits; z += 32) mx = fmaxf(mx, m[z * rows + w]);
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-    float den = 0.f;
-    for (int z = lane; z < splits; z += 32) {
-      const float mz = m[z * rows + w];
-      if (mz != -INFINITY) den += l[z * rows + w] * expf(mz - mx);
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
-    const bool live = mx != -INFINITY && den > 0.f;
-    const size_t orow = row_offset(w, Lq, h, d);
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (live && col) {
-      for (int z = 0; z < splits; ++z) {
+      for (int off = 16; off > 0; off >>= 1)
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+      float den = 0.f;
+      for (int z = lane; z < splits; z += 32) {
         const float mz = m[z * rows + w];
-        if (mz == -INFINITY) continue;
-        const float wz = expf(mz - mx) / den;
-        const float4 v = reinterpret_cast<const float4 *>(o + z * rows * d + orow)[lane];
-        acc.x += wz * v.x;
-        acc.y += wz * v.y;
-        acc.z += wz * v.z;
-        acc.w += wz * v.w;
+        if (mz != -INFINITY) den += l[z * rows + w] * expf(mz - mx);
       }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
+      const bool live = mx != -INFINITY && den > 0.f;
+      const size_t orow = obase + r * ostride;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (live && col) {
+        for (int z = 0; z < splits; ++z) {
+          const float mz = m[z * rows + w];
+          if (mz == -INFINITY) continue;
+          const float wz = expf(mz - mx) / den;
+          const float4 v = reinterpret_cast<const float4 *>(o + z * rows * d + orow)[lane];
+          acc.x += wz * v.x;
+          acc.y += wz * v.y;
+          acc.z += wz * v.z;
+          acc.w += wz * v.w;
+        }
+      }
+      if (col) reinterpret_cast<float4 *>(out + orow)[lane] = acc;
+      if (lane == 0) lse[w] = live ? mx + logf(den) : -INFINITY;
     }
-    if (col) reinterpret_cast<float4 *>(out + orow)[lane] = acc;
-    if (lane == 0) lse[w] = live ? mx + logf(den) : -INFINITY;
   }
 }
 
@@ -262,7 +283,8 @@ cudaError_t launch_finalize(float *o, const float *l, const float *m, float *lse
                             long long Lq, int h, int d, cudaStream_t stream) {
   const long long rows = static_cast<long long>(b) * h * Lq;
   if (rows == 0) return cudaSuccess;
-  finalize_kernel<<<ew_grid(rows * 32), kEwThreads, 0, stream>>>(o, l, m, lse, b, Lq, h, d);
+  finalize_kernel<<<rows_grid(static_cast<long long>(b) * h, Lq, kRowsPerTrip), kEwThreads, 0,
+                    stream>>>(o, l, m, lse, b, Lq, h, d);
   return cudaGetLastError();
 }
 
@@ -271,8 +293,8 @@ cudaError_t launch_merge(const float *o_a, const float *lse_a, const float *o_b,
                          int d, cudaStream_t stream) {
   const long long rows = static_cast<long long>(b) * h * Lq;
   if (rows == 0) return cudaSuccess;
-  merge_kernel<<<ew_grid(rows * 32), kEwThreads, 0, stream>>>(o_a, lse_a, o_b, lse_b, o, lse, b,
-                                                              Lq, h, d);
+  merge_kernel<<<rows_grid(static_cast<long long>(b) * h, Lq, kRowsPerTrip), kEwThreads, 0,
+                 stream>>>(o_a, lse_a, o_b, lse_b, o, lse, b, Lq, h, d);
   return cudaGetLastError();
 }
 
@@ -288,8 +310,8 @@ cudaError_t launch_combine(const float *m, const float *l, const float *o, int s
                            float *lse, int b, long long Lq, int h, int d, cudaStream_t stream) {
   const long long rows = static_cast<long long>(b) * h * Lq;
   if (rows == 0) return cudaSuccess;
-  combine_kernel<<<ew_grid(rows * 32), kEwThreads, 0, stream>>>(m, l, o, splits, out, lse, b, Lq,
-                                                                h, d);
+  combine_kernel<<<rows_grid(static_cast<long long>(b) * h, Lq, 1), kEwThreads, 0, stream>>>(
+      m, l, o, splits, out, lse, b, Lq, h, d);
   return cudaGetLastError();
 }
 
