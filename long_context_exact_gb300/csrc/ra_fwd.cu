@@ -47,6 +47,10 @@ namespace ra {
 namespace {
 
 constexpr float kRescaleThreshold = 8.0f;
+// block mode, causal: the per-CTA classification covers up to this many key
+// tiles (2 KB of bits); longer key ranges are classified 32 tiles at a time
+constexpr int kBitTiles = 8192;
+constexpr int kBitWords = kBitTiles / 32;
 constexpr unsigned int kFull = 0xffffffffu;
 
 template <int D, int NQ>
@@ -71,7 +75,10 @@ struct FwdCfg {
   static constexpr int bDrain = bODone + NQ;
   static constexpr int kNumBars = bDrain + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
-  static constexpr int kSmemBytes = kMiscOff + 16;
+  // block mode, causal: keep / mask bits of up to kMaxBitTiles key tiles of
+  // the CTA's key range, classified once by the whole CTA
+  static constexpr int kBitsOff = kMiscOff + 16;
+  static constexpr int kSmemBytes = kBitsOff + 2 * kBitWords * 4;
   static constexpr int kSmemAlloc = kSmemBytes + 1024;
   static constexpr int kSoftmaxWarps = 4 * NQ;
   static constexpr int kProducerWarp = kSoftmaxWarps;
@@ -106,6 +113,10 @@ struct Unit {
   // ring mode: key positions some row of the tile sees form [wlo, whi]; keys
   // in [flo, fhi] are seen by every row; minvis = fewest keys any row sees
   int wlo, whi, flo, fhi, minvis;
+  // block mode, causal: the CTA's keep bits (kBitWords words) and then its
+  // mask bits in shared memory, or null when its range is classified by
+  // windows as it goes
+  const uint32_t *kbits;
 };
 
 // Work-unit order: groups of (batch, kv head, query shard); inside a group the
@@ -125,6 +136,7 @@ __device__ __forceinline__ Unit decode_unit(const FwdParams &p, long long u) {
   x.bb = static_cast<int>(g2 / p.n_kv);
   x.qmin = 0;
   x.qmax = 0;
+  x.kbits = nullptr;
   // block mode with a key split: blockIdx.y selects split_tiles key tiles
   x.kc0 = p.split_tiles > 0 ? static_cast<int>(blockIdx.y) * p.split_tiles : 0;
   x.kc1 = p.split_tiles > 0 ? min(p.n_ktiles, x.kc0 + p.split_tiles) : p.n_ktiles;
@@ -250,6 +262,28 @@ __device__ __forceinline__ bool kv_next(const FwdParams &p, const Unit &x, KvIte
       c = it.c++;
       j = 0;
       partial = c >= n_complete;
+      return true;
+    }
+    if (x.kbits != nullptr) {
+      // classified once per CTA: bit t for tile kc0 + t
+      const int nt = x.kc1 - x.kc0;
+      int t = it.c - x.kc0;
+      while (t < nt) {
+        const uint32_t w = x.kbits[t >> 5] >> (t & 31);
+        if (w != 0) {
+          t += __ffs(w) - 1;
+          break;
+        }
+        t = (t | 31) + 1;
+      }
+      if (t >= nt) {
+        it.c = x.kc1;
+        return false;
+      }
+      c = x.kc0 + t;
+      j = 0;
+      partial = (x.kbits[kBitWords + (t >> 5)] >> (t & 31)) & 1u;
+      it.c = c + 1;
       return true;
     }
     const int lane = threadIdx.x & 31;
@@ -417,12 +451,49 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::kThreads, 1)
     split = x.minvis < kSplitKeys;
   } else {
     const int k0 = x.kc0 * kTile, k1 = min(p.Lk, x.kc1 * kTile);
-    if (k1 - k0 < kSplitKeys) {
+    const int nt = x.kc1 - x.kc0;
+    int *cnt = reinterpret_cast<int *>(smem + C::kMiscOff + 8);
+    if (p.causal && nt > 0 && nt <= kBitTiles) {
+      // Classify the CTA's key tiles once, a warp per tile: keep a tile
+      // when a key precedes the unit's last query, mask it when a key
+      // follows the first query (or the tile is ragged); count on the way
+      // the keys every query sees.
+      uint32_t *bits = reinterpret_cast<uint32_t *>(smem + C::kBitsOff);
+      for (int w = threadIdx.x; w < 2 * kBitWords; w += blockDim.x) bits[w] = 0;
+      __syncthreads();
+      const int n_complete = p.Lk / kTile;
+      int mine = 0;
+      for (int t = warp; t < nt; t += blockDim.x >> 5) {
+        const int tile = x.kc0 + t;
+        int lo = INT_MAX, hi = INT_MIN;
+#pragma unroll
+        for (int e = 0; e < kTile / 32; ++e) {
+          const int kr = tile * kTile + e * 32 + lane;
+          if (kr < p.Lk) {
+            const int v = p.k_pos[kr];
+            lo = min(lo, v);
+            hi = max(hi, v);
+            mine += v <= x.qmin ? 1 : 0;
+          }
+        }
+        lo = warp_min(lo);
+        hi = warp_max(hi);
+        if (lane == 0 && lo <= x.qmax) {
+          atomicOr(&bits[t >> 5], 1u << (t & 31));
+          if (tile >= n_complete || hi > x.qmin) atomicOr(&bits[kBitWords + (t >> 5)], 1u << (t & 31));
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mine += __shfl_xor_sync(kFull, mine, o);
+      if (lane == 0) atomicAdd(cnt, mine);
+      __syncthreads();
+      split = k1 - k0 < kSplitKeys || *cnt < kSplitKeys;
+      x.kbits = bits;
+    } else if (k1 - k0 < kSplitKeys) {
       split = true;
     } else if (!p.causal) {
       split = false;
     } else {
-      int *cnt = reinterpret_cast<int *>(smem + C::kMiscOff + 8);
       int mine = 0;
       for (int kk = k0 + static_cast<int>(threadIdx.x); kk < k1; kk += blockDim.x)
         mine += p.k_pos[kk] <= x.qmin ? 1 : 0;
