@@ -31,10 +31,11 @@
  *    striped placement).
  *
  * Conventions for every call:
- *  - Tensors are dense, row-major, in DEVICE memory, and owned by the caller.
- *    The library allocates no device memory (the allocation-free backward
- *    uses one fixed array in the library's own device memory).  Base pointers
- *    must be 16-byte aligned.
+ *  - Tensors are dense, row-major, in DEVICE memory, and owned by the caller
+ *    (the host-buffer pipeline at the end takes host memory).  The calls
+ *    allocate no device memory, except ra_pipeline_create (its buffer sets)
+ *    and the allocation-free backward's one fixed array in the library's own
+ *    device memory.  Base pointers must be 16-byte aligned.
  *  - bf16 tensors are passed as raw 16-bit patterns (uint16_t).
  *  - Query-side tensors are [b, rows, h, d]; key/value-side tensors are
  *    [b, rows, n_kv, d].  Per-row statistics are [b, h, rows] float.
@@ -106,7 +107,9 @@ typedef struct {
  *   q_pos  [Lq] int32, k_pos [Lk] int32: token positions, used only when
  *          causal != 0 (key c visible to query r iff k_pos[c] <= q_pos[r]).
  * Initial state: m = -inf, l = 0, o = 0.  Rows with no visible key in this
- * block are left unchanged.  Lq or Lk == 0 is a no-op. */
+ * block are left unchanged.  Lq or Lk == 0 is a no-op.  A causal step takes
+ * at most 8,388,608 keys (each CTA classifies its whole key range once, in
+ * shared memory); RA_ERR_UNSUPPORTED above that. */
 ra_status ra_block_step(const uint16_t *q, const uint16_t *k, const uint16_t *v, float *m,
                         float *l, float *o, const int32_t *q_pos, const int32_t *k_pos,
                         int64_t Lq, int64_t Lk, ra_dims dims, int causal, float scale,
@@ -173,7 +176,9 @@ ra_status ra_ring_attention_packed_bwd(const uint16_t *q, const uint16_t *k, con
  *   q [b, Lq, h, d] bf16; k, v [b, Lk, n_kv, d] bf16; q_pos [Lq], k_pos [Lk]
  *   int32 (needed when causal: key visible iff k_pos <= q_pos);
  *   out [b, Lq, h, d] float; lse [b, h, Lq] float (overwritten).
- *   n_splits: 0 picks enough splits to fill the GPU; at most 64.
+ *   n_splits: 0 picks enough splits to fill the GPU; at most 64.  Under the
+ *   causal rule a split covers at most 8,388,608 keys (RA_ERR_UNSUPPORTED
+ *   when n_splits leaves more; 0 picks enough).
  *   workspace: device memory of ra_prefill_workspace_size() bytes (same
  *   n_splits), 16-byte aligned, scratch after the call.
  * Launches three kernels on `stream`; RA_ERR_WORKSPACE if the workspace is

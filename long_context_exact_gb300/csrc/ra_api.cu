@@ -220,7 +220,7 @@ ra_status launch_attention(const FwdParams &p, int d, const void *q, const void 
 // Key splits for a chunked prefill: n_splits if given (capped by the key
 // tiles and kMaxSplits), else enough splits for about eight waves of CTAs
 // (so the last, partly filled wave costs little) with at least four key
-// tiles each.
+// tiles each, and at most kBlockKeyTiles tiles each.
 constexpr int kMaxSplits = 64;
 
 int resolve_splits(int64_t Lq, int64_t Lk, int n_splits, const ra_dims &dims) {
@@ -233,6 +233,7 @@ int resolve_splits(int64_t Lq, int64_t Lk, int n_splits, const ra_dims &dims) {
     const long long want = (8LL * sm_count() + units - 1) / units;
     s = static_cast<int>(want < 1 ? 1 : (want > kMaxSplits ? kMaxSplits : want));
     s = std::min(s, std::max(1, (n_ktiles + 3) / 4));
+    s = std::max(s, (n_ktiles + kBlockKeyTiles - 1) / kBlockKeyTiles);
   }
   s = std::min(std::min(s, kMaxSplits), std::max(1, n_ktiles));
   // splits of equal whole tiles: the last may be shorter, none empty
@@ -283,6 +284,9 @@ ra_status ra_block_step(const uint16_t *q, const uint16_t *k, const uint16_t *v,
   RA_CHECK_PTR(o);
   if (causal) {
     if (!q_pos || !k_pos) return fail(RA_ERR_INVALID_ARG, "causal block step needs q_pos and k_pos");
+    if ((Lk + kTile - 1) / kTile > kBlockKeyTiles)
+      return fail(RA_ERR_UNSUPPORTED, "a causal block step takes at most %lld keys (Lk=%lld)",
+                  static_cast<long long>(kBlockKeyTiles) * kTile, (long long)Lk);
   }
   float sc = 0.f;
   if ((st = resolve_scale(scale, dims.d, &sc)) != RA_OK) return st;
@@ -372,6 +376,15 @@ ra_status ra_chunked_prefill(const uint16_t *q, const uint16_t *k, const uint16_
   }
   if (causal && (!q_pos || (Lk > 0 && !k_pos)))
     return fail(RA_ERR_INVALID_ARG, "causal prefill needs q_pos and k_pos");
+  if (causal && Lk > 0) {
+    const int splits = resolve_splits(Lq, Lk, n_splits, dims);
+    const long long n_ktiles = (Lk + kTile - 1) / kTile;
+    if ((n_ktiles + splits - 1) / splits > kBlockKeyTiles)
+      return fail(RA_ERR_UNSUPPORTED,
+                  "a causal key split covers at most %lld keys: %lld keys need more than %d "
+                  "splits",
+                  static_cast<long long>(kBlockKeyTiles) * kTile, (long long)Lk, splits);
+  }
   float sc = 0.f;
   if ((st = resolve_scale(scale, dims.d, &sc)) != RA_OK) return st;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);

@@ -47,10 +47,8 @@ namespace ra {
 namespace {
 
 constexpr float kRescaleThreshold = 8.0f;
-// block mode, causal: the per-CTA classification covers up to this many key
-// tiles (2 KB of bits); longer key ranges are classified 32 tiles at a time
-constexpr int kBitTiles = 8192;
-constexpr int kBitWords = kBitTiles / 32;
+// block mode, causal: words of the CTA's keep bits (then as many mask bits)
+constexpr int kBitWords = kBlockKeyTiles / 32;
 constexpr unsigned int kFull = 0xffffffffu;
 
 template <int D, int NQ>
@@ -75,11 +73,12 @@ struct FwdCfg {
   static constexpr int bDrain = bODone + NQ;
   static constexpr int kNumBars = bDrain + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
-  // block mode, causal: keep / mask bits of up to kMaxBitTiles key tiles of
-  // the CTA's key range, classified once by the whole CTA
+  // block mode, causal: keep / mask bits of the CTA's key tiles (16 KB),
+  // classified once by the whole CTA
   static constexpr int kBitsOff = kMiscOff + 16;
   static constexpr int kSmemBytes = kBitsOff + 2 * kBitWords * 4;
   static constexpr int kSmemAlloc = kSmemBytes + 1024;
+  static_assert(kSmemAlloc <= 232448, "shared memory layout too large");
   static constexpr int kSoftmaxWarps = 4 * NQ;
   static constexpr int kProducerWarp = kSoftmaxWarps;
   static constexpr int kMmaWarp = kSoftmaxWarps + 1;
@@ -114,8 +113,7 @@ struct Unit {
   // in [flo, fhi] are seen by every row; minvis = fewest keys any row sees
   int wlo, whi, flo, fhi, minvis;
   // block mode, causal: the CTA's keep bits (kBitWords words) and then its
-  // mask bits in shared memory, or null when its range is classified by
-  // windows as it goes
+  // mask bits in shared memory
   const uint32_t *kbits;
 };
 
@@ -199,11 +197,7 @@ __device__ __forceinline__ void unit_qrange(const FwdParams &p, Unit &x) {
 
 struct KvIter {
   int s = -1, j = 0, c = 0, c_end = 0, c_fbeg = 0, c_full = 0;
-  // block mode: a window of 32 key tiles starting at `win`, with bit t of
-  // `keep` set when tile win + t holds a key some query of the unit sees,
-  // and of `part` when that tile needs the element mask
-  int win = -2;  // -2: not started
-  uint32_t keep = 0, part = 0;
+  bool started = false;  // block mode: c set to the split's first tile
 };
 
 // Next key/value tile of the unit in ring order.  Returns false at the end.
@@ -253,9 +247,9 @@ __device__ __forceinline__ bool kv_next(const FwdParams &p, const Unit &x, KvIte
     ++it.c;
     return true;
   } else {
-    if (it.win == -2) {  // first call: start at the split's first tile
+    if (!it.started) {  // first call: start at the split's first tile
       it.c = x.kc0;
-      it.win = -1;
+      it.started = true;
     }
     if (!p.causal) {
       if (it.c >= x.kc1) return false;
@@ -264,9 +258,9 @@ __device__ __forceinline__ bool kv_next(const FwdParams &p, const Unit &x, KvIte
       partial = c >= n_complete;
       return true;
     }
-    if (x.kbits != nullptr) {
+    {
       // classified once per CTA: bit t for tile kc0 + t
-      const int nt = x.kc1 - x.kc0;
+      const int nt = min(x.kc1 - x.kc0, kBlockKeyTiles);
       int t = it.c - x.kc0;
       while (t < nt) {
         const uint32_t w = x.kbits[t >> 5] >> (t & 31);
@@ -283,58 +277,6 @@ __device__ __forceinline__ bool kv_next(const FwdParams &p, const Unit &x, KvIte
       c = x.kc0 + t;
       j = 0;
       partial = (x.kbits[kBitWords + (t >> 5)] >> (t & 31)) & 1u;
-      it.c = c + 1;
-      return true;
-    }
-    const int lane = threadIdx.x & 31;
-    while (true) {
-      if (it.win < 0 || it.c >= it.win + 32) {
-        if (it.c >= x.kc1) return false;
-        // Classify the next 32 key tiles from their positions' min and max:
-        // eight tiles at a time, every lane loading four positions of each
-        // (coalesced), then one warp reduction per tile.
-        it.win = it.c;
-        it.keep = 0;
-        it.part = 0;
-#pragma unroll 1
-        for (int sb = 0; sb < 4; ++sb) {
-          int lo[8], hi[8];
-#pragma unroll
-          for (int t = 0; t < 8; ++t) {
-            lo[t] = INT_MAX;
-            hi[t] = INT_MIN;
-            const int tile = it.win + sb * 8 + t;
-#pragma unroll
-            for (int e = 0; e < kTile / 32; ++e) {
-              const int kr = tile * kTile + e * 32 + lane;
-              if (tile < x.kc1 && kr < p.Lk) {
-                const int v = p.k_pos[kr];
-                lo[t] = min(lo[t], v);
-                hi[t] = max(hi[t], v);
-              }
-            }
-          }
-#pragma unroll
-          for (int t = 0; t < 8; ++t) {
-            lo[t] = warp_min(lo[t]);
-            hi[t] = warp_max(hi[t]);
-            const int tile = it.win + sb * 8 + t;
-            if (tile < x.kc1 && lo[t] <= x.qmax) {  // else every key follows every query
-              it.keep |= 1u << (sb * 8 + t);
-              if (tile >= n_complete || hi[t] > x.qmin) it.part |= 1u << (sb * 8 + t);
-            }
-          }
-        }
-      }
-      const uint32_t rem = it.keep & (~0u << (it.c - it.win));
-      if (rem == 0) {
-        it.c = it.win + 32;
-        continue;
-      }
-      const int t = __ffs(rem) - 1;
-      c = it.win + t;
-      j = 0;
-      partial = (it.part >> t) & 1u;
       it.c = c + 1;
       return true;
     }
@@ -452,8 +394,8 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::kThreads, 1)
   } else {
     const int k0 = x.kc0 * kTile, k1 = min(p.Lk, x.kc1 * kTile);
     const int nt = x.kc1 - x.kc0;
-    int *cnt = reinterpret_cast<int *>(smem + C::kMiscOff + 8);
-    if (p.causal && nt > 0 && nt <= kBitTiles) {
+    if (p.causal) {
+      int *cnt = reinterpret_cast<int *>(smem + C::kMiscOff + 8);
       // Classify the CTA's key tiles once, a warp per tile: keep a tile
       // when a key precedes the unit's last query, mask it when a key
       // follows the first query (or the tile is ragged); count on the way
@@ -463,7 +405,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::kThreads, 1)
       __syncthreads();
       const int n_complete = p.Lk / kTile;
       int mine = 0;
-      for (int t = warp; t < nt; t += blockDim.x >> 5) {
+      for (int t = warp; t < min(nt, kBlockKeyTiles); t += blockDim.x >> 5) {
         const int tile = x.kc0 + t;
         int lo = INT_MAX, hi = INT_MIN;
 #pragma unroll
@@ -489,19 +431,8 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::kThreads, 1)
       __syncthreads();
       split = k1 - k0 < kSplitKeys || *cnt < kSplitKeys;
       x.kbits = bits;
-    } else if (k1 - k0 < kSplitKeys) {
-      split = true;
-    } else if (!p.causal) {
-      split = false;
     } else {
-      int mine = 0;
-      for (int kk = k0 + static_cast<int>(threadIdx.x); kk < k1; kk += blockDim.x)
-        mine += p.k_pos[kk] <= x.qmin ? 1 : 0;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) mine += __shfl_xor_sync(kFull, mine, o);
-      if (lane == 0) atomicAdd(cnt, mine);
-      __syncthreads();
-      split = *cnt < kSplitKeys;
+      split = k1 - k0 < kSplitKeys;  // without the causal rule every row sees the range
     }
   }
 

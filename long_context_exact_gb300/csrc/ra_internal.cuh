@@ -22,6 +22,11 @@ constexpr float kLn2 = 0.6931471805599453f;
 // Longer rows spread the weights and keep plain bf16.
 constexpr int kSplitKeys = 4096;
 
+// Causal block steps: one CTA classifies its whole key range once (keep and
+// mask bits in shared memory), so a range holds at most this many key tiles
+// (8,388,608 keys); the host refuses longer causal ranges.
+constexpr int kBlockKeyTiles = 65536;
+
 // ------------------------------------------------------------ placement
 // Token held at local row r of shard p.  Contiguous: shard p holds
 // [p*L, (p+1)*L).  Striped: token t lives on shard t mod N at row t div N

@@ -224,3 +224,24 @@ def test_host_buffer_and_pipeline_validation(lib):
                                   None) == binding.RA_ERR_INVALID_ARG
     assert lib.ra_pipeline_sync(None) == binding.RA_ERR_INVALID_ARG
     assert lib.ra_pipeline_destroy(None) == binding.RA_OK
+
+
+def test_causal_block_ranges_are_bounded(lib):
+    """A causal block step classifies its whole key range in shared memory:
+    at most 65,536 key tiles (8,388,608 keys); longer ranges are refused on
+    the host, and a chunked prefill needs enough key splits."""
+    d = _dims()
+    over = 65536 * 128 + 1
+    assert lib.ra_block_step(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 128, over, d, 1,
+                             0.0, None) == binding.RA_ERR_UNSUPPORTED
+    assert b"at most 8388608 keys" in lib.ra_last_error()
+    lib.ra_prefill_workspace_size.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
+                                              binding.Dims]
+    lib.ra_prefill_workspace_size.restype = ctypes.c_size_t
+    st = lib.ra_chunked_prefill(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 128, 2 * over, 1, d, 1,
+                                0.0, FAKE, 1 << 40, None)
+    assert st == binding.RA_ERR_UNSUPPORTED
+    # the automatic split count covers long ranges
+    rows = 1 * 4 * 128
+    need = lib.ra_prefill_workspace_size(128, 2 * over, 0, d)
+    assert need >= 3 * rows * (2 + 128) * 4
