@@ -557,10 +557,10 @@ ra_status ra_ring_attention_packed_bwd(const uint16_t *q, const uint16_t *k, con
   if ((st = make_dq_map(&dkm, dk, layout, dims.b, n_shards, p.L, dims.n_kv, dims.d)) != RA_OK) return st;
   if ((st = make_dq_map(&dvm, dv, layout, dims.b, n_shards, p.L, dims.n_kv, dims.d)) != RA_OK) return st;
   // one unit per (key tile, query shard, query head); packed documents: one
-  // per key tile
+  // per (key tile, query shard), the KV head's query heads inside
   const long long n_units =
       cu_seqlens != nullptr
-          ? static_cast<long long>(dims.b) * dims.n_kv * n_shards * p.n_ktiles
+          ? static_cast<long long>(dims.b) * dims.n_kv * n_shards * n_shards * p.n_ktiles
           : static_cast<long long>(dims.b) * dims.h * n_shards * n_shards * p.n_ktiles;
   if (n_units > 0x7fffffffLL) return fail(RA_ERR_UNSUPPORTED, "too many work units (%lld)", n_units);
   cudaStream_t cs = static_cast<cudaStream_t>(stream);

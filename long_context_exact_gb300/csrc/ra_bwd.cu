@@ -9,7 +9,8 @@
 // One CTA handles one 128-key tile of one KV head against one query shard i
 // and one query head of its GQA group: K, V stay in shared memory and the
 // unit's dK, dV accumulate in tensor memory over every query tile of shard i
-// the causal rule does not mask completely.  The key/value block of the
+// the causal rule does not mask completely (packed documents: against one
+// query shard and all g heads).  The key/value block of the
 // pages carries its gradient accumulators around the ring and meets shard
 // (j + s) mod N at step s; here the N shards (and g heads) of a tile are
 // separate units whose dK, dV partials are summed into the fp32 dk, dv with
@@ -135,10 +136,11 @@ enum : unsigned int {
 
 struct KvUnit {
   int bb, kh, j, c;   // batch, kv head, kv shard, kv tile
-  int i, hq;          // unpacked: the query shard and query head it meets
+  int i, hq;          // the query shard it meets; unpacked: and the query head
   int kmin, kmax;     // token positions of the tile's first and last existing key
-  int a_lo, a_hi;     // unpacked: query tiles [a_lo, a_hi) see a key of the tile
-  int a_flo;          // unpacked: query tiles a >= a_flo see every key (no mask)
+  int a_lo, a_hi;     // query tiles [a_lo, a_hi) of shard i see a key of the tile
+  int a_flo;          // query tiles a >= a_flo see every key of the tile (no mask) ...
+  int a_fhi;          // ... and, packed, a < a_fhi (the tile's documents end later)
   int ds0, de0, ds1, de1;  // packed: documents of the first and last key
 };
 
@@ -149,10 +151,11 @@ struct KvUnit {
 // Q / dO tiles and add their dQ partials into the same 64 KB dq tiles: one
 // group's dq rows (n_qtiles x 64 KB) stay in L2 while every key tile adds
 // to them.
-// Units (packed documents): one 128-key tile against every query shard and
-// head, like the key/value block of the pages: a tile sees only the query
-// tiles of its own documents, so per-shard units would be a few steps long,
-// and the dq rows it adds into are those few tiles anyway.
+// Units (packed documents): one 128-key tile against one query shard, with
+// the g query heads of its KV head inside the unit (a tile sees only its own
+// documents' query tiles, so a unit per head would be a few steps long).
+// Units run grouped by (batch, kv head, query shard) with the key tiles
+// innermost, so the resident CTAs add into one shard's dq rows of g heads.
 template <bool kDocs>
 __device__ __forceinline__ KvUnit decode_kv_unit(const BwdParams &p, long long u) {
   KvUnit x;
@@ -169,15 +172,17 @@ __device__ __forceinline__ KvUnit decode_kv_unit(const BwdParams &p, long long u
     x.bb = static_cast<int>(g / p.n_kv);
     x.hq = x.kh * p.g + hh;
   } else {
+    x.i = static_cast<int>(g % p.N);
+    g /= p.N;
     x.kh = static_cast<int>(g % p.n_kv);
     x.bb = static_cast<int>(g / p.n_kv);
-    x.i = -1;
     x.hq = -1;
   }
   const int r0 = x.c * kTile;
   const int r1 = min(r0 + kTile, p.L) - 1;
   x.kmin = token_at(p.layout, p.L, p.N, x.j, r0);
   x.kmax = token_at(p.layout, p.L, p.N, x.j, r1);
+  x.a_fhi = p.n_qtiles;
   if constexpr (!kDocs) {
     x.a_hi = p.n_qtiles;
     if (!p.causal) {
@@ -192,18 +197,31 @@ __device__ __forceinline__ KvUnit decode_kv_unit(const BwdParams &p, long long u
       x.a_flo = min(p.n_qtiles, (r_full + kTile - 1) / kTile);
     }
   } else {
+    // A query at t sees key kp iff kp lies in t's document [ds, de) and,
+    // causal, kp <= t: iff t >= (causal ? kp : ds(kp)) and t < de(kp).
+    // Query rows of shard i are increasing positions, so the rows that see
+    // some key of the tile and those that see all of them are row ranges.
     doc_of(p.cu, p.n_docs, x.bb, p.S, x.kmin, x.ds0, x.de0);
     doc_of(p.cu, p.n_docs, x.bb, p.S, x.kmax, x.ds1, x.de1);
+    const int r_vis = max(0, first_row_at_or_after(p.layout, p.L, p.N, x.i,
+                                                   p.causal ? x.kmin : x.ds0));
+    const int r_end = min(p.L, first_row_at_or_after(p.layout, p.L, p.N, x.i, x.de1));
+    x.a_lo = r_vis / kTile;
+    x.a_hi = r_vis >= r_end ? x.a_lo : (r_end + kTile - 1) / kTile;
+    const int r_flo = max(0, first_row_at_or_after(p.layout, p.L, p.N, x.i,
+                                                   p.causal ? x.kmax : x.ds1));
+    const int r_fhi = min(p.L, first_row_at_or_after(p.layout, p.L, p.N, x.i, x.de0));
+    x.a_flo = (r_flo + kTile - 1) / kTile;
+    x.a_fhi = r_fhi >= p.L ? p.n_qtiles : r_fhi / kTile;
   }
   return x;
 }
 
 struct QIter {
   int a = INT_MAX;
-  // packed documents: shard step, query shard, its visible and unmasked tile
-  // ranges, query head, and the documents of the current tile's first and
-  // last rows
-  int s = -1, i = 0, a_lo = 0, a_flo = 0, a_fhi = 0, hh = 0;
+  // packed documents: the query shard, query head, and the documents of the
+  // current tile's first and last rows
+  int i = 0, hh = 0;
   int d0 = -1, d1 = -1;
 };
 
@@ -243,43 +261,22 @@ __device__ __forceinline__ bool q_next(const BwdParams &p, const KvUnit &x, QIte
                      : (p.S < kSplitKeys);
     return true;
   }
-  // Query shards in ring order (j + s) mod N; inside a shard the visible
-  // query tiles from the last down; then the g query heads.  A query at t
-  // sees key kp iff kp lies in t's document [ds, de) and, causal, kp <= t:
-  // iff t >= (causal ? kp : ds(kp)) and t < de(kp).  Query rows of a shard
-  // are increasing positions, so the rows that see some key of the tile and
-  // those that see all of them are row ranges.
-  bool next_shard = false;
+  // The unit's query shard: its visible query tiles from the last down, and
+  // for each the g query heads of the key tile's KV head.
   if (it.a == INT_MAX) {
-    next_shard = true;
+    it.a = x.a_hi - 1;
+    it.hh = 0;
+    it.d0 = it.d1 = -1;
   } else if (++it.hh >= p.g) {
     it.hh = 0;
-    next_shard = --it.a < it.a_lo;
+    --it.a;
   }
-  if (next_shard) {
-    for (;;) {
-      if (++it.s >= p.N) return false;
-      it.i = (x.j + it.s) % p.N;
-      const int r_vis = max(0, first_row_at_or_after(p.layout, p.L, p.N, it.i,
-                                                     p.causal ? x.kmin : x.ds0));
-      const int r_end = min(p.L, first_row_at_or_after(p.layout, p.L, p.N, it.i, x.de1));
-      if (r_vis >= r_end) continue;
-      const int r_flo = max(0, first_row_at_or_after(p.layout, p.L, p.N, it.i,
-                                                     p.causal ? x.kmax : x.ds1));
-      const int r_fhi = min(p.L, first_row_at_or_after(p.layout, p.L, p.N, it.i, x.de0));
-      it.a_lo = r_vis / kTile;
-      it.a = (r_end + kTile - 1) / kTile - 1;
-      it.a_flo = (r_flo + kTile - 1) / kTile;
-      it.a_fhi = r_fhi >= p.L ? p.n_qtiles : r_fhi / kTile;
-      it.hh = 0;
-      it.d0 = it.d1 = -1;
-      break;
-    }
-  }
+  if (it.a < x.a_lo) return false;
+  it.i = x.i;
   i = it.i;
   a = it.a;
   hq = x.kh * p.g + it.hh;
-  partial = it.a < it.a_flo || it.a >= it.a_fhi;
+  partial = it.a < x.a_flo || it.a >= x.a_fhi;
   const int t0 = token_at(p.layout, p.L, p.N, it.i, it.a * kTile);
   int minvis;
   {
@@ -373,9 +370,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                const __grid_constant__ CUtensorMap dvmap) {
   using C = BwdCfg<D>;
   const KvUnit x = decode_kv_unit<kDocs>(p, blockIdx.x);
-  if constexpr (!kDocs) {
-    if (x.a_lo >= x.a_hi) return;  // no query of this shard sees the tile: nothing to add
-  }
+  if (x.a_lo >= x.a_hi) return;  // no query of this shard sees the tile: nothing to add
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   if (pad > static_cast<uint32_t>(C::kSlack)) {  // uniform: never touch smem beyond the allocation
