@@ -246,6 +246,68 @@ def _time_ms(fn, reps=2):
     return best
 
 
+def ring_imbalance(b, S, h, d, N, q, k, v, dev):
+    """One ra_block_step per (query shard i, ring step s), timed with CUDA
+    events, t(i, s); the makespan an N-device ring would see,
+    T = sum_s max_i t(i, s), and its utilisation sum t / (N T), for the
+    contiguous, striped and zig-zag placements."""
+    import torch
+
+    from long_context_exact_gb300 import binding as ra
+    from long_context_exact_gb300.inputs import CONTIGUOUS, STRIPED, ZIGZAG
+
+    rep = {}
+    L = S // N
+    for name, layout in (("contiguous", CONTIGUOUS), ("striped", STRIPED), ("zigzag", ZIGZAG)):
+        _, _, tok = ra.position_map(layout, S, N, device=dev)
+        t = [[0.0] * N for _ in range(N)]
+        for i in range(N):
+            qi = q.index_select(1, tok[i].long()).contiguous()
+            st = ra.new_state(b, L, h, d, dev)
+            for s_ in range(N):
+                j = (i - s_) % N
+                kj = k.index_select(1, tok[j].long()).contiguous()
+                vj = v.index_select(1, tok[j].long()).contiguous()
+                torch.cuda.synchronize()
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record()
+                ra.block_step(qi, kj, vj, st, tok[i], tok[j], True)
+                e1.record()
+                torch.cuda.synchronize()
+                t[i][s_] = e0.elapsed_time(e1)
+                del kj, vj
+            del qi, st
+        total = sum(sum(r) for r in t)
+        makespan = sum(max(t[i][s_] for i in range(N)) for s_ in range(N))
+        rep["ring_" + name] = {
+            "sum_ms": total, "makespan_ms": makespan, "utilisation": total / (N * makespan),
+            "per_shard_ms": [sum(t[i]) for i in range(N)]}
+    ra.stream_check()
+    return rep
+
+
+def imbalance_at(name, dev):
+    """The ring imbalance picture at another workload's shape (its own
+    seeded device inputs)."""
+    import torch
+
+    from long_context_exact_gb300.inputs import WORKLOADS
+
+    w = WORKLOADS[name]
+    gen = torch.Generator(device=dev).manual_seed(w.seed)
+
+    def rnd(*shape):
+        x = torch.randn(shape, generator=gen, device=dev, dtype=torch.float32)
+        return x.mul_(w.amplitude).to(torch.bfloat16)
+
+    q, k, v = rnd(w.b, w.S, w.h, w.d), rnd(w.b, w.S, w.n_kv, w.d), rnd(w.b, w.S, w.n_kv, w.d)
+    rep = ring_imbalance(w.b, w.S, w.h, w.d, w.n_shards, q, k, v, dev)
+    rep["workload"] = w.name
+    return {k_: ({kk: vv for kk, vv in v_.items() if kk != "per_shard_ms"}
+                 if isinstance(v_, dict) else v_) for k_, v_ in rep.items()}
+
+
 def layout_and_imbalance_report(w, q, k, v, dev):
     """Forward of the same shape non-causal, with contiguous shards and with
     zig-zag shards, and the causal load-balance picture of the third page's
@@ -275,33 +337,8 @@ def layout_and_imbalance_report(w, q, k, v, dev):
     rep["striped_causal_vs_noncausal_per_useful_flop"] = (
         rep["causal_striped_fwd_tflops"] / rep["noncausal_fwd_tflops"])
     del out, lse
-    # per-(shard, step) block steps
-    N, L = w.n_shards, w.S // w.n_shards
-    for name, layout in (("contiguous", CONTIGUOUS), ("striped", STRIPED), ("zigzag", ZIGZAG)):
-        _, _, tok = ra.position_map(layout, w.S, N, device=dev)
-        t = [[0.0] * N for _ in range(N)]
-        for i in range(N):
-            qi = q.index_select(1, tok[i].long()).contiguous()
-            st = ra.new_state(w.b, L, w.h, w.d, dev)
-            for s_ in range(N):
-                j = (i - s_) % N
-                kj = k.index_select(1, tok[j].long()).contiguous()
-                vj = v.index_select(1, tok[j].long()).contiguous()
-                torch.cuda.synchronize()
-                e0 = torch.cuda.Event(enable_timing=True)
-                e1 = torch.cuda.Event(enable_timing=True)
-                e0.record()
-                ra.block_step(qi, kj, vj, st, tok[i], tok[j], True)
-                e1.record()
-                torch.cuda.synchronize()
-                t[i][s_] = e0.elapsed_time(e1)
-                del kj, vj
-            del qi, st
-        total = sum(sum(r) for r in t)
-        makespan = sum(max(t[i][s_] for i in range(N)) for s_ in range(N))
-        rep["ring_" + name] = {
-            "sum_ms": total, "makespan_ms": makespan, "utilisation": total / (N * makespan),
-            "per_shard_ms": [sum(t[i]) for i in range(N)]}
+    N = w.n_shards
+    rep.update(ring_imbalance(w.b, w.S, w.h, w.d, N, q, k, v, dev))
     rep["model_utilisation_contiguous"] = {
         "(N+1)/2N": accounting.causal_utilisation_contiguous(N),
         "N/(2N-1)": accounting.causal_utilisation_contiguous(N, half_diagonal=True)}
@@ -589,6 +626,8 @@ def run_ours(a, rank, world, local_rank):
     extras = None
     if rank == 0 and not a.no_extras:
         extras = layout_and_imbalance_report(w, q, k, v, dev)
+        if w.S != 65536:
+            extras["imbalance_causal64k"] = imbalance_at("causal64k", dev)
         extras["exp2_roof"] = exp2_roof_report(w, dev, clk)
         extras["hbm_kernels"] = hbm_kernel_report(w, dev, peaks)
         extras["chunked_prefill"] = prefill_report(w, q, k, v, dev)
