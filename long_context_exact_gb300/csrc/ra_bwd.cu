@@ -33,8 +33,8 @@
 //              steps); dS^T = P^T (dP^T - D) to shared memory (its residual to
 //              the staging buffer, on split steps)
 //   warps 8-11 dQ drain: TMEM -> registers -> staging buffer -> TMA bulk
-//              reduce-add into dq, 32 rows per warp (d = 128; vector
-//              reductions for d = 64); then the dK / dV epilogue
+//              reduce-add into dq, 32 rows per warp; then the dK / dV
+//              epilogue the same way
 //   warp 12    TMA producer: K, V once; Q tiles (with their rows' LSE2 and
 //              D) into a 2-deep ring, dO tiles into one buffer
 //   warp 13    TMEM allocator and MMA issuer (lane 0)
@@ -117,11 +117,11 @@ struct BwdCfg {
   static constexpr uint32_t kColS = 0, kColDp = 128, kColDv = 256, kColDk = 384;
   static constexpr uint32_t kIdescKK = idesc_bf16_f32(128, 128, false, false);  // S^T, dP^T
   static constexpr uint32_t kIdescDv = idesc_bf16_f32(128, D, false, true);     // dV
-  // D = 128: each drain warp adds its 32 rows of the dQ tile into dq with TMA
-  // bulk reductions from its 8 KB of the staging buffer, 32 columns x 32 rows
-  // per box (128-byte swizzled), two boxes per round, two rounds.
-  // D = 64: vector reductions from registers.
-  static constexpr bool kDqTma = D == 128;
+  // Each drain warp adds its 32 rows of the dQ tile into dq with TMA bulk
+  // reductions from its 8 KB of the staging buffer, 32 columns x 32 rows per
+  // box (128-byte swizzled), two boxes per round, D / 64 rounds; the unit's
+  // dK and dV leave the same way.
+  static constexpr int kDqRounds = D / 64;
   static constexpr int kDqBoxBytes = 32 * 32 * 4;
   static constexpr int kDqWarpStgBytes = 2 * kDqBoxBytes;
 };
@@ -673,7 +673,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       bool go = mbar_wait(&bars[C::bDpFull], n & 1, abort_flag, kSiteBSmDp);
       if (go) go = mbar_wait(&bars[C::bDsEmpty], (n & 1) ^ 1, abort_flag, kSiteBSmDs);
       // the residual goes to the staging buffer once the drain is done with it
-      if (C::kDqTma && go && split && n > 0)
+      if (go && split && n > 0)
         go = mbar_wait(&bars[C::bStgEmpty], (n - 1) & 1, abort_flag, kSiteBSmStg);
       if (!__all_sync(kFull, go)) break;
       tc_fence_after();
@@ -730,7 +730,6 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
   } else if (warp < C::kDrainWarp0 + 4) {
     regs_set<C::kDrainRegs, C::kLaunchRegs>();
     // ------------------------------------------------------------ dQ drain, then dK/dV
-    const int row = (warp & 3) * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tDq = tmem + lane_off + C::kColDp;
     uint8_t *stg = smem + C::kStgOff + (warp & 3) * C::kDqWarpStgBytes;  // this warp's 32 rows
@@ -744,24 +743,26 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         break;
       }
       tc_fence_after();
-      if constexpr (C::kDqTma) {
-        // Two rounds of two 32 x 32 boxes through this warp's staging slice;
+      {
+        // D / 64 rounds of two 32 x 32 boxes through this warp's staging slice;
         // the staging buffer is free: this step's dS_lo^T readers finished
         // before dQ was committed, and the previous round's read completed.
         int c2, c3;
         map_coords(p.layout, p.L, p.N, i, a * kTile + (warp & 3) * 32, c2, c3);
 #pragma unroll
-        for (int round = 0; round < 2; ++round) {
+        for (int round = 0; round < C::kDqRounds; ++round) {
           uint32_t r[2][32];
           tmem_ld32_start(tDq + round * 64, r[0]);
           tmem_ld32_start(tDq + round * 64 + 32, r[1]);
           tmem_ld_wait_regs(r[0]);
           tmem_ld_wait_regs(r[1]);
-          if (round == 1) {  // every dQ column is in registers: TMEM free for dP
+          if (round == C::kDqRounds - 1) {  // every dQ column is in registers: TMEM free for dP
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars[C::bDqEmpty]);
-            if (lane == 0) bulk_wait_group0<true>();  // round 0's staging read
+          }
+          if (round > 0) {
+            if (lane == 0) bulk_wait_group0<true>();  // the previous round's staging read
             __syncwarp();
           }
 #pragma unroll
@@ -786,56 +787,32 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
           }
         }
         if (lane == 0) {
-          bulk_wait_group0<true>();  // round 1's staging read: slice reusable
+          bulk_wait_group0<true>();  // the last round's staging read: slice reusable
           mbar_arrive(&bars[C::bStgEmpty]);
         }
         __syncwarp();
-      } else {
-        uint32_t r[D / 32][32];
-#pragma unroll
-        for (int ch = 0; ch < D / 32; ++ch) tmem_ld32(tDq + ch * 32, r[ch]);
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars[C::bDqEmpty]);
-        const int qr = a * kTile + row;
-        if (qr < p.L) {
-          float *dst = p.dq + ((static_cast<size_t>(x.bb) * p.S + token_at(p.layout, p.L, p.N, i, qr)) *
-                                   p.h + hq) * D;
-#pragma unroll
-          for (int ch = 0; ch < D / 32; ++ch)
-#pragma unroll
-            for (int u = 0; u < 8; ++u)
-              asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(
-                               dst + ch * 32 + u * 4),
-                           "f"(__uint_as_float(r[ch][u * 4 + 0]) * p.scale),
-                           "f"(__uint_as_float(r[ch][u * 4 + 1]) * p.scale),
-                           "f"(__uint_as_float(r[ch][u * 4 + 2]) * p.scale),
-                           "f"(__uint_as_float(r[ch][u * 4 + 3]) * p.scale)
-                           : "memory");
-        }
       }
       ++n;
     }
-    if constexpr (C::kDqTma) {
-      if (lane == 0) bulk_wait_group0<false>();  // this warp's reductions complete
-    }
+    if (lane == 0) bulk_wait_group0<false>();  // this warp's reductions complete
     // dK, dV of this unit, added into dk and dv (other units of the tile add
-    // theirs): through this warp's staging slice with bulk reductions for
-    // d = 128, vector reductions for d = 64.
+    // theirs) through this warp's staging slice with bulk reductions.
     bool have = n > 0 && !aborted;
     if (have) have = mbar_wait(&bars[C::bDone], 0, abort_flag, kSiteBDone);
     have = __all_sync(kFull, have && *abort_flag == 0);
     if (have) {
       tc_fence_after();
       const int r0 = x.c * kTile + (warp & 3) * 32;  // this warp's first key row
-      if constexpr (C::kDqTma) {
+      {
         uint8_t *stg = smem + C::kStgOff + (warp & 3) * C::kDqWarpStgBytes;
         int c2, c3;
         map_coords(p.layout, p.L, p.N, x.j, r0, c2, c3);
 #pragma unroll
-        for (int round = 0; round < 4; ++round) {  // dK cols 0-63, 64-127, then dV
-          const uint32_t col = (round < 2 ? C::kColDk : C::kColDv) + (round & 1) * 64;
-          const float mul = round < 2 ? p.scale : 1.f;
+        for (int round = 0; round < 2 * C::kDqRounds; ++round) {  // dK, then dV, 64 columns a round
+          const bool is_dk = round < C::kDqRounds;
+          const int part = round % C::kDqRounds;
+          const uint32_t col = (is_dk ? C::kColDk : C::kColDv) + part * 64;
+          const float mul = is_dk ? p.scale : 1.f;
           uint32_t r[2][32];
           tmem_ld32_start(tmem + lane_off + col, r[0]);
           tmem_ld32_start(tmem + lane_off + col + 32, r[1]);
@@ -859,39 +836,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
           if (lane == 0 && r0 < p.L) {
 #pragma unroll
             for (int bx = 0; bx < 2; ++bx)
-              tma_reduce_add_5d(round < 2 ? &dkmap : &dvmap, stg + bx * C::kDqBoxBytes,
-                                (round & 1) * 64 + bx * 32, x.kh, c2, c3, x.bb);
+              tma_reduce_add_5d(is_dk ? &dkmap : &dvmap, stg + bx * C::kDqBoxBytes,
+                                part * 64 + bx * 32, x.kh, c2, c3, x.bb);
             bulk_commit_group();
           }
         }
         if (lane == 0) bulk_wait_group0<false>();
-      } else {
-        const int kr = x.c * kTile + row;
-        const size_t off =
-            ((static_cast<size_t>(x.bb) * p.S +
-              token_at(p.layout, p.L, p.N, x.j, kr < p.L ? kr : 0)) * p.n_kv + x.kh) * D;
-#pragma unroll
-        for (int which = 0; which < 2; ++which) {
-          const uint32_t col = which == 0 ? C::kColDk : C::kColDv;
-          float *dst = (which == 0 ? p.dk : p.dv) + off;
-          const float mul = which == 0 ? p.scale : 1.f;
-#pragma unroll
-          for (int ch = 0; ch < D / 32; ++ch) {
-            uint32_t r[32];
-            tmem_ld32(tmem + lane_off + col + ch * 32, r);
-            if (kr < p.L) {
-#pragma unroll
-              for (int u = 0; u < 8; ++u)
-                asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(
-                                 dst + ch * 32 + u * 4),
-                             "f"(__uint_as_float(r[u * 4 + 0]) * mul),
-                             "f"(__uint_as_float(r[u * 4 + 1]) * mul),
-                             "f"(__uint_as_float(r[u * 4 + 2]) * mul),
-                             "f"(__uint_as_float(r[u * 4 + 3]) * mul)
-                             : "memory");
-            }
-          }
-        }
       }
     }
   }
