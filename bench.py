@@ -36,7 +36,7 @@ WORKLOAD = "causal256k"
 # (dram__bytes_read.sum + dram__bytes_write.sum, one pass, this workload),
 # valid only while the kernel source hashes match (see profiles/).
 TRAFFIC = {
-    "bwd": {"bytes_per_launch": 119090004992 + 81380603648, "src_sha": "00021c67057064df",
+    "bwd": {"bytes_per_launch": 118850519552 + 81280138496, "src_sha": "190094a2c1db44a2",
             "profile": "profiles/traffic_bwd_causal256k.md"},
 }
 
