@@ -425,21 +425,32 @@ class Pipeline:
                                       ctypes.byref(handle)))
         self._h = handle.value
         self.backward = backward
+        rows = b * S
+        # bytes each host buffer must hold: inputs bf16, results fp32
+        self._need = {"q": rows * h * d * 2, "k": rows * n_kv * d * 2, "v": rows * n_kv * d * 2,
+                      "dout": rows * h * d * 2, "out": rows * h * d * 4, "lse": rows * h * 4,
+                      "dq": rows * h * d * 4, "dk": rows * n_kv * d * 4, "dv": rows * n_kv * d * 4}
 
-    @staticmethod
-    def _hp(x):
+    def _hp(self, name, x):
         if x is None:
             return None
         if isinstance(x, HostBuffer):
-            return ctypes.c_void_p(x.data_ptr())
-        if x.is_cuda or not x.is_contiguous():
-            raise RAError(RA_ERR_INVALID_ARG, "pipeline buffers are contiguous host tensors")
-        return ctypes.c_void_p(x.data_ptr())
+            nbytes, ptr = x.nbytes, x.data_ptr()
+        else:
+            if x.is_cuda or not x.is_contiguous():
+                raise RAError(RA_ERR_INVALID_ARG, "pipeline buffers are contiguous host tensors")
+            nbytes, ptr = x.numel() * x.element_size(), x.data_ptr()
+        if nbytes < self._need[name]:
+            raise RAError(RA_ERR_INVALID_ARG,
+                          f"{name}: {nbytes} bytes given, {self._need[name]} needed")
+        return ctypes.c_void_p(ptr)
 
     def submit(self, q, k, v, dout=None, out=None, lse=None, dq=None, dk=None, dv=None):
         hp = self._hp
-        _check(load().ra_pipeline_submit(ctypes.c_void_p(self._h), hp(q), hp(k), hp(v), hp(dout),
-                                         hp(out), hp(lse), hp(dq), hp(dk), hp(dv)))
+        _check(load().ra_pipeline_submit(ctypes.c_void_p(self._h), hp("q", q), hp("k", k),
+                                         hp("v", v), hp("dout", dout), hp("out", out),
+                                         hp("lse", lse), hp("dq", dq), hp("dk", dk),
+                                         hp("dv", dv)))
 
     def sync(self):
         _check(load().ra_pipeline_sync(ctypes.c_void_p(self._h)))

@@ -112,3 +112,18 @@ def test_host_alloc_round_trip():
     assert ra.host_numa_node() >= -1
     hb.free()
     assert ra.HostBuffer((0,), torch.float32).nbytes == 0
+
+
+def test_pipeline_refuses_short_host_buffers():
+    b, S, h, n_kv, d, N = 1, 512, 4, 2, 64, 2
+    q, k, v, do = make_inputs(b, S, h, n_kv, d, seed=3, with_dout=True)
+    pl = ra.Pipeline(S, N, STRIPED, True, b, h, n_kv, d, backward=True)
+    try:
+        with pytest.raises(ra.RAError) as ei:
+            pl.submit(q[:, : S // 2].contiguous(), k, v, do)
+        assert ei.value.status == ra.RA_ERR_INVALID_ARG
+        out = torch.empty((b, S, h, d // 2))
+        with pytest.raises(ra.RAError):
+            pl.submit(q, k, v, do, out=out)
+    finally:
+        pl.close()
