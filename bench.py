@@ -625,14 +625,22 @@ def run_ours(a, rank, world, local_rank):
 
     extras = None
     if rank == 0 and not a.no_extras:
-        extras = layout_and_imbalance_report(w, q, k, v, dev)
+        # Side measurements: one that fails records its error instead of the
+        # whole line going missing.
+        def extra(fn, *args):
+            try:
+                return fn(*args)
+            except Exception as exc:  # noqa: BLE001 - reported in the JSON line
+                return {"error": f"{type(exc).__name__}: {exc}"[:300]}
+
+        extras = extra(layout_and_imbalance_report, w, q, k, v, dev)
         if w.S != 65536:
-            extras["imbalance_causal64k"] = imbalance_at("causal64k", dev)
-        extras["exp2_roof"] = exp2_roof_report(w, dev, clk)
-        extras["hbm_kernels"] = hbm_kernel_report(w, dev, peaks)
-        extras["chunked_prefill"] = prefill_report(w, q, k, v, dev)
+            extras["imbalance_causal64k"] = extra(imbalance_at, "causal64k", dev)
+        extras["exp2_roof"] = extra(exp2_roof_report, w, dev, clk)
+        extras["hbm_kernels"] = extra(hbm_kernel_report, w, dev, peaks)
+        extras["chunked_prefill"] = extra(prefill_report, w, q, k, v, dev)
         if have_bwd:
-            extras["packed_documents"] = packed_report(w, q, k, v, do, layout, dev)
+            extras["packed_documents"] = extra(packed_report, w, q, k, v, do, layout, dev)
 
     cpu = None
     if rank == 0 and world == 1 and not a.no_cpu_baseline:
