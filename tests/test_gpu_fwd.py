@@ -359,3 +359,20 @@ def test_workload_causal_64k_zigzag(orc):
 
 def test_workload_causal_256k_striped(orc):
     _workload_parity(orc, "causal256k")
+
+
+def test_launch_counter_and_exp2_probe():
+    """The library's launch counter sees each kernel it starts (the forward
+    is one launch; the backward a pre-pass and the main kernel), and the
+    exp2-rate probe runs and writes finite values."""
+    q, k, v, do = _dev(*make_inputs(1, 512, 4, 2, 128, seed=9, with_dout=True))
+    n0 = ra.launch_count()
+    out, lse = ra.ring_attention(q, k, v, 2, STRIPED, True)
+    n1 = ra.launch_count()
+    ra.ring_attention_bwd(q, k, v, out, lse, do, 2, STRIPED, True)
+    n2 = ra.launch_count()
+    ra.stream_check()
+    assert n1 - n0 == 1 and n2 - n1 == 2
+    sink, evaluated = ra.ex2_probe(4)
+    ra.stream_check()
+    assert evaluated == 32 * sink.numel() and bool(torch.isfinite(sink).all())
