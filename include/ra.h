@@ -115,7 +115,8 @@ ra_status ra_block_step(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                         int64_t Lq, int64_t Lk, ra_dims dims, int causal, float scale,
                         void *stream);
 
-/* Final division ("... recovered by dividing by the accumulated normalizer"):
+/* Finalize ("Blockwise Attention and Online Softmax Formulations": the
+ * output is the unnormalised O divided by the row sum l):
  * o <- o / l in place, lse = m + ln(l).  Rows with l == 0 get o = 0 and
  * lse = -inf.  o [b, Lq, h, d]; l, m, lse [b, h, Lq]. */
 ra_status ra_finalize(float *o, const float *l, const float *m, float *lse, int64_t Lq,
