@@ -33,11 +33,10 @@ METRIC = "useful attention TFLOP/s fwd & bwd (causal, S=256K GQA) and % of BF16 
 WORKLOAD = "causal256k"
 
 # Per-launch DRAM traffic of the dominant kernels from one ncu capture
-# (dram__bytes_read.sum + dram__bytes_write.sum, one pass, this workload),
-# valid only while the kernel source hashes match (see profiles/).
+# (dram__bytes_read.sum + dram__bytes_write.sum), valid only while the
+# kernel source hash matches the one the capture was taken with.
 TRAFFIC = {
-    "bwd": {"bytes_per_launch": 118850519552 + 81280138496, "src_sha": "190094a2c1db44a2",
-            "profile": "profiles/traffic_bwd_causal256k.md"},
+    "bwd": {"bytes_per_launch": 118850519552 + 81280138496, "src_sha": "190094a2c1db44a2"},
 }
 
 

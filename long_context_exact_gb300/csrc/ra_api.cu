@@ -253,6 +253,10 @@ ra_status report_error(ra_status st, const char *fmt, ...) {
   return st;
 }
 
+const char *last_error_text() { return g_last_error.c_str(); }
+
+void restore_last_error(const char *text) { g_last_error = text; }
+
 }  // namespace ra
 
 using namespace ra;

@@ -216,6 +216,10 @@ cudaError_t launch_ex2_probe(long long iters, float *sink, int blocks, int threa
                              cudaStream_t stream);
 // Record a message for ra_last_error() on this thread and return `st`.
 ra_status report_error(ra_status st, const char *fmt, ...) __attribute__((format(printf, 2, 3)));
+// The calling thread's last error message, and a way to put back a saved one
+// (for a call that runs another entry point only to validate its arguments).
+const char *last_error_text();
+void restore_last_error(const char *text);
 
 // Read-and-clear of each translation unit's device error word.
 cudaError_t read_error_word_fwd(unsigned int *word);

@@ -14,6 +14,7 @@
 // a stand-in for the symbol: host code must ask the runtime for the device
 // address (cudaGetSymbolAddress) with the device current, once per device.
 #include <mutex>
+#include <string>
 
 #include "ra_internal.cuh"
 
@@ -59,12 +60,18 @@ ra_status ra_ring_attention_bwd_noalloc(const uint16_t *q, const uint16_t *k, co
                                         float *dq, float *dk, float *dv, int64_t S, int n_shards,
                                         ra_layout layout, int causal, float scale, ra_dims dims,
                                         void *stream) {
-  // Validate exactly as the ordinary entry point does: called without a
-  // workspace it checks every argument and launches nothing, answering
-  // RA_ERR_WORKSPACE when the arguments are good (RA_OK for an empty problem).
+  // First pass: the ordinary entry point without a workspace.  It checks the
+  // shape (dims, layout, S against n_shards and the zig-zag tile rule) and
+  // every pointer (null, 16-byte alignment), launches nothing, and answers
+  // RA_ERR_WORKSPACE when those are good (RA_OK for an empty problem).  The
+  // scale and the tensor-map encodings are checked by the second call below,
+  // before it launches anything.  The first pass's expected workspace
+  // complaint is not left behind as this thread's last error.
+  const std::string before = ra::last_error_text();
   const ra_status st = ra_ring_attention_bwd(q, k, v, out, lse, dout, dq, dk, dv, nullptr, 0, S,
                                              n_shards, layout, causal, scale, dims, stream);
   if (st != RA_ERR_WORKSPACE) return st;
+  ra::restore_last_error(before.c_str());
   const size_t need = ra_bwd_workspace_size(S, n_shards, dims);
   if (need > ra::kNoAllocScratchBytes)
     return ra::report_error(RA_ERR_WORKSPACE,

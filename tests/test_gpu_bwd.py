@@ -13,10 +13,13 @@ import torch
 from long_context_exact_gb300 import binding as ra
 from long_context_exact_gb300.inputs import (CONTIGUOUS, STRIPED, WORKLOADS, ZIGZAG,
                                              make_inputs, sample_rows, workload_inputs)
+from parity_util import (bwd_oracle_parallel, peaked_inputs, plain_only_keys, plain_rows,
+                         rel_to_max)
 
 pytestmark = pytest.mark.gpu
 
 G_TOL = 1e-2
+REL_TOL = 1e-2   # error relative to max|ref| where only plain-bf16 steps contribute
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -38,6 +41,17 @@ def _run(q, k, v, do, N, layout, causal, scale=0.0):
 
 def _err(a, r):
     return float(np.abs(a - r).max())
+
+
+def _check_plain(got, ref, sel, what):
+    """max|gpu - ref| / max|ref| over the selected rows (dq) or keys (dk, dv)
+    that only plain-bf16 steps reach: a result too small for the max-abs
+    bound to see (dK = 0, say) still fails here."""
+    if not np.any(sel):
+        return 0.0
+    rel, mref = rel_to_max(got[:, sel], ref[:, sel])
+    assert rel <= REL_TOL, f"{what}: plain-path max-abs error / max|ref| {rel:.3e} (max|ref| {mref:.3e})"
+    return rel
 
 
 CASES = [
@@ -75,6 +89,59 @@ def test_backward_custom_scale(orc):
     rq, rk, rv = orc.attn_bwd_rows(q, k, v, do, True, scale=0.07)
     errs = (_err(dq, rq), _err(dk, rk), _err(dv, rv))
     assert max(errs) <= G_TOL, errs
+
+
+PLAIN_CASES = [
+    # b, S, h, n_kv, d, N, layout, causal -- most query tiles (every one when
+    # not causal) see 4096 keys or more, so the plain bf16 P / dS path
+    # carries most of the work, against full dO on every row
+    (1, 8192, 8, 2, 128, 4, STRIPED, True),
+    (1, 8192, 8, 2, 128, 4, CONTIGUOUS, True),
+    (1, 8192, 8, 2, 128, 4, ZIGZAG, True),
+    (1, 8192, 8, 2, 128, 4, CONTIGUOUS, False),
+    (1, 8192, 6, 2, 64, 4, STRIPED, True),        # d = 64, g = 3
+]
+
+
+@pytest.mark.parametrize("b,S,h,n_kv,d,N,layout,causal", PLAIN_CASES)
+def test_backward_full_dout_plain_path(orc, b, S, h, n_kv, d, N, layout, causal):
+    q, k, v, do = make_inputs(b, S, h, n_kv, d, seed=S + 13 * N + d + layout, with_dout=True)
+    dq, dk, dv = _run(q, k, v, do, N, layout, causal)
+    rq, rk, rv = bwd_oracle_parallel(orc, q, k, v, do, causal)
+    errs = (_err(dq, rq), _err(dk, rk), _err(dv, rv))
+    assert max(errs) <= G_TOL, errs
+    pr = plain_rows(orc, layout, S, N, causal)
+    pk = plain_only_keys(orc, layout, S, N, causal)
+    assert pr.mean() >= 0.5 and pk.mean() >= 0.5
+    _check_plain(dq, rq, pr, "dq")
+    _check_plain(dk, rk, pk, "dk")
+    _check_plain(dv, rv, pk, "dv")
+
+
+# Peaked attention (parity_util.peaked_inputs): each query has one aligned key
+# met late in its ring order, so P holds entries near 1 beside many near 0.
+PEAKED = [
+    # S, h, n_kv, d, N, layout -- causal
+    (2048, 8, 2, 128, 4, STRIPED),
+    (2048, 8, 2, 128, 4, CONTIGUOUS),
+    (2048, 8, 2, 128, 4, ZIGZAG),
+    (8192, 8, 2, 128, 4, STRIPED),
+    (8192, 8, 2, 128, 4, CONTIGUOUS),
+]
+
+
+@pytest.mark.parametrize("S,h,n_kv,d,N,layout", PEAKED)
+def test_backward_peaked(orc, S, h, n_kv, d, N, layout):
+    q, k, v, do = peaked_inputs(orc, 1, S, h, n_kv, d, N, layout, True, seed=40 + S + layout,
+                                with_dout=True)
+    dq, dk, dv = _run(q, k, v, do, N, layout, True)
+    rq, rk, rv = bwd_oracle_parallel(orc, q, k, v, do, True)
+    errs = (_err(dq, rq), _err(dk, rk), _err(dv, rv))
+    assert max(errs) <= G_TOL, errs
+    _check_plain(dq, rq, plain_rows(orc, layout, S, N, True), "dq")
+    pk = plain_only_keys(orc, layout, S, N, True)
+    _check_plain(dk, rk, pk, "dk")
+    _check_plain(dv, rv, pk, "dv")
 
 
 def test_backward_layouts_agree_and_sum_invariants():
@@ -115,6 +182,11 @@ def test_workload_bwd64k_sampled_rows(orc):
     rq, rk, rv = orc.attn_bwd_rows(q, k, v, do, True, rows=rows)
     errs = (_err(dq[:, rows], rq), _err(dk, rk), _err(dv, rv))
     assert max(errs) <= G_TOL, errs
+    pr = plain_rows(orc, STRIPED, w.S, w.n_shards, True)[rows]
+    pk = plain_only_keys(orc, STRIPED, w.S, w.n_shards, True)
+    _check_plain(dq[:, rows], rq, pr, "dq")
+    _check_plain(dk, rk, pk, "dk")
+    _check_plain(dv, rv, pk, "dv")
 
 
 def test_workload_causal256k_bwd_sampled_rows(orc):
@@ -140,3 +212,8 @@ def test_workload_causal256k_bwd_sampled_rows(orc):
     rq, rk, rv = orc.attn_bwd_rows(q, k, v, do, True, rows=rows)
     errs = (_err(dq_rows, rq), _err(dk, rk), _err(dv, rv))
     assert max(errs) <= G_TOL, errs
+    pr = plain_rows(orc, STRIPED, w.S, w.n_shards, True)[rows]
+    pk = plain_only_keys(orc, STRIPED, w.S, w.n_shards, True)
+    _check_plain(dq_rows, rq, pr, "dq")
+    _check_plain(dk, rk, pk, "dk")
+    _check_plain(dv, rv, pk, "dv")

@@ -43,11 +43,15 @@ def test_noalloc_backward_matches_workspace_backward_twice(lib):
         dq = torch.full((b, S, h, d), float("nan"), device="cuda")
         dk = torch.full((b, S, n_kv, d), float("nan"), device="cuda")
         dv = torch.full((b, S, n_kv, d), float("nan"), device="cuda")
+        # a known last error first: a successful call must leave it as it was
+        assert lib.ra_ring_order(0, None, None) != ra.RA_OK
+        marker = lib.ra_last_error()
         st = lib.ra_ring_attention_bwd_noalloc(
             _p(q), _p(k), _p(v), _p(out), _p(lse), _p(do), _p(dq), _p(dk), _p(dv), S, N,
             layout, int(causal), 0.0, ra.Dims(b, h, n_kv, d),
             ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
         assert st == ra.RA_OK, lib.ra_last_error()
+        assert lib.ra_last_error() == marker
         ra.stream_check()
         for got, want in zip((dq, dk, dv), ref):
             err = (got - want).abs().max().item()
@@ -102,5 +106,7 @@ def test_forward_and_noalloc_backward_replay_as_a_cuda_graph(lib):
         e_out, e_lse = ra.ring_attention(*inputs[:3], N, layout, True)
         e_grads = ra.ring_attention_bwd(*inputs[:3], e_out, e_lse, inputs[3], N, layout, True)
         assert torch.equal(out, e_out) and torch.equal(lse, e_lse)
+        # dq, dk, dv are sums of fp32 partials added in arrival order: equal
+        # to the eager run up to fp32 rounding relative to their size
         for got, want in zip((dq, dk, dv), e_grads):
-            assert float((got - want).abs().max()) <= 1e-5
+            assert float((got - want).abs().max()) <= 1e-5 * float(want.abs().max())
