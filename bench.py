@@ -51,6 +51,9 @@ def _args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the layout / causal-imbalance measurements")
+    ap.add_argument("--ring", action="store_true",
+                    help="the real ring across the ranks: the workload's sequence split over "
+                         "them, key/value blocks exchanged point to point (ring.py)")
     return ap.parse_args()
 
 
@@ -466,6 +469,57 @@ def packed_report(w, q, k, v, do, layout, dev):
 
 
 # ---------------------------------------------------------------- our arm
+def config_table_report(dev):
+    """Throughput on each configuration of the pages' workload set, one
+    GB300: the forward (and for the b = 2 configuration the backward, as
+    2.5 x and as 2 x the forward's useful FLOPs), each timed as the best of
+    two launches after one warm-up, inputs seeded on the device."""
+    import torch
+
+    from long_context_exact_gb300 import accounting
+    from long_context_exact_gb300 import binding as ra
+    from long_context_exact_gb300.inputs import CONTIGUOUS, STRIPED, WORKLOADS
+
+    rep = {}
+    for key in ("tiny", "noncausal32k", "causal64k", "causal256k", "bwd64k"):
+        w = WORKLOADS[key]
+        gen = torch.Generator(device=dev).manual_seed(w.seed)
+
+        def rnd(*shape):
+            x = torch.randn(shape, generator=gen, device=dev, dtype=torch.float32)
+            return x.mul_(w.amplitude).to(torch.bfloat16)
+
+        q, k, v = rnd(w.b, w.S, w.h, w.d), rnd(w.b, w.S, w.n_kv, w.d), rnd(w.b, w.S, w.n_kv, w.d)
+        out = torch.empty((w.b, w.S, w.h, w.d), dtype=torch.float32, device=dev)
+        lse = torch.empty((w.b, w.h, w.S), dtype=torch.float32, device=dev)
+        f_fwd = accounting.fwd_useful_flops(w.b, w.S, w.h, w.d, w.causal)
+        for layout in w.layouts:
+            name = {CONTIGUOUS: "contiguous", STRIPED: "striped"}.get(layout, "zigzag")
+            ms = _time_ms(lambda: ra.ring_attention(q, k, v, w.n_shards, layout, w.causal,
+                                                    out=out, lse=lse))
+            row = {"workload": w.name, "fwd_ms": ms, "fwd_tflops": f_fwd / (ms / 1e3) / 1e12}
+            if w.backward:
+                do = rnd(w.b, w.S, w.h, w.d)
+                dq = torch.empty_like(out)
+                dk = torch.empty((w.b, w.S, w.n_kv, w.d), dtype=torch.float32, device=dev)
+                dv = torch.empty_like(dk)
+                ws = torch.empty(max(ra.bwd_workspace_size(w.S, w.n_shards, w.b, w.h, w.n_kv,
+                                                           w.d), 16),
+                                 dtype=torch.uint8, device=dev)
+                bms = _time_ms(lambda: ra.ring_attention_bwd(q, k, v, out, lse, do, w.n_shards,
+                                                             layout, w.causal, dq=dq, dk=dk,
+                                                             dv=dv, workspace=ws))
+                f_bwd = accounting.bwd_useful_flops(w.b, w.S, w.h, w.d, w.causal)
+                row.update({"bwd_ms": bms, "bwd_tflops": f_bwd / (bms / 1e3) / 1e12,
+                            "bwd_tflops_2x": 2.0 * f_fwd / (bms / 1e3) / 1e12,
+                            "step_tflops": (f_fwd + f_bwd) / ((ms + bms) / 1e3) / 1e12})
+                del do, dq, dk, dv, ws
+            rep[f"{key}_{name}"] = row
+        del q, k, v, out, lse
+    ra.stream_check()
+    return rep
+
+
 def run_ours(a, rank, world, local_rank):
     import torch
 
@@ -633,6 +687,7 @@ def run_ours(a, rank, world, local_rank):
                 return {"error": f"{type(exc).__name__}: {exc}"[:300]}
 
         extras = extra(layout_and_imbalance_report, w, q, k, v, dev)
+        extras["configs"] = extra(config_table_report, dev)
         if w.S != 65536:
             extras["imbalance_causal64k"] = extra(imbalance_at, "causal64k", dev)
         extras["exp2_roof"] = extra(exp2_roof_report, w, dev, clk)
@@ -674,10 +729,101 @@ def run_ours(a, rank, world, local_rank):
             "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
             "fwd_tflops": f_fwd / (fwd_ms / 1e3) / 1e12,
             "bwd_tflops": (f_bwd / (bwd_ms / 1e3) / 1e12) if have_bwd else None,
+            "bwd_tflops_2x": (2.0 * f_fwd / (bwd_ms / 1e3) / 1e12) if have_bwd else None,
+            "bwd_flops_convention": "bwd_tflops counts 2.5 x the forward's useful FLOPs (five "
+                                    "GEMMs with the recomputed QK^T); bwd_tflops_2x counts 2 x "
+                                    "(the pages' 'roughly twice')",
             "clocks": clk, "e2e": e2e, "gpu_launches": launches, "roofline": roofline,
             "cpu_baseline": cpu,
             "extras": extras,
         }
+        print(json.dumps(line), flush=True)
+
+
+def run_ring(a, rank, world, local_rank):
+    """One sequence of the workload split over the ranks of a real ring:
+    rank r holds shard r (the workload's placement) of Q, K, V and dO; a step
+    is the ring forward and backward of ring.py, key/value blocks (and the
+    backward's dK, dV) moving to the next rank over point-to-point sends
+    while each rank computes with the library's block calls.  The total work
+    is fixed as the ranks grow (strong scaling); `value` is the useful
+    TFLOP/s of the whole sequence."""
+    import torch
+
+    from long_context_exact_gb300 import accounting, ring
+    from long_context_exact_gb300 import binding as ra
+    from long_context_exact_gb300 import build as lib_build
+    from long_context_exact_gb300.inputs import STRIPED, WORKLOADS
+
+    w = WORKLOADS[a.workload]
+    layout = STRIPED if STRIPED in w.layouts else w.layouts[0]
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if rank == 0:
+        lib_build.build()
+    if world > 1:
+        torch.distributed.barrier()
+    ra.load()
+    if w.S % world != 0:
+        raise SystemExit(f"S={w.S} is not a multiple of the {world} ranks")
+    _, _, tok = ra.position_map(layout, w.S, world, device=dev)
+    pos = tok[rank].contiguous()
+    L = w.S // world
+    gen = torch.Generator(device=dev).manual_seed(replica_seed(w.seed, rank))
+
+    def rnd(*shape):
+        x = torch.randn(shape, generator=gen, device=dev, dtype=torch.float32)
+        return x.mul_(w.amplitude).to(torch.bfloat16)
+
+    q, k, v, do = rnd(w.b, L, w.h, w.d), rnd(w.b, L, w.n_kv, w.d), rnd(w.b, L, w.n_kv, w.d), \
+        rnd(w.b, L, w.h, w.d)
+
+    def step():
+        out, lse = ring.ring_attention_fwd(q, k, v, pos, pos, w.causal)
+        ring.ring_attention_bwd(q, k, v, out, lse, do, pos, pos, w.causal)
+
+    for _ in range(a.warmup):
+        step()
+    ra.stream_check()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clk_sampler = ClockSampler(local_rank)
+    clk_sampler.start()
+    launches0 = ra.launch_count()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(a.steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clk_sampler.stop()
+    launches = ra.launch_count() - launches0
+    ra.stream_check()
+    ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    flops = accounting.fwd_useful_flops(w.b, w.S, w.h, w.d, w.causal) + \
+        accounting.bwd_useful_flops(w.b, w.S, w.h, w.d, w.causal)
+    value = flops * a.steps / (ms / 1e3) / 1e12
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": a.steps, "warmup": a.warmup, "ms_per_step": ms / a.steps,
+            "higher_is_better": True, "scaling": "strong", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic", "mode": "ring",
+            "config": {"workload": w.name, "b": w.b, "S": w.S, "h": w.h, "n_kv": w.n_kv,
+                       "d": w.d, "ring_ranks": world, "rows_per_rank": L,
+                       "layout": {0: "contiguous", 1: "striped", 2: "zigzag"}[layout],
+                       "causal": w.causal, "parallelism": f"ring x{world}",
+                       "l2": "inputs larger than L2; no flush"},
+            "pct_of_bf16_peak": 100.0 * value / world / _peaks()["bf16_sustained"],
+            "clocks": clk, "gpu_launches": launches, "e2e": None, "roofline": None,
+            "cpu_baseline": None,
+            "note": "per step: ring forward (N block steps + finalize) and backward (N block "
+                    "backward steps) with the key/value exchange over torch.distributed "
+                    "point-to-point; e2e and roofline are reported by the default mode"}
         print(json.dumps(line), flush=True)
 
 
@@ -694,7 +840,10 @@ def main():
         torch.cuda.set_device(local_rank)
         torch.distributed.init_process_group("nccl")
     try:
-        run_ours(a, rank, world, local_rank)
+        if a.ring:
+            run_ring(a, rank, world, local_rank)
+        else:
+            run_ours(a, rank, world, local_rank)
     finally:
         if world > 1:
             import torch

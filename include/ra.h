@@ -57,6 +57,14 @@
  *  - The backward's dq, dk and dv are sums of fp32 partial tiles added in
  *    arrival order: two runs agree to fp32 rounding, not bit for bit.  The
  *    forward calls are deterministic.
+ *  - Precision: P (and in the backward dS) reaches the tensor cores as bf16
+ *    with fp32 accumulation.  Where that rounding could carry a large share
+ *    of a result it goes as a bf16 pair hi + lo (the second term the
+ *    rounding residual): in query tiles whose earliest row sees fewer than
+ *    4096 keys, and in the backward on steps whose P holds an entry above
+ *    1/16.  The forward re-references a row's exponent shift to the exact
+ *    row max when a key would hold more than 1/9 of the row's weight so far,
+ *    so that key's P is exactly 1.
  */
 #ifndef RA_H
 #define RA_H
@@ -215,6 +223,41 @@ ra_status ra_ring_attention_bwd(const uint16_t *q, const uint16_t *k, const uint
                                 int causal, float scale, ra_dims dims, void *stream);
 /* (dq is zeroed on the stream and then accumulated; the workspace contents
  * need no initialisation and are scratch after the call.) */
+
+/* Bytes of device workspace ra_block_step_bwd needs for Lq query rows:
+ * D and the log2-domain LSE per row, rows padded to a multiple of 128. */
+size_t ra_block_bwd_workspace_size(int64_t Lq, ra_dims dims);
+
+/* One ring step of the backward ("The Backward Pass and Gradient Exchange":
+ * the key/value block travels with its gradient accumulators dK_j, dV_j while
+ * dQ_i stays with its query block; "The Backward Pass: Symmetric Ring
+ * Operation"): the contribution of one key/value block to the gradients of
+ * one query block, with P recomputed from the query rows' final LSE,
+ *   P = exp(scale Q K^T - LSE), D = rowsum(dO * O), dS = P * (dP - D),
+ *   dq += scale dS K,  dk += scale dS^T Q,  dv += P^T dO
+ * (dk, dv summed over the g query heads of each KV head).
+ *   q, dout [b, Lq, h, d] bf16;  k, v [b, Lk, n_kv, d] bf16;
+ *   out [b, Lq, h, d] float, lse [b, h, Lq] float: the query rows' results
+ *     over the WHOLE sequence (ra_finalize after every ring step, or the
+ *     matching rows of ra_ring_attention);
+ *   dq [b, Lq, h, d], dk, dv [b, Lk, n_kv, d] float: ADDED TO, not
+ *     overwritten, so a ring walk accumulates into them step by step;
+ *   q_pos [Lq], k_pos [Lk] int32 token positions, increasing along each
+ *     block, used only when causal != 0 (key c visible to query r iff
+ *     k_pos[c] <= q_pos[r]); a causal row at position t counts as seeing
+ *     t + 1 keys for the precision rule below;
+ *   workspace: device memory of at least ra_block_bwd_workspace_size(Lq)
+ *     bytes, scratch (D and LSE are recomputed by every call).
+ * Precision as in ra_ring_attention_bwd: query tiles whose earliest row sees
+ * fewer than 4096 keys (without the causal rule: Lk < 4096) and steps whose
+ * P holds an entry above 1/16 go to the tensor cores as bf16 hi + lo pairs.
+ * Lq or Lk == 0 is a no-op.  Positions that do not increase give undefined
+ * gradients (they are not checked). */
+ra_status ra_block_step_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                            const float *out, const float *lse, const uint16_t *dout, float *dq,
+                            float *dk, float *dv, const int32_t *q_pos, const int32_t *k_pos,
+                            int64_t Lq, int64_t Lk, ra_dims dims, int causal, float scale,
+                            void *workspace, size_t workspace_bytes, void *stream);
 
 /* Size of the fixed scratch array behind ra_ring_attention_bwd_noalloc. */
 #define RA_BWD_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)

@@ -65,6 +65,8 @@ def load(path: str | None = None):
                                              I, I, I, F, Dims, P, I, P],
             "ra_ring_attention_bwd": [P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, I64, I, I, I,
                                       F, Dims, P],
+            "ra_block_step_bwd": [P, P, P, P, P, P, P, P, P, P, P, I64, I64, Dims, I, F, P,
+                                  ctypes.c_size_t, P],
             "ra_position_map": [I, I64, I, P, P, P, P],
             "ra_ring_order": [I, P, P],
             "ra_stream_check": [P],
@@ -84,6 +86,8 @@ def load(path: str | None = None):
         lib.ra_chunked_prefill.restype = I
         lib.ra_bwd_workspace_size.argtypes = [I64, I, Dims]
         lib.ra_bwd_workspace_size.restype = ctypes.c_size_t
+        lib.ra_block_bwd_workspace_size.argtypes = [I64, Dims]
+        lib.ra_block_bwd_workspace_size.restype = ctypes.c_size_t
         lib.ra_last_error.argtypes = []
         lib.ra_last_error.restype = ctypes.c_char_p
         lib.ra_version.argtypes = []
@@ -304,6 +308,37 @@ def ring_attention_bwd(q, k, v, out, lse, dout, n_shards: int, layout: int = STR
     else:
         _check(lib.ra_ring_attention_packed_bwd(*args, cu_p, n_docs, _stream(stream)))
     return dq, dk, dv
+
+
+def block_bwd_workspace_size(Lq: int, b: int, h: int, n_kv: int, d: int) -> int:
+    return int(load().ra_block_bwd_workspace_size(Lq, _dims(b, h, n_kv, d)))
+
+
+def block_step_bwd(q, k, v, out, lse, dout, grads, q_pos=None, k_pos=None,
+                   causal: bool = False, scale: float = 0.0, workspace=None, stream=None):
+    """One ring step of the backward: ADD the contribution of the key/value
+    block (k, v) to grads = (dq [b,Lq,h,d], dk, dv [b,Lk,n_kv,d]) float32,
+    given the query rows' whole-sequence out / lse.  Returns grads."""
+    lib = load()
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (dout, "dout")):
+        _need(t, torch.bfloat16, n)
+    dq, dk, dv = grads
+    for t, n in ((out, "out"), (lse, "lse"), (dq, "dq"), (dk, "dk"), (dv, "dv")):
+        _need(t, torch.float32, n)
+    if causal:
+        _need(q_pos, torch.int32, "q_pos")
+        _need(k_pos, torch.int32, "k_pos")
+    b, Lq, h, d = q.shape
+    Lk, n_kv = k.shape[1], k.shape[2]
+    ws_bytes = block_bwd_workspace_size(Lq, b, h, n_kv, d)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=q.device)
+    _check(lib.ra_block_step_bwd(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
+        _ptr(dv), _ptr(q_pos) if causal else None, _ptr(k_pos) if causal else None, Lq, Lk,
+        _dims(b, h, n_kv, d), int(bool(causal)), float(scale), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+    return grads
 
 
 def ring_attention_bwd_noalloc(q, k, v, out, lse, dout, n_shards: int, layout: int = STRIPED,

@@ -579,6 +579,84 @@ ra_status ra_ring_attention_packed_bwd(const uint16_t *q, const uint16_t *k, con
   return e == cudaSuccess ? RA_OK : cuda_fail(e, "backward launch");
 }
 
+size_t ra_block_bwd_workspace_size(int64_t Lq, ra_dims dims) {
+  return ra_bwd_workspace_size(Lq, 1, dims);
+}
+
+ra_status ra_block_step_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                            const float *out, const float *lse, const uint16_t *dout, float *dq,
+                            float *dk, float *dv, const int32_t *q_pos, const int32_t *k_pos,
+                            int64_t Lq, int64_t Lk, ra_dims dims, int causal, float scale,
+                            void *workspace, size_t workspace_bytes, void *stream) {
+  ra_status st;
+  if ((st = check_dims(dims)) != RA_OK) return st;
+  if (Lq < 0 || Lk < 0) return fail(RA_ERR_INVALID_ARG, "negative length Lq=%lld Lk=%lld",
+                                    (long long)Lq, (long long)Lk);
+  if (Lq >= (1LL << 31) || Lk >= (1LL << 31))
+    return fail(RA_ERR_UNSUPPORTED, "Lq/Lk must be below 2^31");
+  if (Lq == 0 || Lk == 0 || dims.b == 0) return RA_OK;
+  RA_CHECK_PTR(q);
+  RA_CHECK_PTR(k);
+  RA_CHECK_PTR(v);
+  RA_CHECK_PTR(out);
+  RA_CHECK_PTR(lse);
+  RA_CHECK_PTR(dout);
+  RA_CHECK_PTR(dq);
+  RA_CHECK_PTR(dk);
+  RA_CHECK_PTR(dv);
+  if (causal && (!q_pos || !k_pos))
+    return fail(RA_ERR_INVALID_ARG, "causal block backward needs q_pos and k_pos");
+  const size_t need = ra_block_bwd_workspace_size(Lq, dims);
+  if (workspace == nullptr || workspace_bytes < need)
+    return fail(RA_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need,
+                workspace == nullptr ? (size_t)0 : workspace_bytes);
+  if (!aligned16(workspace)) return fail(RA_ERR_INVALID_ARG, "workspace is not 16-byte aligned");
+  float sc = 0.f;
+  if ((st = resolve_scale(scale, dims.d, &sc)) != RA_OK) return st;
+  BwdParams p{};
+  p.cu = nullptr;
+  p.n_docs = 0;
+  p.b = dims.b;
+  p.h = dims.h;
+  p.n_kv = dims.n_kv;
+  p.g = dims.h / dims.n_kv;
+  p.N = 1;
+  p.L = static_cast<int>(Lq);
+  p.S = static_cast<int>(Lq);
+  p.layout = RA_LAYOUT_CONTIGUOUS;
+  p.causal = causal ? 1 : 0;
+  p.scale = sc;
+  p.scale_log2 = sc * kLog2e;
+  p.n_qtiles = static_cast<int>((Lq + kTile - 1) / kTile);
+  p.n_ktiles = static_cast<int>((Lk + kTile - 1) / kTile);
+  p.Lpad = p.n_qtiles * kTile;
+  p.block = 1;
+  p.Lk = static_cast<int>(Lk);
+  p.q_pos = causal ? q_pos : nullptr;
+  p.k_pos = causal ? k_pos : nullptr;
+  const size_t rows = static_cast<size_t>(dims.b) * dims.h * p.Lpad;
+  p.dvec = static_cast<float *>(workspace);
+  p.lse2 = p.dvec + rows;
+  p.dq = dq;
+  p.dk = dk;
+  p.dv = dv;
+  CUtensorMap qm, km, vm, dom, dqm, dkm, dvm;
+  const int Lqi = p.L, Lki = p.Lk;
+  if ((st = make_map(&qm, q, RA_LAYOUT_CONTIGUOUS, dims.b, 1, Lqi, dims.h, dims.d)) != RA_OK) return st;
+  if ((st = make_map(&km, k, RA_LAYOUT_CONTIGUOUS, dims.b, 1, Lki, dims.n_kv, dims.d)) != RA_OK) return st;
+  if ((st = make_map(&vm, v, RA_LAYOUT_CONTIGUOUS, dims.b, 1, Lki, dims.n_kv, dims.d)) != RA_OK) return st;
+  if ((st = make_map(&dom, dout, RA_LAYOUT_CONTIGUOUS, dims.b, 1, Lqi, dims.h, dims.d)) != RA_OK) return st;
+  if ((st = make_dq_map(&dqm, dq, RA_LAYOUT_CONTIGUOUS, dims.b, 1, Lqi, dims.h, dims.d)) != RA_OK) return st;
+  if ((st = make_dq_map(&dkm, dk, RA_LAYOUT_CONTIGUOUS, dims.b, 1, Lki, dims.n_kv, dims.d)) != RA_OK) return st;
+  if ((st = make_dq_map(&dvm, dv, RA_LAYOUT_CONTIGUOUS, dims.b, 1, Lki, dims.n_kv, dims.d)) != RA_OK) return st;
+  // one unit per (key tile, query head); dq, dk and dv are added to, not cleared
+  const long long n_units = static_cast<long long>(dims.b) * dims.h * p.n_ktiles;
+  if (n_units > 0x7fffffffLL) return fail(RA_ERR_UNSUPPORTED, "too many work units (%lld)", n_units);
+  cudaError_t e = counted(launch_bwd(p, dims.d, out, lse, dout, qm, km, vm, dom, dqm, dkm, dvm,
+                                     n_units, sm_count(), static_cast<cudaStream_t>(stream)), 2);
+  return e == cudaSuccess ? RA_OK : cuda_fail(e, "block backward launch");
+}
+
 ra_status ra_ring_attention_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                                 const float *out, const float *lse, const uint16_t *dout,
                                 float *dq, float *dk, float *dv, void *workspace,

@@ -24,7 +24,10 @@
 // steps whose query tile has a row seeing fewer than kSplitKeys keys, P and
 // dS also go to the tensor cores as a bf16 pair hi + lo (lo = the rounding
 // residual): dV += P_hi^T dO + P_lo^T dO, dK += dS_hi^T Q + dS_lo^T Q,
-// dQ = dS_hi K + dS_lo K.
+// dQ = dS_hi K + dS_lo K.  So does any step whose P holds an entry above
+// kPeakP (peaked attention): each softmax warp votes before storing P, the
+// MMA issuer reads the votes once P is ready and the dS phase once every
+// warp has voted (an mbarrier with a bounded wait, like every other).
 //
 // Warp roles (16 warps):
 //   warps 0-7  "softmax", two warpgroups each owning 64 of the 128 query
@@ -56,6 +59,10 @@ namespace ra {
 namespace {
 
 constexpr unsigned int kFull = 0xffffffffu;
+// A step whose P (normalised, <= 1) holds an entry above this also goes to
+// the tensor cores as hi + lo: one rounded bf16 P or dS then carries at most
+// 2^-8 / 16 of a row's weight (peaked attention on the plain path).
+constexpr float kPeakP = 1.0f / 16.0f;
 
 template <int D>
 struct BwdCfg {
@@ -90,9 +97,12 @@ struct BwdCfg {
   static constexpr int bStgEmpty = bDqEmpty + 1;
   static constexpr int bDone = bStgEmpty + 1;
   static constexpr int bDrain = bDone + 1;
-  static constexpr int kNumBars = bDrain + 1;
+  static constexpr int bVote = bDrain + 1;
+  static constexpr int kNumBars = bVote + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
-  static constexpr int kSmemBytes = kMiscOff + 16;
+  // per step parity and softmax warp: does the warp hold a P above kPeakP
+  static constexpr int kVoteOff = kMiscOff + 16;
+  static constexpr int kSmemBytes = kVoteOff + 2 * 8 * 4;
   // Alignment slack for the 1024-byte aligned tiles: as much as the 227 KB
   // limit leaves (the kernel checks at run time that its base needs no more).
   static constexpr int kMaxSmem = 232448;
@@ -130,7 +140,7 @@ enum : unsigned int {
   kSiteBProdKV = 0x51, kSiteBProdQ = 0x52,
   kSiteBMmaKV = 0x61, kSiteBMmaQ = 0x62, kSiteBMmaP = 0x63, kSiteBMmaDs = 0x64, kSiteBMmaDq = 0x65,
   kSiteBMmaDo = 0x66,
-  kSiteBSmS = 0x71, kSiteBSmDp = 0x72, kSiteBSmDs = 0x73, kSiteBSmStg = 0x74,
+  kSiteBSmS = 0x71, kSiteBSmDp = 0x72, kSiteBSmDs = 0x73, kSiteBSmStg = 0x74, kSiteBSmVote = 0x75,
   kSiteBDq = 0x81, kSiteBDone = 0x82, kSiteBProdDo = 0x53,
 };
 
@@ -156,7 +166,20 @@ struct KvUnit {
 // documents' query tiles, so a unit per head would be a few steps long).
 // Units run grouped by (batch, kv head, query shard) with the key tiles
 // innermost, so the resident CTAs add into one shard's dq rows of g heads.
-template <bool kDocs>
+// First index r in [0, n] with pos[r] >= v (pos increasing).
+__device__ __forceinline__ int lower_bound_pos(const int32_t *pos, int n, int v) {
+  int lo = 0, hi = n;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(pos + mid) < v)
+      lo = mid + 1;
+    else
+      hi = mid;
+  }
+  return lo;
+}
+
+template <bool kDocs, bool kBlock>
 __device__ __forceinline__ KvUnit decode_kv_unit(const BwdParams &p, long long u) {
   KvUnit x;
   x.c = static_cast<int>(u % p.n_ktiles);
@@ -179,9 +202,15 @@ __device__ __forceinline__ KvUnit decode_kv_unit(const BwdParams &p, long long u
     x.hq = -1;
   }
   const int r0 = x.c * kTile;
-  const int r1 = min(r0 + kTile, p.L) - 1;
-  x.kmin = token_at(p.layout, p.L, p.N, x.j, r0);
-  x.kmax = token_at(p.layout, p.L, p.N, x.j, r1);
+  if constexpr (kBlock) {
+    // positions of the key block's rows: given only under the causal rule
+    x.kmin = p.causal ? __ldg(p.k_pos + r0) : 0;
+    x.kmax = p.causal ? __ldg(p.k_pos + min(r0 + kTile, p.Lk) - 1) : 0;
+  } else {
+    const int r1 = min(r0 + kTile, p.L) - 1;
+    x.kmin = token_at(p.layout, p.L, p.N, x.j, r0);
+    x.kmax = token_at(p.layout, p.L, p.N, x.j, r1);
+  }
   x.a_fhi = p.n_qtiles;
   if constexpr (!kDocs) {
     x.a_hi = p.n_qtiles;
@@ -190,10 +219,12 @@ __device__ __forceinline__ KvUnit decode_kv_unit(const BwdParams &p, long long u
       x.a_flo = 0;
     } else {
       // visible query tiles: those whose last row sees the tile's first key
-      const int r_vis = max(0, first_row_at_or_after(p.layout, p.L, p.N, x.i, x.kmin));
+      const int r_vis = kBlock ? lower_bound_pos(p.q_pos, p.L, x.kmin)
+                               : max(0, first_row_at_or_after(p.layout, p.L, p.N, x.i, x.kmin));
       x.a_lo = r_vis >= p.L ? p.n_qtiles : r_vis / kTile;
       // unmasked query tiles: every row sees the tile's last key
-      const int r_full = max(0, first_row_at_or_after(p.layout, p.L, p.N, x.i, x.kmax));
+      const int r_full = kBlock ? lower_bound_pos(p.q_pos, p.L, x.kmax)
+                                : max(0, first_row_at_or_after(p.layout, p.L, p.N, x.i, x.kmax));
       x.a_flo = min(p.n_qtiles, (r_full + kTile - 1) / kTile);
     }
   } else {
@@ -247,7 +278,7 @@ __device__ __forceinline__ int doc_walk(const int32_t *c, int n_docs, int d, int
 // (every key tile of a group starts on the same query tile).  `partial` marks
 // steps that need the element mask; `split` steps whose query tile has a row
 // seeing fewer than kSplitKeys keys.
-template <bool kDocs>
+template <bool kDocs, bool kBlock>
 __device__ __forceinline__ bool q_next(const BwdParams &p, const KvUnit &x, QIter &it, int &i,
                                        int &a, int &hq, bool &partial, bool &split) {
   if constexpr (!kDocs) {
@@ -257,8 +288,13 @@ __device__ __forceinline__ bool q_next(const BwdParams &p, const KvUnit &x, QIte
     a = it.a;
     hq = x.hq;
     partial = it.a < x.a_flo;
-    split = p.causal ? (token_at(p.layout, p.L, p.N, x.i, it.a * kTile) + 1 < kSplitKeys)
-                     : (p.S < kSplitKeys);
+    // a causal row at position t sees t + 1 keys of its sequence; a block
+    // step without the causal rule takes its key block's length as the bound
+    if constexpr (kBlock)
+      split = p.causal ? (__ldg(p.q_pos + it.a * kTile) + 1 < kSplitKeys) : (p.Lk < kSplitKeys);
+    else
+      split = p.causal ? (token_at(p.layout, p.L, p.N, x.i, it.a * kTile) + 1 < kSplitKeys)
+                       : (p.S < kSplitKeys);
     return true;
   }
   // The unit's query shard: its visible query tiles from the last down, and
@@ -360,7 +396,7 @@ __device__ __forceinline__ void store_p_half(const float (&pf)[64], uint32_t tS,
   }
 }
 
-template <int D, bool kDocs>
+template <int D, bool kDocs, bool kBlock>
 __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     bwd_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUtensorMap qmap,
                const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
@@ -369,7 +405,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                const __grid_constant__ CUtensorMap dkmap,
                const __grid_constant__ CUtensorMap dvmap) {
   using C = BwdCfg<D>;
-  const KvUnit x = decode_kv_unit<kDocs>(p, blockIdx.x);
+  const KvUnit x = decode_kv_unit<kDocs, kBlock>(p, blockIdx.x);
   if (x.a_lo >= x.a_hi) return;  // no query of this shard sees the tile: nothing to add
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
@@ -403,6 +439,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     mbar_init(&bars[C::bStgEmpty], 4);
     mbar_init(&bars[C::bDone], 1);
     mbar_init(&bars[C::bDrain], 1);
+    mbar_init(&bars[C::bVote], 8);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -440,7 +477,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       QIter it;
       int i, a, hq, n = 0;
       bool partial, split;
-      while (q_next<kDocs>(p, x, it, i, a, hq, partial, split)) {
+      while (q_next<kDocs, kBlock>(p, x, it, i, a, hq, partial, split)) {
         if (lane == 0) {
           int c2, c3;
           map_coords(p.layout, p.L, p.N, i, a * kTile, c2, c3);
@@ -497,7 +534,18 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         QIter it;
         int i, a, hq, n = 0;
         bool partial, split;
-        bool has = q_next<kDocs>(p, x, it, i, a, hq, partial, split);
+        // S^T of the step after n, once its Q tile has landed
+        auto issue_next_s = [&](int n_cur) -> bool {
+          const int st1 = (n_cur + 1) % C::kQSt;
+          if (!mbar_wait(&bars[C::bQFull + st1], ((n_cur + 1) / C::kQSt) & 1, abort_flag,
+                         kSiteBMmaQ))
+            return false;
+          tc_fence_after();
+          mma_kk<D>(tmem + C::kColS, k_s, sbase + C::kQOff + st1 * C::kTileBytes, C::kIdescKK);
+          mma_commit(&bars[C::bSFull]);
+          return true;
+        };
+        bool has = q_next<kDocs, kBlock>(p, x, it, i, a, hq, partial, split);
         if (has && lane == 0) {
           if (mbar_wait(&bars[C::bQFull + 0], 0, abort_flag, kSiteBMmaQ)) {
             tc_fence_after();
@@ -507,8 +555,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         }
         __syncwarp();
         while (has && !*abort_flag) {
-          const bool cur_split = split;
-          const bool has_next = q_next<kDocs>(p, x, it, i, a, hq, partial, split);
+          bool cur_split = split;
+          const bool has_next = q_next<kDocs, kBlock>(p, x, it, i, a, hq, partial, split);
           if (lane == 0) {
             const int st = n % C::kQSt;
             const uint32_t q_s = sbase + C::kQOff + st * C::kTileBytes;
@@ -522,8 +570,22 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
               mma_commit(&bars[C::bDpFull]);
               go = mbar_wait(&bars[C::bPReady], n & 1, abort_flag, kSiteBMmaP);
             }
+            // a step with a peaked P (some softmax warp's vote, written
+            // before it arrived on bPReady) also takes the hi + lo path; its
+            // residual MMA for dV waits for the dS phase, where the warps
+            // without a peaked P write zero residuals, and the next S^T
+            // (which overwrites P) waits with it
+            bool dyn = false;
             if (go) {
               tc_fence_after();
+              if (!cur_split) {
+                const volatile uint32_t *vote =
+                    reinterpret_cast<const volatile uint32_t *>(smem + C::kVoteOff) + (n & 1) * 8;
+                uint32_t any = 0u;
+#pragma unroll
+                for (int w = 0; w < 8; ++w) any |= vote[w];
+                dyn = any != 0u;
+              }
               // dV += P_hi^T dO (+ P_lo^T dO): A from TMEM (bf16 pairs), B = dO MN-major
 #pragma unroll
               for (int kk = 0; kk < kTile / 16; ++kk)
@@ -536,23 +598,26 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                   mma_ts(tmem + C::kColDv, tmem + C::kColS + (kk >> 2) * 64 + 32 + (kk & 3) * 8,
                          smem_desc_sw128(do_s + kk * 16 * 128, kTile * 128, 1024), C::kIdescDv,
                          1u);
-              mma_commit(&bars[C::bDoEmpty]);
-              if (has_next) {
-                const int st1 = (n + 1) % C::kQSt;
-                go = mbar_wait(&bars[C::bQFull + st1], ((n + 1) / C::kQSt) & 1, abort_flag,
-                               kSiteBMmaQ);
-                if (go) {
-                  tc_fence_after();
-                  mma_kk<D>(tmem + C::kColS, k_s, sbase + C::kQOff + st1 * C::kTileBytes,
-                            C::kIdescKK);
-                  mma_commit(&bars[C::bSFull]);
-                }
+              if (!dyn) {
+                mma_commit(&bars[C::bDoEmpty]);
+                if (has_next) go = issue_next_s(n);
               }
             }
             if (go) go = mbar_wait(&bars[C::bDsReady], n & 1, abort_flag, kSiteBMmaDs);
             if (go) {
               tc_fence_after();
-              if (!cur_split) {
+              if (dyn) {
+#pragma unroll
+                for (int kk = 0; kk < kTile / 16; ++kk)
+                  mma_ts(tmem + C::kColDv, tmem + C::kColS + (kk >> 2) * 64 + 32 + (kk & 3) * 8,
+                         smem_desc_sw128(do_s + kk * 16 * 128, kTile * 128, 1024), C::kIdescDv,
+                         1u);
+                mma_commit(&bars[C::bDoEmpty]);
+                if (has_next) go = issue_next_s(n);
+              }
+            }
+            if (go) {
+              if (!(cur_split || dyn)) {
                 // dQ first, so the drain (and with it the next dP^T) starts
                 // while dK accumulates
                 issue_dq<D>(tmem + C::kColDp, ds_s, k_s);
@@ -594,8 +659,15 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     const uint32_t tS = tmem + lane_off + C::kColS;
     const uint32_t tDp = tmem + lane_off + C::kColDp + cb;
     const int kr = x.c * kTile + row;
-    const bool key_exists = kr < p.L;
-    const int kp = token_at(p.layout, p.L, p.N, x.j, key_exists ? kr : p.L - 1);
+    const int n_keys = kBlock ? p.Lk : p.L;
+    const bool key_exists = kr < n_keys;
+    // this key's position (a block step without the causal rule has none:
+    // nothing below reads it then)
+    int kp;
+    if constexpr (kBlock)
+      kp = p.causal ? __ldg(p.k_pos + (key_exists ? kr : n_keys - 1)) : 0;
+    else
+      kp = token_at(p.layout, p.L, p.N, x.j, key_exists ? kr : p.L - 1);
     // this key is seen by the query positions [kq_lo, kq_hi)
     int kq_lo = kp, kq_hi = p.S;
     if constexpr (kDocs) {
@@ -610,7 +682,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     QIter it;
     int i, a, hq, n = 0;
     bool partial, split;
-    while (q_next<kDocs>(p, x, it, i, a, hq, partial, split)) {
+    while (q_next<kDocs, kBlock>(p, x, it, i, a, hq, partial, split)) {
       // this step's LSE2 and D rows, staged by the producer with the Q tile
       const float4 *lse4 = reinterpret_cast<const float4 *>(
                                smem + C::kStatOff + (n % C::kQSt) * 2 * C::kRowStatBytes) +
@@ -619,7 +691,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       // query columns cb + c with c < c0 or c >= c1 are masked for this key
       int c0 = 0, c1 = C::kHalfCols;
       if (partial) {
-        c0 = first_row_at_or_after(p.layout, p.L, p.N, i, kq_lo) - a * kTile - cb;
+        c0 = (kBlock ? lower_bound_pos(p.q_pos, p.L, kq_lo)
+                     : first_row_at_or_after(p.layout, p.L, p.N, i, kq_lo)) -
+             a * kTile - cb;
         if constexpr (kDocs)
           c1 = first_row_at_or_after(p.layout, p.L, p.N, i, kq_hi) - a * kTile - cb;
       }
@@ -661,7 +735,23 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         for (int c = 0; c < C::kHalfCols; ++c)
           if (c < c0 || (kDocs && c >= c1)) pf[c] = 0.f;
       }
-      if (split)
+      // Vote: does this warp hold a P above kPeakP?  Any vote sends the step
+      // through hi + lo (the MMA issuer and the dS phase read the votes); a
+      // warp that voted stores its P residual now, the others store zeros
+      // in the dS phase if the step turns out split.
+      bool peaked = false;
+      if (!split) {
+        float pm = 0.f;
+#pragma unroll
+        for (int c = 0; c < C::kHalfCols; c += 2) pm = fmax3(pm, pf[c], pf[c + 1]);
+        peaked = __any_sync(kFull, pm > kPeakP);
+      }
+      if (lane == 0) {
+        reinterpret_cast<volatile uint32_t *>(smem + C::kVoteOff)[(n & 1) * 8 + warp] =
+            peaked ? 1u : 0u;
+        mbar_arrive(&bars[C::bVote]);
+      }
+      if (split || peaked)
         store_p_half<true>(pf, tS, cb);
       else
         store_p_half<false>(pf, tS, cb);
@@ -672,8 +762,31 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
 
       bool go = mbar_wait(&bars[C::bDpFull], n & 1, abort_flag, kSiteBSmDp);
       if (go) go = mbar_wait(&bars[C::bDsEmpty], (n & 1) ^ 1, abort_flag, kSiteBSmDs);
+      // every softmax warp's vote for this step is in
+      bool step_split = split;
+      if (go && !split) {
+        go = mbar_wait(&bars[C::bVote], n & 1, abort_flag, kSiteBSmVote);
+        if (go) {
+          const volatile uint32_t *vote =
+              reinterpret_cast<const volatile uint32_t *>(smem + C::kVoteOff) + (n & 1) * 8;
+          uint32_t any = 0u;
+#pragma unroll
+          for (int w = 0; w < 8; ++w) any |= vote[w];
+          step_split = any != 0u;
+        }
+      }
+      // switched to hi + lo by another warp's vote: this warp's P residual
+      // columns get zeros (its P entries are all below kPeakP).  The MMA
+      // issuer reads them after bDsReady and only then issues the next S^T.
+      const bool zero_lo = go && step_split && !split && !peaked;
+      if (__any_sync(kFull, zero_lo)) {
+        uint32_t z[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) z[e] = 0u;
+        tmem_st32(tS + cb + 32, z);
+      }
       // the residual goes to the staging buffer once the drain is done with it
-      if (go && split && n > 0)
+      if (go && step_split && n > 0)
         go = mbar_wait(&bars[C::bStgEmpty], (n - 1) & 1, abort_flag, kSiteBSmStg);
       if (!__all_sync(kFull, go)) break;
       tc_fence_after();
@@ -707,7 +820,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
           *reinterpret_cast<uint4 *>(ds_row + chunk * 16) =
               make_uint4(whi[u * 4 + 0], whi[u * 4 + 1], whi[u * 4 + 2], whi[u * 4 + 3]);
         }
-        if (split) {
+        if (step_split) {
           uint32_t wlo[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e)
@@ -721,6 +834,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
           }
         }
       }
+      if (zero_lo) tmem_st_wait();
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
@@ -737,7 +851,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     int i, a, hq, n = 0;
     bool partial, split;
     bool aborted = false;
-    while (q_next<kDocs>(p, x, it, i, a, hq, partial, split)) {
+    while (q_next<kDocs, kBlock>(p, x, it, i, a, hq, partial, split)) {
       if (!__all_sync(kFull, mbar_wait(&bars[C::bDqFull], n & 1, abort_flag, kSiteBDq))) {
         aborted = true;
         break;
@@ -833,7 +947,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
           }
           fence_proxy_async_smem();
           __syncwarp();
-          if (lane == 0 && r0 < p.L) {
+          if (lane == 0 && r0 < (kBlock ? p.Lk : p.L)) {
 #pragma unroll
             for (int bx = 0; bx < 2; ++bx)
               tma_reduce_add_5d(is_dk ? &dkmap : &dvmap, stg + bx * C::kDqBoxBytes,
@@ -935,7 +1049,8 @@ cudaError_t launch_bwd_t(const BwdParams &p, const float *out, const float *lse,
                       stream>>>(p, out, lse, dout);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  auto kern = p.cu != nullptr ? bwd_kernel<D, true> : bwd_kernel<D, false>;
+  auto kern = p.block ? bwd_kernel<D, false, true>
+                      : (p.cu != nullptr ? bwd_kernel<D, true, false> : bwd_kernel<D, false, false>);
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemAlloc);
   if (e != cudaSuccess) return e;
   {

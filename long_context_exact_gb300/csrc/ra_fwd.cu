@@ -25,8 +25,9 @@
 //
 // Exponentials are base 2 with log2(e) folded into the scale.  The running
 // max used as the exponent shift is only raised when a row's max grows by
-// more than 8 (log2 units), so most tiles skip the O rescale; P stays
-// <= 2^8 and the result is unchanged because O and l share the same shift.
+// more than 8 (log2 units), or when the key that raised it would dominate
+// the row's sum so far, so most tiles skip the O rescale; P stays <= 2^8 and
+// the result is unchanged because O and l share the same shift.
 // Once every row of a warp has a shift, P is formed against it before the
 // tile's row max is known (the max is taken while the P stores drain); the
 // rare tile whose max passes a row's shift by more than 8 is formed again.
@@ -47,6 +48,11 @@ namespace ra {
 namespace {
 
 constexpr float kRescaleThreshold = 8.0f;
+// A row also takes its tile max as the exact shift when a key of the tile
+// would hold more than 1 / (kDominance + 1) of the row's weight so far: that
+// key's P is then exactly 1, and no single rounded bf16 P carries a large
+// share of the row (peaked attention on the plain path).
+constexpr float kDominance = 8.0f;
 // block mode, causal: words of the CTA's keep bits (then as many mask bits)
 constexpr int kBitWords = kBlockKeyTiles / 32;
 constexpr unsigned int kFull = 0xffffffffu;
@@ -675,10 +681,16 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::kThreads, 1)
       // its shift by more than the threshold (rare after the first tiles)
       // takes a new shift and the warp forms the tile's P again.
       bool spec = __all_sync(kFull, m_run != -INFINITY);
+      // a new shift: the max passed the old one by more than the threshold,
+      // or by less but with a key that would dominate the row's sum so far
+      auto needs_shift = [&](float mx2) {
+        return mx2 > m_run + kRescaleThreshold ||
+               (mx2 > m_run && ex2(mx2 - m_run) * kDominance > l_sum);
+      };
       if (!spec) {
         const float mx2 = row_max() * sl2;
         m_max = fmaxf(m_max, mx2);
-        const bool need = mx2 > m_run + kRescaleThreshold;
+        const bool need = needs_shift(mx2);
         float alpha = 1.f;
         if (need) {
           alpha = ex2(m_run - mx2);  // 0 when m_run is still -inf
@@ -694,7 +706,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::kThreads, 1)
         spec = false;
         const float mx2 = row_max() * sl2;
         m_max = fmaxf(m_max, mx2);
-        const bool need = mx2 > m_run + kRescaleThreshold;
+        const bool need = needs_shift(mx2);
         if (!__any_sync(kFull, need)) break;
         float alpha = 1.f;
         if (need) {

@@ -172,6 +172,12 @@ struct BwdParams {
   const int32_t *cu;        // packed-document offsets [b][n_docs + 1], or null
   int n_docs;
   int N, L, S;              // shards, rows per shard, tokens per sequence
+  // block mode: one query block of L rows (N = 1, S = L) against one key
+  // block of Lk rows, token positions from q_pos / k_pos (increasing)
+  int block;
+  int Lk;
+  const int32_t *q_pos;     // [L]
+  const int32_t *k_pos;     // [Lk]
   int layout, causal;
   float scale;              // dQ, dK multiplier
   float scale_log2;         // scale * log2(e)

@@ -1,3 +1,4 @@
+import json
 import os
 import sys
 
@@ -18,3 +19,14 @@ def orc():
     from oracle import oracle
     oracle.build()
     return oracle
+
+
+def pytest_sessionfinish(session, exitstatus):
+    """With RA_PARITY_REPORT set, write the errors the parity tests measured
+    (max-abs and relative, per output) to that file as JSON."""
+    path = os.environ.get("RA_PARITY_REPORT")
+    mod = sys.modules.get("parity_util")
+    if not path or mod is None or not mod.RECORDS:
+        return
+    with open(path, "w") as f:
+        json.dump(mod.RECORDS, f, indent=1, sort_keys=True)

@@ -22,6 +22,16 @@ import numpy as np
 SPLIT_KEYS = 4096   # the library's hi + lo threshold (keys seen by a tile's earliest row)
 TILE = 128          # query rows per tile
 
+# Measured errors per test, written out at the end of the session when
+# RA_PARITY_REPORT names a file (tests/conftest.py).
+RECORDS: dict = {}
+
+
+def record(prefix: str = "", **errs) -> None:
+    """Keep the measured errors of the running test under its node id."""
+    name = os.environ.get("PYTEST_CURRENT_TEST", "?").split(" ")[0]
+    RECORDS.setdefault(name, {}).update({prefix + k: float(v) for k, v in errs.items()})
+
 
 def plain_rows(orc, layout: int, S: int, N: int, causal: bool) -> np.ndarray:
     """Boolean [S] over token positions: True where the token's query tile

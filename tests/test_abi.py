@@ -245,3 +245,41 @@ def test_causal_block_ranges_are_bounded(lib):
     rows = 1 * 4 * 128
     need = lib.ra_prefill_workspace_size(128, 2 * over, 0, d)
     assert need >= 3 * rows * (2 + 128) * 4
+
+
+def test_block_step_bwd_validates_on_the_host(lib):
+    """The block backward rejects bad arguments before any launch: causal
+    without positions, a missing or short workspace, null or misaligned
+    pointers; empty blocks are a no-op."""
+    d = _dims()
+    ws = lib.ra_block_bwd_workspace_size(1024, d)
+    assert ws == lib.ra_bwd_workspace_size(1024, 1, d) == 2 * 1 * 4 * 1024 * 4
+    args = [FAKE] * 9
+    # causal without q_pos / k_pos
+    assert lib.ra_block_step_bwd(*args, None, None, 1024, 512, d, 1, 0.0, FAKE, ws, None) == \
+        binding.RA_ERR_INVALID_ARG
+    # workspace missing or too small
+    assert lib.ra_block_step_bwd(*args, FAKE, FAKE, 1024, 512, d, 1, 0.0, None, 0, None) == \
+        binding.RA_ERR_WORKSPACE
+    assert lib.ra_block_step_bwd(*args, FAKE, FAKE, 1024, 512, d, 1, 0.0, FAKE, ws - 16,
+                                 None) == binding.RA_ERR_WORKSPACE
+    # null dk, misaligned dout
+    bad = list(args)
+    bad[7] = None
+    assert lib.ra_block_step_bwd(*bad, FAKE, FAKE, 1024, 512, d, 1, 0.0, FAKE, ws, None) == \
+        binding.RA_ERR_INVALID_ARG
+    assert "dk" in lib.ra_last_error().decode()
+    bad = list(args)
+    bad[5] = MISALIGNED
+    assert lib.ra_block_step_bwd(*bad, FAKE, FAKE, 1024, 512, d, 1, 0.0, FAKE, ws, None) == \
+        binding.RA_ERR_INVALID_ARG
+    # d unsupported, negative length
+    assert lib.ra_block_step_bwd(*args, FAKE, FAKE, 1024, 512, _dims(d=96), 1, 0.0, FAKE, ws,
+                                 None) == binding.RA_ERR_UNSUPPORTED
+    assert lib.ra_block_step_bwd(*args, FAKE, FAKE, -1, 512, d, 1, 0.0, FAKE, ws, None) == \
+        binding.RA_ERR_INVALID_ARG
+    # empty blocks: nothing to do, nothing launched
+    assert lib.ra_block_step_bwd(*args, FAKE, FAKE, 0, 512, d, 1, 0.0, None, 0, None) == \
+        binding.RA_OK
+    assert lib.ra_block_step_bwd(*args, FAKE, FAKE, 1024, 0, d, 1, 0.0, None, 0, None) == \
+        binding.RA_OK

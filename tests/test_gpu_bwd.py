@@ -14,7 +14,7 @@ from long_context_exact_gb300 import binding as ra
 from long_context_exact_gb300.inputs import (CONTIGUOUS, STRIPED, WORKLOADS, ZIGZAG,
                                              make_inputs, sample_rows, workload_inputs)
 from parity_util import (bwd_oracle_parallel, peaked_inputs, plain_only_keys, plain_rows,
-                         rel_to_max)
+                         record, rel_to_max)
 
 pytestmark = pytest.mark.gpu
 
@@ -50,6 +50,7 @@ def _check_plain(got, ref, sel, what):
     if not np.any(sel):
         return 0.0
     rel, mref = rel_to_max(got[:, sel], ref[:, sel])
+    record(**{what + "_plain_rel": rel})
     assert rel <= REL_TOL, f"{what}: plain-path max-abs error / max|ref| {rel:.3e} (max|ref| {mref:.3e})"
     return rel
 
@@ -80,6 +81,7 @@ def test_backward_matches_oracle(orc, b, S, h, n_kv, d, N, layout, causal):
     dq, dk, dv = _run(q, k, v, do, N, layout, causal)
     rq, rk, rv = orc.attn_bwd_rows(q, k, v, do, causal)
     errs = (_err(dq, rq), _err(dk, rk), _err(dv, rv))
+    record(dq_max_abs=errs[0], dk_max_abs=errs[1], dv_max_abs=errs[2])
     assert max(errs) <= G_TOL, errs
 
 
@@ -88,6 +90,7 @@ def test_backward_custom_scale(orc):
     dq, dk, dv = _run(q, k, v, do, 4, STRIPED, True, scale=0.07)
     rq, rk, rv = orc.attn_bwd_rows(q, k, v, do, True, scale=0.07)
     errs = (_err(dq, rq), _err(dk, rk), _err(dv, rv))
+    record(dq_max_abs=errs[0], dk_max_abs=errs[1], dv_max_abs=errs[2])
     assert max(errs) <= G_TOL, errs
 
 
@@ -109,6 +112,7 @@ def test_backward_full_dout_plain_path(orc, b, S, h, n_kv, d, N, layout, causal)
     dq, dk, dv = _run(q, k, v, do, N, layout, causal)
     rq, rk, rv = bwd_oracle_parallel(orc, q, k, v, do, causal)
     errs = (_err(dq, rq), _err(dk, rk), _err(dv, rv))
+    record(dq_max_abs=errs[0], dk_max_abs=errs[1], dv_max_abs=errs[2])
     assert max(errs) <= G_TOL, errs
     pr = plain_rows(orc, layout, S, N, causal)
     pk = plain_only_keys(orc, layout, S, N, causal)
@@ -137,11 +141,79 @@ def test_backward_peaked(orc, S, h, n_kv, d, N, layout):
     dq, dk, dv = _run(q, k, v, do, N, layout, True)
     rq, rk, rv = bwd_oracle_parallel(orc, q, k, v, do, True)
     errs = (_err(dq, rq), _err(dk, rk), _err(dv, rv))
+    record(dq_max_abs=errs[0], dk_max_abs=errs[1], dv_max_abs=errs[2])
     assert max(errs) <= G_TOL, errs
     _check_plain(dq, rq, plain_rows(orc, layout, S, N, True), "dq")
     pk = plain_only_keys(orc, layout, S, N, True)
     _check_plain(dk, rk, pk, "dk")
     _check_plain(dv, rv, pk, "dv")
+
+
+def _block_ring_bwd(q, k, v, do, N, layout, causal):
+    """The ring's backward as block steps: query block i stays home with its
+    dQ_i; key/value block j carries its dK_j, dV_j and meets the query blocks
+    in ring order (block (i - s) mod N at query block i's step s)."""
+    b, S, h, d = q.shape
+    n_kv = k.shape[2]
+    L = S // N
+    qd, kd, vd, dod = (t.cuda() for t in (q, k, v, do))
+    out, lse = ra.ring_attention(qd, kd, vd, N, layout, causal)
+    _, _, tok = ra.position_map(layout, S, N)
+    order = ra.ring_order(N).cpu().numpy()
+    dk_acc = [torch.zeros((b, L, n_kv, d), device="cuda") for _ in range(N)]
+    dv_acc = [torch.zeros((b, L, n_kv, d), device="cuda") for _ in range(N)]
+    kb = [kd.index_select(1, tok[j].long()).contiguous() for j in range(N)]
+    vb = [vd.index_select(1, tok[j].long()).contiguous() for j in range(N)]
+    dq = torch.full((b, S, h, d), float("nan"), device="cuda")
+    for i in range(N):
+        ti = tok[i].long()
+        qi, oi, doi = (t.index_select(1, ti).contiguous() for t in (qd, out, dod))
+        li = lse.index_select(2, ti).contiguous()
+        dq_i = torch.zeros((b, L, h, d), device="cuda")
+        for s_ in range(N):
+            j = int(order[i, s_])
+            ra.block_step_bwd(qi, kb[j], vb[j], oi, li, doi, (dq_i, dk_acc[j], dv_acc[j]),
+                              tok[i], tok[j], causal)
+        dq[:, ti] = dq_i
+    dk = torch.full((b, S, n_kv, d), float("nan"), device="cuda")
+    dv = torch.full((b, S, n_kv, d), float("nan"), device="cuda")
+    for j in range(N):
+        dk[:, tok[j].long()] = dk_acc[j]
+        dv[:, tok[j].long()] = dv_acc[j]
+    ra.stream_check()
+    return [t.double().cpu().numpy() for t in (dq, dk, dv)]
+
+
+@pytest.mark.parametrize("S,N,layout,causal", [
+    (2048, 4, STRIPED, True), (2048, 4, CONTIGUOUS, True), (2048, 4, ZIGZAG, True),
+    (2048, 4, CONTIGUOUS, False),
+    (8192, 2, STRIPED, True),          # mostly the plain bf16 path
+    (1200, 3, STRIPED, True),          # ragged blocks of 400 rows
+])
+def test_block_step_bwd_over_ring_matches_oracle(orc, S, N, layout, causal):
+    b, h, n_kv, d = 1, 8, 2, 128
+    q, k, v, do = make_inputs(b, S, h, n_kv, d, seed=S + N + layout, with_dout=True)
+    dq, dk, dv = _block_ring_bwd(q, k, v, do, N, layout, causal)
+    assert not (np.isnan(dq).any() or np.isnan(dk).any() or np.isnan(dv).any())
+    rq, rk, rv = bwd_oracle_parallel(orc, q, k, v, do, causal)
+    errs = (_err(dq, rq), _err(dk, rk), _err(dv, rv))
+    record(dq_max_abs=errs[0], dk_max_abs=errs[1], dv_max_abs=errs[2])
+    assert max(errs) <= G_TOL, errs
+    _check_plain(dq, rq, plain_rows(orc, layout, S, N, causal), "dq")
+    pk = plain_only_keys(orc, layout, S, N, causal)
+    _check_plain(dk, rk, pk, "dk")
+    _check_plain(dv, rv, pk, "dv")
+
+
+def test_block_step_bwd_d64_gqa_odd(orc):
+    """d = 64 and three query heads per KV head through the block backward."""
+    b, S, h, n_kv, d, N = 1, 1024, 6, 2, 64, 2
+    q, k, v, do = make_inputs(b, S, h, n_kv, d, seed=77, with_dout=True)
+    dq, dk, dv = _block_ring_bwd(q, k, v, do, N, STRIPED, True)
+    rq, rk, rv = bwd_oracle_parallel(orc, q, k, v, do, True)
+    errs = (_err(dq, rq), _err(dk, rk), _err(dv, rv))
+    record(dq_max_abs=errs[0], dk_max_abs=errs[1], dv_max_abs=errs[2])
+    assert max(errs) <= G_TOL, errs
 
 
 def test_backward_layouts_agree_and_sum_invariants():
@@ -181,6 +253,7 @@ def test_workload_bwd64k_sampled_rows(orc):
     dq, dk, dv = _run(q, k, v, do_m, w.n_shards, STRIPED, True)
     rq, rk, rv = orc.attn_bwd_rows(q, k, v, do, True, rows=rows)
     errs = (_err(dq[:, rows], rq), _err(dk, rk), _err(dv, rv))
+    record(dq_max_abs=errs[0], dk_max_abs=errs[1], dv_max_abs=errs[2])
     assert max(errs) <= G_TOL, errs
     pr = plain_rows(orc, STRIPED, w.S, w.n_shards, True)[rows]
     pk = plain_only_keys(orc, STRIPED, w.S, w.n_shards, True)
@@ -211,9 +284,31 @@ def test_workload_causal256k_bwd_sampled_rows(orc):
     del qd, kd, vd, dod, out, lse, dq
     rq, rk, rv = orc.attn_bwd_rows(q, k, v, do, True, rows=rows)
     errs = (_err(dq_rows, rq), _err(dk, rk), _err(dv, rv))
+    record(dq_max_abs=errs[0], dk_max_abs=errs[1], dv_max_abs=errs[2])
     assert max(errs) <= G_TOL, errs
     pr = plain_rows(orc, STRIPED, w.S, w.n_shards, True)[rows]
     pk = plain_only_keys(orc, STRIPED, w.S, w.n_shards, True)
     _check_plain(dq_rows, rq, pr, "dq")
     _check_plain(dk, rk, pk, "dk")
     _check_plain(dv, rv, pk, "dv")
+
+
+def test_ring_module_single_process_on_gpu(orc):
+    """ring.py's product path (the library's block calls) in one process, a
+    ring of one: the forward is one block step over the whole sequence and a
+    finalize, the backward one block backward; both match the oracle."""
+    from long_context_exact_gb300 import ring
+    b, S, h, n_kv, d = 1, 1024, 4, 2, 128
+    q, k, v, do = make_inputs(b, S, h, n_kv, d, seed=5, with_dout=True)
+    qd, kd, vd, dod = (t.cuda() for t in (q, k, v, do))
+    pos = torch.arange(S, dtype=torch.int32, device="cuda")
+    out, lse = ring.ring_attention_fwd(qd, kd, vd, pos, pos, True)
+    dq, dk, dv = ring.ring_attention_bwd(qd, kd, vd, out, lse, dod, pos, pos, True)
+    ra.stream_check()
+    ref_o, ref_l = orc.attn_fwd_rows(q, k, v, True)
+    assert _err(out.double().cpu().numpy(), ref_o) <= 1e-2
+    assert _err(lse.double().cpu().numpy(), ref_l) <= 1e-3
+    rq, rk, rv = orc.attn_bwd_rows(q, k, v, do, True)
+    errs = (_err(dq.double().cpu().numpy(), rq), _err(dk.double().cpu().numpy(), rk),
+            _err(dv.double().cpu().numpy(), rv))
+    assert max(errs) <= G_TOL, errs

@@ -12,7 +12,7 @@ import torch
 from long_context_exact_gb300 import binding as ra
 from long_context_exact_gb300.inputs import (CONTIGUOUS, STRIPED, WORKLOADS, ZIGZAG,
                                              make_inputs, sample_rows, workload_inputs)
-from parity_util import peaked_inputs, plain_rows, rel_to_max
+from parity_util import peaked_inputs, plain_rows, record, rel_to_max
 
 pytestmark = pytest.mark.gpu
 
@@ -46,17 +46,18 @@ def _ring(q, k, v, N, layout, causal, scale=0.0):
     return ra.ring_attention(q, k, v, N, layout, causal, scale=scale, out=out, lse=lse)
 
 
-def _rel_plain(o, ref_o, plain, what):
+def _rel_plain(o, ref_o, plain, what, tag=""):
     """On the rows that take the plain bf16 path: max|gpu - ref| / max|ref|
     <= REL_TOL, so that a small reference cannot hide a wrong result."""
     if not plain.any():
         return 0.0
     rel, ref = rel_to_max(o[:, plain], ref_o[:, plain])
+    record(tag, o_plain_rel=rel)
     assert rel <= REL_TOL, f"{what}: plain-path rows max-abs error / max|ref| {rel:.3e} (max|ref| {ref:.3e})"
     return rel
 
 
-def _cmp(out, lse, ref_out, ref_lse, rows=None):
+def _cmp(out, lse, ref_out, ref_lse, rows=None, tag=""):
     """Every output written (no NaN left in the NaN-filled buffers), then the
     spec max-abs bounds on O and LSE over the checked rows."""
     assert not bool(torch.isnan(out).any()) and not bool(torch.isnan(lse).any()), \
@@ -71,6 +72,7 @@ def _cmp(out, lse, ref_out, ref_lse, rows=None):
     fin = np.isfinite(ref_lse)
     assert np.array_equal(np.isfinite(l), fin)
     err_l = np.abs(l[fin] - ref_lse[fin]).max() if fin.any() else 0.0
+    record(tag, o_max_abs=err_o, lse_max_abs=err_l)
     assert err_o <= O_TOL, f"O max-abs {err_o}"
     assert err_l <= LSE_TOL, f"LSE max-abs {err_l}"
     return err_o, err_l
@@ -480,10 +482,11 @@ def _workload_parity(orc, name, layouts=None):
     for layout in (layouts or w.layouts):
         out, lse = _ring(qd, kd, vd, w.n_shards, layout, w.causal)
         ra.stream_check()
-        errs[layout] = _cmp(out, lse, ref_o, ref_l, rows)
+        tag = ("contiguous_", "striped_", "zigzag_")[layout]
+        errs[layout] = _cmp(out, lse, ref_o, ref_l, rows, tag=tag)
         plain = plain_rows(orc, layout, w.S, w.n_shards, w.causal)[rows]
         o = out.index_select(1, torch.from_numpy(rows).cuda()).double().cpu().numpy()
-        errs[layout] += (_rel_plain(o, ref_o, plain, f"{name} layout {layout}"),)
+        errs[layout] += (_rel_plain(o, ref_o, plain, f"{name} layout {layout}", tag=tag),)
         del out, lse
     return errs
 
