@@ -24,10 +24,13 @@
 // steps whose query tile has a row seeing fewer than kSplitKeys keys, P and
 // dS also go to the tensor cores as a bf16 pair hi + lo (lo = the rounding
 // residual): dV += P_hi^T dO + P_lo^T dO, dK += dS_hi^T Q + dS_lo^T Q,
-// dQ = dS_hi K + dS_lo K.  So does any step whose P holds an entry above
-// kPeakP (peaked attention): each softmax warp votes before storing P, the
-// MMA issuer reads the votes once P is ready and the dS phase once every
-// warp has voted (an mbarrier with a bounded wait, like every other).
+// dQ = dS_hi K + dS_lo K.  Peaked attention: a softmax warp that meets an
+// entry of P above kPeakP on a plain step marks the unit, and once every
+// role has finished the unit's steps (an mbarrier the softmax warps arrive
+// on, waited with the usual bound) a marked unit walks its plain steps a
+// second time, adding only the residual terms P_lo^T dO, dS_lo^T Q and
+// dS_lo K: the sum is what the hi + lo path would have given.  Units that
+// meet no such entry (all of them on diffuse inputs) pay only the max.
 //
 // Warp roles (16 warps):
 //   warps 0-7  "softmax", two warpgroups each owning 64 of the 128 query
@@ -50,6 +53,7 @@
 // MN-major); dQ = dS K (dS^T read MN-major, K MN-major).
 #include <climits>
 #include <cmath>
+#include <type_traits>
 
 #include "ra_internal.cuh"
 #include "ra_ptx.cuh"
@@ -59,9 +63,9 @@ namespace ra {
 namespace {
 
 constexpr unsigned int kFull = 0xffffffffu;
-// A step whose P (normalised, <= 1) holds an entry above this also goes to
-// the tensor cores as hi + lo: one rounded bf16 P or dS then carries at most
-// 2^-8 / 16 of a row's weight (peaked attention on the plain path).
+// A plain step whose P (normalised, <= 1) holds an entry above this gets its
+// residual terms added in a second round: one rounded bf16 P or dS then
+// carries at most 2^-8 / 16 of a row's weight (peaked attention).
 constexpr float kPeakP = 1.0f / 16.0f;
 
 template <int D>
@@ -97,12 +101,12 @@ struct BwdCfg {
   static constexpr int bStgEmpty = bDqEmpty + 1;
   static constexpr int bDone = bStgEmpty + 1;
   static constexpr int bDrain = bDone + 1;
-  static constexpr int bVote = bDrain + 1;
-  static constexpr int kNumBars = bVote + 1;
+  static constexpr int bRound = bDrain + 1;  // the softmax warps finished round one
+  static constexpr int kNumBars = bRound + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
-  // per step parity and softmax warp: does the warp hold a P above kPeakP
-  static constexpr int kVoteOff = kMiscOff + 16;
-  static constexpr int kSmemBytes = kVoteOff + 2 * 8 * 4;
+  // misc: TMEM base, abort flag, and at +8 the "redo" word (a softmax warp
+  // met a P above kPeakP on a plain step: the unit takes a second round)
+  static constexpr int kSmemBytes = kMiscOff + 16;
   // Alignment slack for the 1024-byte aligned tiles: as much as the 227 KB
   // limit leaves (the kernel checks at run time that its base needs no more).
   static constexpr int kMaxSmem = 232448;
@@ -140,7 +144,7 @@ enum : unsigned int {
   kSiteBProdKV = 0x51, kSiteBProdQ = 0x52,
   kSiteBMmaKV = 0x61, kSiteBMmaQ = 0x62, kSiteBMmaP = 0x63, kSiteBMmaDs = 0x64, kSiteBMmaDq = 0x65,
   kSiteBMmaDo = 0x66,
-  kSiteBSmS = 0x71, kSiteBSmDp = 0x72, kSiteBSmDs = 0x73, kSiteBSmStg = 0x74, kSiteBSmVote = 0x75,
+  kSiteBSmS = 0x71, kSiteBSmDp = 0x72, kSiteBSmDs = 0x73, kSiteBSmStg = 0x74, kSiteBRound = 0x75,
   kSiteBDq = 0x81, kSiteBDone = 0x82, kSiteBProdDo = 0x53,
 };
 
@@ -277,57 +281,71 @@ __device__ __forceinline__ int doc_walk(const int32_t *c, int n_docs, int d, int
 // Next query tile of the unit, from the last down to the first visible one
 // (every key tile of a group starts on the same query tile).  `partial` marks
 // steps that need the element mask; `split` steps whose query tile has a row
-// seeing fewer than kSplitKeys keys.
-template <bool kDocs, bool kBlock>
+// seeing fewer than kSplitKeys keys.  In the second round of a marked unit
+// (kLo) only the steps the first round took plain come back, each marked
+// split: their residual terms are what the round adds.
+template <bool kDocs, bool kBlock, bool kLo = false>
 __device__ __forceinline__ bool q_next(const BwdParams &p, const KvUnit &x, QIter &it, int &i,
                                        int &a, int &hq, bool &partial, bool &split) {
   if constexpr (!kDocs) {
-    it.a = it.a == INT_MAX ? p.n_qtiles - 1 : it.a - 1;
-    if (it.a < x.a_lo) return false;
-    i = x.i;
-    a = it.a;
-    hq = x.hq;
-    partial = it.a < x.a_flo;
-    // a causal row at position t sees t + 1 keys of its sequence; a block
-    // step without the causal rule takes its key block's length as the bound
-    if constexpr (kBlock)
-      split = p.causal ? (__ldg(p.q_pos + it.a * kTile) + 1 < kSplitKeys) : (p.Lk < kSplitKeys);
-    else
-      split = p.causal ? (token_at(p.layout, p.L, p.N, x.i, it.a * kTile) + 1 < kSplitKeys)
-                       : (p.S < kSplitKeys);
-    return true;
+    for (;;) {
+      it.a = it.a == INT_MAX ? p.n_qtiles - 1 : it.a - 1;
+      if (it.a < x.a_lo) return false;
+      i = x.i;
+      a = it.a;
+      hq = x.hq;
+      partial = it.a < x.a_flo;
+      // a causal row at position t sees t + 1 keys of its sequence; a block
+      // step without the causal rule takes its key block's length as the bound
+      if constexpr (kBlock)
+        split = p.causal ? (__ldg(p.q_pos + it.a * kTile) + 1 < kSplitKeys) : (p.Lk < kSplitKeys);
+      else
+        split = p.causal ? (token_at(p.layout, p.L, p.N, x.i, it.a * kTile) + 1 < kSplitKeys)
+                         : (p.S < kSplitKeys);
+      if constexpr (!kLo) return true;
+      if (!split) {
+        split = true;
+        return true;
+      }
+    }
   }
   // The unit's query shard: its visible query tiles from the last down, and
   // for each the g query heads of the key tile's KV head.
-  if (it.a == INT_MAX) {
-    it.a = x.a_hi - 1;
-    it.hh = 0;
-    it.d0 = it.d1 = -1;
-  } else if (++it.hh >= p.g) {
-    it.hh = 0;
-    --it.a;
+  for (;;) {
+    if (it.a == INT_MAX) {
+      it.a = x.a_hi - 1;
+      it.hh = 0;
+      it.d0 = it.d1 = -1;
+    } else if (++it.hh >= p.g) {
+      it.hh = 0;
+      --it.a;
+    }
+    if (it.a < x.a_lo) return false;
+    it.i = x.i;
+    i = it.i;
+    a = it.a;
+    hq = x.kh * p.g + it.hh;
+    partial = it.a < x.a_flo || it.a >= x.a_fhi;
+    const int t0 = token_at(p.layout, p.L, p.N, it.i, it.a * kTile);
+    int minvis;
+    {
+      const int t1 = token_at(p.layout, p.L, p.N, it.i, min(it.a * kTile + kTile, p.L) - 1);
+      const int32_t *cb = p.cu + static_cast<size_t>(x.bb) * (p.n_docs + 1);
+      it.d0 = doc_walk(cb, p.n_docs, it.d0, t0);
+      it.d1 = doc_walk(cb, p.n_docs, it.d1, t1);
+      const int ds0 = cb[it.d0], de0 = cb[it.d0 + 1], ds1 = cb[it.d1], de1 = cb[it.d1 + 1];
+      if (p.causal)
+        minvis = ds1 > t0 ? 1 : t0 - ds0 + 1;  // a document starting inside: 1
+      else
+        minvis = de0 < ds1 ? 1 : min(de0 - ds0, de1 - ds1);
+    }
+    split = minvis < kSplitKeys;
+    if constexpr (!kLo) return true;
+    if (!split) {
+      split = true;
+      return true;
+    }
   }
-  if (it.a < x.a_lo) return false;
-  it.i = x.i;
-  i = it.i;
-  a = it.a;
-  hq = x.kh * p.g + it.hh;
-  partial = it.a < x.a_flo || it.a >= x.a_fhi;
-  const int t0 = token_at(p.layout, p.L, p.N, it.i, it.a * kTile);
-  int minvis;
-  {
-    const int t1 = token_at(p.layout, p.L, p.N, it.i, min(it.a * kTile + kTile, p.L) - 1);
-    const int32_t *cb = p.cu + static_cast<size_t>(x.bb) * (p.n_docs + 1);
-    it.d0 = doc_walk(cb, p.n_docs, it.d0, t0);
-    it.d1 = doc_walk(cb, p.n_docs, it.d1, t1);
-    const int ds0 = cb[it.d0], de0 = cb[it.d0 + 1], ds1 = cb[it.d1], de1 = cb[it.d1 + 1];
-    if (p.causal)
-      minvis = ds1 > t0 ? 1 : t0 - ds0 + 1;  // a document starting inside: 1
-    else
-      minvis = de0 < ds1 ? 1 : min(de0 - ds0, de1 - ds1);
-  }
-  split = minvis < kSplitKeys;
-  return true;
 }
 
 // D = A B^T style: both operands K-major 128 x D tiles (M = N = 128).
@@ -439,8 +457,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     mbar_init(&bars[C::bStgEmpty], 4);
     mbar_init(&bars[C::bDone], 1);
     mbar_init(&bars[C::bDrain], 1);
-    mbar_init(&bars[C::bVote], 8);
+    mbar_init(&bars[C::bRound], 8);
     *abort_flag = 0;
+    *reinterpret_cast<volatile int *>(smem + C::kMiscOff + 8) = 0;
     fence_barrier_init();
   }
   if (warp == C::kMmaWarp) {
@@ -451,6 +470,17 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
+
+  // Every role, after its first round over the unit, learns whether a
+  // softmax warp met a P above kPeakP on a plain step; the unit then takes a
+  // second round over those steps for their residual terms (warp-collective).
+  auto second_round = [&]() -> bool {
+    int r = 0;
+    if (lane == 0 && mbar_wait(&bars[C::bRound], 0, abort_flag, kSiteBRound))
+      r = *reinterpret_cast<volatile int *>(smem + C::kMiscOff + 8);
+    r = __shfl_sync(kFull, r, 0);
+    return r != 0 && *abort_flag == 0;
+  };
 
   if (warp >= C::kProducerWarp) {
     regs_set<C::kOtherRegs, C::kLaunchRegs>();
@@ -477,7 +507,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       QIter it;
       int i, a, hq, n = 0;
       bool partial, split;
-      while (q_next<kDocs, kBlock>(p, x, it, i, a, hq, partial, split)) {
+      // one step's loads: the Q tile with its rows' LSE2 and D, and dO
+      auto load_step = [&]() -> bool {
         if (lane == 0) {
           int c2, c3;
           map_coords(p.layout, p.L, p.N, i, a * kTile, c2, c3);
@@ -509,8 +540,16 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
           }
         }
         __syncwarp();
-        if (*abort_flag) break;
+        if (*abort_flag) return false;
         ++n;
+        return true;
+      };
+      while (q_next<kDocs, kBlock>(p, x, it, i, a, hq, partial, split))
+        if (!load_step()) break;
+      if (!*abort_flag && second_round()) {
+        QIter it2;
+        while (q_next<kDocs, kBlock, true>(p, x, it2, i, a, hq, partial, split))
+          if (!load_step()) break;
       }
       if (lane == 0 && *abort_flag) {
         // Let every copy this warp started land before the CTA unwinds.
@@ -534,28 +573,21 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         QIter it;
         int i, a, hq, n = 0;
         bool partial, split;
-        // S^T of the step after n, once its Q tile has landed
-        auto issue_next_s = [&](int n_cur) -> bool {
-          const int st1 = (n_cur + 1) % C::kQSt;
-          if (!mbar_wait(&bars[C::bQFull + st1], ((n_cur + 1) / C::kQSt) & 1, abort_flag,
-                         kSiteBMmaQ))
+        // S^T of step n_s into the S^T columns once its Q tile has landed
+        auto issue_s = [&](int n_s) -> bool {
+          const int st = n_s % C::kQSt;
+          if (!mbar_wait(&bars[C::bQFull + st], (n_s / C::kQSt) & 1, abort_flag, kSiteBMmaQ))
             return false;
           tc_fence_after();
-          mma_kk<D>(tmem + C::kColS, k_s, sbase + C::kQOff + st1 * C::kTileBytes, C::kIdescKK);
+          mma_kk<D>(tmem + C::kColS, k_s, sbase + C::kQOff + st * C::kTileBytes, C::kIdescKK);
           mma_commit(&bars[C::bSFull]);
           return true;
         };
         bool has = q_next<kDocs, kBlock>(p, x, it, i, a, hq, partial, split);
-        if (has && lane == 0) {
-          if (mbar_wait(&bars[C::bQFull + 0], 0, abort_flag, kSiteBMmaQ)) {
-            tc_fence_after();
-            mma_kk<D>(tmem + C::kColS, k_s, sbase + C::kQOff, C::kIdescKK);
-            mma_commit(&bars[C::bSFull]);
-          }
-        }
+        if (has && lane == 0) issue_s(0);
         __syncwarp();
         while (has && !*abort_flag) {
-          bool cur_split = split;
+          const bool cur_split = split;
           const bool has_next = q_next<kDocs, kBlock>(p, x, it, i, a, hq, partial, split);
           if (lane == 0) {
             const int st = n % C::kQSt;
@@ -570,22 +602,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
               mma_commit(&bars[C::bDpFull]);
               go = mbar_wait(&bars[C::bPReady], n & 1, abort_flag, kSiteBMmaP);
             }
-            // a step with a peaked P (some softmax warp's vote, written
-            // before it arrived on bPReady) also takes the hi + lo path; its
-            // residual MMA for dV waits for the dS phase, where the warps
-            // without a peaked P write zero residuals, and the next S^T
-            // (which overwrites P) waits with it
-            bool dyn = false;
             if (go) {
               tc_fence_after();
-              if (!cur_split) {
-                const volatile uint32_t *vote =
-                    reinterpret_cast<const volatile uint32_t *>(smem + C::kVoteOff) + (n & 1) * 8;
-                uint32_t any = 0u;
-#pragma unroll
-                for (int w = 0; w < 8; ++w) any |= vote[w];
-                dyn = any != 0u;
-              }
               // dV += P_hi^T dO (+ P_lo^T dO): A from TMEM (bf16 pairs), B = dO MN-major
 #pragma unroll
               for (int kk = 0; kk < kTile / 16; ++kk)
@@ -598,26 +616,23 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                   mma_ts(tmem + C::kColDv, tmem + C::kColS + (kk >> 2) * 64 + 32 + (kk & 3) * 8,
                          smem_desc_sw128(do_s + kk * 16 * 128, kTile * 128, 1024), C::kIdescDv,
                          1u);
-              if (!dyn) {
-                mma_commit(&bars[C::bDoEmpty]);
-                if (has_next) go = issue_next_s(n);
+              mma_commit(&bars[C::bDoEmpty]);
+              if (has_next) {
+                const int st1 = (n + 1) % C::kQSt;
+                go = mbar_wait(&bars[C::bQFull + st1], ((n + 1) / C::kQSt) & 1, abort_flag,
+                               kSiteBMmaQ);
+                if (go) {
+                  tc_fence_after();
+                  mma_kk<D>(tmem + C::kColS, k_s, sbase + C::kQOff + st1 * C::kTileBytes,
+                            C::kIdescKK);
+                  mma_commit(&bars[C::bSFull]);
+                }
               }
             }
             if (go) go = mbar_wait(&bars[C::bDsReady], n & 1, abort_flag, kSiteBMmaDs);
             if (go) {
               tc_fence_after();
-              if (dyn) {
-#pragma unroll
-                for (int kk = 0; kk < kTile / 16; ++kk)
-                  mma_ts(tmem + C::kColDv, tmem + C::kColS + (kk >> 2) * 64 + 32 + (kk & 3) * 8,
-                         smem_desc_sw128(do_s + kk * 16 * 128, kTile * 128, 1024), C::kIdescDv,
-                         1u);
-                mma_commit(&bars[C::bDoEmpty]);
-                if (has_next) go = issue_next_s(n);
-              }
-            }
-            if (go) {
-              if (!(cur_split || dyn)) {
+              if (!cur_split) {
                 // dQ first, so the drain (and with it the next dP^T) starts
                 // while dK accumulates
                 issue_dq<D>(tmem + C::kColDp, ds_s, k_s);
@@ -639,6 +654,51 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
           __syncwarp();
           ++n;
           has = has_next;
+        }
+        // Second round of a marked unit: the plain steps again, adding only
+        // their residual terms (every accumulator keeps adding).
+        if (!*abort_flag && second_round()) {
+          QIter it2;
+          has = q_next<kDocs, kBlock, true>(p, x, it2, i, a, hq, partial, split);
+          if (has && lane == 0) issue_s(n);
+          __syncwarp();
+          while (has && !*abort_flag) {
+            const bool has_next = q_next<kDocs, kBlock, true>(p, x, it2, i, a, hq, partial, split);
+            if (lane == 0) {
+              const int st = n % C::kQSt;
+              const uint32_t q_s = sbase + C::kQOff + st * C::kTileBytes;
+              bool go = mbar_wait(&bars[C::bDqEmpty], (n - 1) & 1, abort_flag, kSiteBMmaDq);
+              if (go) go = mbar_wait(&bars[C::bDoFull], n & 1, abort_flag, kSiteBMmaDo);
+              if (go) {
+                tc_fence_after();
+                mma_kk<D>(tmem + C::kColDp, v_s, do_s, C::kIdescKK);
+                mma_commit(&bars[C::bDpFull]);
+                go = mbar_wait(&bars[C::bPReady], n & 1, abort_flag, kSiteBMmaP);
+              }
+              if (go) {
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < kTile / 16; ++kk)
+                  mma_ts(tmem + C::kColDv, tmem + C::kColS + (kk >> 2) * 64 + 32 + (kk & 3) * 8,
+                         smem_desc_sw128(do_s + kk * 16 * 128, kTile * 128, 1024), C::kIdescDv,
+                         1u);
+                mma_commit(&bars[C::bDoEmpty]);
+                if (has_next) go = issue_s(n + 1);
+              }
+              if (go) go = mbar_wait(&bars[C::bDsReady], n & 1, abort_flag, kSiteBMmaDs);
+              if (go) {
+                tc_fence_after();
+                issue_dk<D>(tmem + C::kColDk, dslo_s, q_s, true);
+                issue_dq<D>(tmem + C::kColDp, dslo_s, k_s);
+                mma_commit(&bars[C::bDqFull]);
+                mma_commit(&bars[C::bDsEmpty]);
+                mma_commit(&bars[C::bQEmpty + st]);
+              }
+            }
+            __syncwarp();
+            ++n;
+            has = has_next;
+          }
         }
         if (lane == 0) mma_commit(&bars[C::bDone]);
       }
@@ -682,7 +742,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     QIter it;
     int i, a, hq, n = 0;
     bool partial, split;
-    while (q_next<kDocs, kBlock>(p, x, it, i, a, hq, partial, split)) {
+    // one step; the second round of a marked unit (kLoRound) detects nothing
+    auto sm_step = [&](auto lo_tag) -> bool {
+      constexpr bool kLoRound = decltype(lo_tag)::value;
       // this step's LSE2 and D rows, staged by the producer with the Q tile
       const float4 *lse4 = reinterpret_cast<const float4 *>(
                                smem + C::kStatOff + (n % C::kQSt) * 2 * C::kRowStatBytes) +
@@ -701,7 +763,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         c0 = C::kHalfCols;
         partial = true;
       }
-      if (!__all_sync(kFull, mbar_wait(&bars[C::bSFull], n & 1, abort_flag, kSiteBSmS))) break;
+      if (!__all_sync(kFull, mbar_wait(&bars[C::bSFull], n & 1, abort_flag, kSiteBSmS))) return false;
       tc_fence_after();
       float pf[C::kHalfCols];  // this warpgroup's half of the P^T row, fp32
       {
@@ -735,23 +797,16 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         for (int c = 0; c < C::kHalfCols; ++c)
           if (c < c0 || (kDocs && c >= c1)) pf[c] = 0.f;
       }
-      // Vote: does this warp hold a P above kPeakP?  Any vote sends the step
-      // through hi + lo (the MMA issuer and the dS phase read the votes); a
-      // warp that voted stores its P residual now, the others store zeros
-      // in the dS phase if the step turns out split.
-      bool peaked = false;
-      if (!split) {
+      // A P above kPeakP on a plain step: the unit takes a second round
+      // for the residual terms of its plain steps.
+      if (!kLoRound && !split) {
         float pm = 0.f;
 #pragma unroll
         for (int c = 0; c < C::kHalfCols; c += 2) pm = fmax3(pm, pf[c], pf[c + 1]);
-        peaked = __any_sync(kFull, pm > kPeakP);
+        if (__any_sync(kFull, pm > kPeakP) && lane == 0)
+          *reinterpret_cast<volatile int *>(smem + C::kMiscOff + 8) = 1;
       }
-      if (lane == 0) {
-        reinterpret_cast<volatile uint32_t *>(smem + C::kVoteOff)[(n & 1) * 8 + warp] =
-            peaked ? 1u : 0u;
-        mbar_arrive(&bars[C::bVote]);
-      }
-      if (split || peaked)
+      if (split)
         store_p_half<true>(pf, tS, cb);
       else
         store_p_half<false>(pf, tS, cb);
@@ -762,33 +817,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
 
       bool go = mbar_wait(&bars[C::bDpFull], n & 1, abort_flag, kSiteBSmDp);
       if (go) go = mbar_wait(&bars[C::bDsEmpty], (n & 1) ^ 1, abort_flag, kSiteBSmDs);
-      // every softmax warp's vote for this step is in
-      bool step_split = split;
-      if (go && !split) {
-        go = mbar_wait(&bars[C::bVote], n & 1, abort_flag, kSiteBSmVote);
-        if (go) {
-          const volatile uint32_t *vote =
-              reinterpret_cast<const volatile uint32_t *>(smem + C::kVoteOff) + (n & 1) * 8;
-          uint32_t any = 0u;
-#pragma unroll
-          for (int w = 0; w < 8; ++w) any |= vote[w];
-          step_split = any != 0u;
-        }
-      }
-      // switched to hi + lo by another warp's vote: this warp's P residual
-      // columns get zeros (its P entries are all below kPeakP).  The MMA
-      // issuer reads them after bDsReady and only then issues the next S^T.
-      const bool zero_lo = go && step_split && !split && !peaked;
-      if (__any_sync(kFull, zero_lo)) {
-        uint32_t z[32];
-#pragma unroll
-        for (int e = 0; e < 32; ++e) z[e] = 0u;
-        tmem_st32(tS + cb + 32, z);
-      }
       // the residual goes to the staging buffer once the drain is done with it
-      if (go && step_split && n > 0)
+      if (go && split && n > 0)
         go = mbar_wait(&bars[C::bStgEmpty], (n - 1) & 1, abort_flag, kSiteBSmStg);
-      if (!__all_sync(kFull, go)) break;
+      if (!__all_sync(kFull, go)) return false;
       tc_fence_after();
       // all 64 dP^T columns of this half in one round of loads; dS = P (dP - D)
       // on f32x2 pairs
@@ -820,7 +852,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
           *reinterpret_cast<uint4 *>(ds_row + chunk * 16) =
               make_uint4(whi[u * 4 + 0], whi[u * 4 + 1], whi[u * 4 + 2], whi[u * 4 + 3]);
         }
-        if (step_split) {
+        if (split) {
           uint32_t wlo[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e)
@@ -834,12 +866,21 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
           }
         }
       }
-      if (zero_lo) tmem_st_wait();
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[C::bDsReady]);
       ++n;
+      return true;
+    };
+    while (q_next<kDocs, kBlock>(p, x, it, i, a, hq, partial, split))
+      if (!sm_step(std::false_type{})) break;
+    // round one is over for this warp (and its detections are written)
+    if (lane == 0) mbar_arrive(&bars[C::bRound]);
+    if (!*abort_flag && second_round()) {
+      QIter it2;
+      while (q_next<kDocs, kBlock, true>(p, x, it2, i, a, hq, partial, split))
+        if (!sm_step(std::true_type{})) break;
     }
   } else if (warp < C::kDrainWarp0 + 4) {
     regs_set<C::kDrainRegs, C::kLaunchRegs>();
@@ -851,10 +892,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     int i, a, hq, n = 0;
     bool partial, split;
     bool aborted = false;
-    while (q_next<kDocs, kBlock>(p, x, it, i, a, hq, partial, split)) {
+    // one step's dQ partial: TMEM -> registers -> staging -> bulk reduce-add
+    auto drain_step = [&]() -> bool {
       if (!__all_sync(kFull, mbar_wait(&bars[C::bDqFull], n & 1, abort_flag, kSiteBDq))) {
         aborted = true;
-        break;
+        return false;
       }
       tc_fence_after();
       {
@@ -907,6 +949,14 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         __syncwarp();
       }
       ++n;
+      return true;
+    };
+    while (q_next<kDocs, kBlock>(p, x, it, i, a, hq, partial, split))
+      if (!drain_step()) break;
+    if (!aborted && second_round()) {
+      QIter it2;
+      while (q_next<kDocs, kBlock, true>(p, x, it2, i, a, hq, partial, split))
+        if (!drain_step()) break;
     }
     if (lane == 0) bulk_wait_group0<false>();  // this warp's reductions complete
     // dK, dV of this unit, added into dk and dv (other units of the tile add
