@@ -61,7 +61,7 @@
  *    with fp32 accumulation.  Where that rounding could carry a large share
  *    of a result it goes as a bf16 pair hi + lo (the second term the
  *    rounding residual): in query tiles whose earliest row sees fewer than
- *    4096 keys, and in the backward on steps whose P holds an entry above
+ *    512 keys, and in the backward on steps whose P holds an entry above
  *    1/16.  The forward re-references a row's exponent shift to the exact
  *    row max when a key would hold more than 1/9 of the row's weight so far,
  *    so that key's P is exactly 1.
@@ -161,7 +161,7 @@ ra_status ra_ring_attention(const uint16_t *q, const uint16_t *k, const uint16_t
  *   cu_seqlens: device int32 [b][n_docs + 1], document offsets of each batch
  *   row, from 0 to S, non-decreasing (empty documents allowed); the contents
  *   are not checked on the host.  n_docs >= 1.
- * Precision: query tiles with a row that sees fewer than 4096 keys (a row
+ * Precision: query tiles with a row that sees fewer than 512 keys (a row
  * near the start of a document) take the hi + lo bf16 path. */
 ra_status ra_ring_attention_packed(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                                    float *out, float *lse, int64_t S, int n_shards,
@@ -249,7 +249,7 @@ size_t ra_block_bwd_workspace_size(int64_t Lq, ra_dims dims);
  *   workspace: device memory of at least ra_block_bwd_workspace_size(Lq)
  *     bytes, scratch (D and LSE are recomputed by every call).
  * Precision as in ra_ring_attention_bwd: query tiles whose earliest row sees
- * fewer than 4096 keys (without the causal rule: Lk < 4096) and steps whose
+ * fewer than 512 keys (without the causal rule: Lk < 512) and steps whose
  * P holds an entry above 1/16 go to the tensor cores as bf16 hi + lo pairs.
  * Lq or Lk == 0 is a no-op.  Positions that do not increase give undefined
  * gradients (they are not checked). */

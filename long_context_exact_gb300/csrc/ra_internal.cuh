@@ -18,9 +18,12 @@ constexpr float kLn2 = 0.6931471805599453f;
 // Rows that see fewer keys than this put large weights on single keys, so
 // their P (and dS) go to the tensor cores as a bf16 pair hi + lo instead of
 // one bf16 value: a bf16 operand keeps 8 significant bits, and on such rows
-// the dropped 2^-9 of each weight alone approaches the 1e-2 parity budget.
-// Longer rows spread the weights and keep plain bf16.
-constexpr int kSplitKeys = 4096;
+// the dropped 2^-9 of each weight alone approaches the 1e-2 parity budget
+// (a row with two keys: dQ off by up to 1.3e-2 in a model of the rounding,
+// 2e-3 at 256 keys, 1.6e-3 at 512).  Longer rows spread the weights and keep
+// plain bf16; a longer row that still puts a large weight on a few keys is
+// caught by the peaked-P rules of the forward and backward kernels.
+constexpr int kSplitKeys = 512;
 
 // Causal block steps: one CTA classifies its whole key range once (keep and
 // mask bits in shared memory), so a range holds at most this many key tiles
@@ -176,6 +179,9 @@ struct BwdParams {
   // block of Lk rows, token positions from q_pos / k_pos (increasing)
   int block;
   int Lk;
+  // unpacked ring: each unit meets qgroup consecutive query shards (n_groups
+  // groups of them), so that short shards still make long units
+  int qgroup, n_groups;
   const int32_t *q_pos;     // [L]
   const int32_t *k_pos;     // [Lk]
   int layout, causal;

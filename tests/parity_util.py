@@ -5,7 +5,7 @@ computed on several cores, and inputs whose attention is sharply peaked.
 Test infrastructure only (it calls the oracle; the product never imports it).
 
 Precision rule of the library (stated in ra.h): a query tile whose earliest
-row sees fewer than 4096 keys sends P (and dS) to the tensor cores as a bf16
+row sees fewer than 512 keys sends P (and dS) to the tensor cores as a bf16
 pair hi + lo; every other tile rounds them once to bf16.  On the ring a row
 at position t sees t + 1 keys under the causal rule and all S otherwise, so
 for full-size workloads nearly all of the work is on the plain path and the
@@ -19,7 +19,7 @@ import threading
 
 import numpy as np
 
-SPLIT_KEYS = 4096   # the library's hi + lo threshold (keys seen by a tile's earliest row)
+SPLIT_KEYS = 512    # the library's hi + lo threshold (keys seen by a tile's earliest row)
 TILE = 128          # query rows per tile
 
 # Measured errors per test, written out at the end of the session when

@@ -96,7 +96,7 @@ def test_backward_custom_scale(orc):
 
 PLAIN_CASES = [
     # b, S, h, n_kv, d, N, layout, causal -- most query tiles (every one when
-    # not causal) see 4096 keys or more, so the plain bf16 P / dS path
+    # not causal) see 512 keys or more, so the plain bf16 P / dS path
     # carries most of the work, against full dO on every row
     (1, 8192, 8, 2, 128, 4, STRIPED, True),
     (1, 8192, 8, 2, 128, 4, CONTIGUOUS, True),

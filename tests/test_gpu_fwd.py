@@ -329,7 +329,7 @@ def test_block_steps_over_ring_reproduce_full_attention(orc, layout):
 @pytest.mark.parametrize("Lq,Lk,causal,g,d,splits", [
     (256, 4096, True, 4, 128, 0), (256, 4096, True, 4, 128, 1), (256, 4096, True, 4, 128, 5),
     (200, 1000, True, 2, 64, 3), (128, 2048, False, 1, 128, 0), (384, 640, True, 3, 128, 64),
-    # splits of >= 4096 visible keys per row take the plain bf16 P path
+    # splits of >= 512 visible keys per row take the plain bf16 P path
     (256, 16384, True, 4, 128, 2), (128, 12288, False, 2, 64, 0),
 ])
 def test_chunked_prefill_matches_oracle(orc, Lq, Lk, causal, g, d, splits):
