@@ -32,11 +32,14 @@ if ROOT not in sys.path:
 METRIC = "useful attention TFLOP/s fwd & bwd (causal, S=256K GQA) and % of BF16 tensor peak"
 WORKLOAD = "causal256k"
 
-# Per-launch DRAM traffic of the dominant kernels from one ncu capture
-# (dram__bytes_read.sum + dram__bytes_write.sum), valid only while the
-# kernel source hash matches the one the capture was taken with.
+# Per-launch DRAM traffic of the dominant kernel (dram__bytes_read.sum +
+# dram__bytes_write.sum), valid only while the kernel source hash matches
+# the one the capture was taken with.  Captured on the one-shard 32K case
+# (5.19 GB) and scaled to this workload: the compulsory 2.3 GB with S (x 8),
+# the rest with the causal step count (x 64).
 TRAFFIC = {
-    "bwd": {"bytes_per_launch": 118850519552 + 81280138496, "src_sha": "190094a2c1db44a2"},
+    "bwd": {"bytes_per_launch": 204e9, "src_sha": "4ac805f625d439fb",
+            "method": "ncu on the causal32k1 case (5.19 GB), scaled: 2.3 GB x 8 + 2.89 GB x 64"},
 }
 
 
@@ -630,6 +633,7 @@ def run_ours(a, rank, world, local_rank):
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_sustained"],
                 "unit": "TFLOP/s", "frac": achieved / peaks["bf16_sustained"],
                 "traffic": traffic, "kernel": dom,
+                "traffic_note": tr["method"] if tr and traffic is not None else None,
                 "peak_note": f"{peaks['source']} bf16 sustained; frac of burst "
                              f"{achieved / peaks['bf16']:.3f}"}
 

@@ -190,9 +190,14 @@ ra_status ra_ring_attention_packed_bwd(const uint16_t *q, const uint16_t *k, con
  *   when n_splits leaves more; 0 picks enough).
  *   workspace: device memory of ra_prefill_workspace_size() bytes (same
  *   n_splits), 16-byte aligned, scratch after the call.
- * Launches three kernels on `stream`; RA_ERR_WORKSPACE if the workspace is
- * missing or small.  The pages give no kernel for this case; splitting the
- * keys is this library's way to fill the GPU when Lq is short. */
+ * Under the causal rule the key tiles that every row of a 128-query tile sees
+ * in full (all keys at or before the tile's earliest query position) run
+ * without the causal mask, and then only the remaining tiles with it, merged
+ * into the same split states; the results do not depend on this.
+ * Launches three kernels on `stream` (five under the causal rule);
+ * RA_ERR_WORKSPACE if the workspace is missing or small.  The pages give no
+ * kernel for this case; splitting the keys is this library's way to fill
+ * the GPU when Lq is short. */
 size_t ra_prefill_workspace_size(int64_t Lq, int64_t Lk, int n_splits, ra_dims dims);
 ra_status ra_chunked_prefill(const uint16_t *q, const uint16_t *k, const uint16_t *v, float *out,
                              float *lse, const int32_t *q_pos, const int32_t *k_pos, int64_t Lq,

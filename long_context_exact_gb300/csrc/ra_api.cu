@@ -349,13 +349,22 @@ ra_status ra_merge(const float *o_a, const float *lse_a, const float *o_b, const
   return e == cudaSuccess ? RA_OK : cuda_fail(e, "merge launch");
 }
 
+// ints of the per-query-tile array in the prefill workspace (16-byte padded)
+static inline int64_t p_qtiles_rounded(int64_t Lq) { return ((Lq + kTile - 1) / kTile + 3) / 4 * 4; }
+
 size_t ra_prefill_workspace_size(int64_t Lq, int64_t Lk, int n_splits, ra_dims dims) {
   if (Lq <= 0 || Lk <= 0 || dims.b <= 0 || dims.h <= 0 || dims.n_kv <= 0 ||
       dims.h % dims.n_kv != 0 || dims.d <= 0 || Lq >= (1LL << 31) || Lk >= (1LL << 31))
     return 0;
   const int s = resolve_splits(Lq, Lk, n_splits, dims);
   const size_t rows = static_cast<size_t>(dims.b) * dims.h * static_cast<size_t>(Lq);
-  return static_cast<size_t>(s) * rows * (2 + static_cast<size_t>(dims.d)) * sizeof(float);
+  // states of the s key splits, then one int per query tile (a causal
+  // prefill's split point between its two passes) and one per key tile (the
+  // tile's largest key position)
+  const size_t n_qtiles = static_cast<size_t>((Lq + kTile - 1) / kTile);
+  const size_t n_ktiles = static_cast<size_t>((Lk + kTile - 1) / kTile);
+  return static_cast<size_t>(s) * rows * (2 + static_cast<size_t>(dims.d)) * sizeof(float) +
+         (n_qtiles * sizeof(int32_t) + 15) / 16 * 16 + (n_ktiles * sizeof(int32_t) + 15) / 16 * 16;
 }
 
 ra_status ra_chunked_prefill(const uint16_t *q, const uint16_t *k, const uint16_t *v, float *out,
@@ -406,6 +415,8 @@ ra_status ra_chunked_prefill(const uint16_t *q, const uint16_t *k, const uint16_
   float *m = static_cast<float *>(workspace);
   float *l = m + static_cast<size_t>(splits) * rows;
   float *o = l + static_cast<size_t>(splits) * rows;
+  int32_t *kt_end = reinterpret_cast<int32_t *>(o + static_cast<size_t>(splits) * rows * dims.d);
+  int32_t *kmax = kt_end + (p_qtiles_rounded(Lq));
   FwdParams p{};
   p.b = dims.b;
   p.h = dims.h;
@@ -430,6 +441,21 @@ ra_status ra_chunked_prefill(const uint16_t *q, const uint16_t *k, const uint16_
   cudaError_t e = counted(launch_state_init(m, l, o, static_cast<long long>(splits) * rows,
                                             dims.d, cs));
   if (e != cudaSuccess) return cuda_fail(e, "state init");
+  if (causal) {
+    // The key tiles every row of a query tile sees in full (for the usual
+    // prefill, all but the last few) go through the block kernel without the
+    // causal rule, which runs them ~25 % faster; then the rest through the
+    // causal one, whose block steps merge into the same split states.
+    e = counted(launch_prefill_visible(q_pos, k_pos, Lq, Lk, kmax, kt_end, cs), 2);
+    if (e != cudaSuccess) return cuda_fail(e, "prefill pre-pass");
+    FwdParams pv = p;
+    pv.causal = 0;
+    pv.q_pos = nullptr;
+    pv.k_pos = nullptr;
+    pv.kt_end = kt_end;
+    if ((st = launch_attention(pv, dims.d, q, k, v, Lq, Lk, cs)) != RA_OK) return st;
+    p.kt_begin = kt_end;
+  }
   if ((st = launch_attention(p, dims.d, q, k, v, Lq, Lk, cs)) != RA_OK) return st;
   e = counted(launch_combine(m, l, o, splits, out, lse, dims.b, Lq, dims.h, dims.d, cs));
   return e == cudaSuccess ? RA_OK : cuda_fail(e, "combine launch");
@@ -560,12 +586,16 @@ ra_status ra_ring_attention_packed_bwd(const uint16_t *q, const uint16_t *k, con
   if ((st = make_dq_map(&dqm, dq, layout, dims.b, n_shards, p.L, dims.h, dims.d)) != RA_OK) return st;
   if ((st = make_dq_map(&dkm, dk, layout, dims.b, n_shards, p.L, dims.n_kv, dims.d)) != RA_OK) return st;
   if ((st = make_dq_map(&dvm, dv, layout, dims.b, n_shards, p.L, dims.n_kv, dims.d)) != RA_OK) return st;
-  // one unit per (key tile, query shard, query head); packed documents: one
-  // per (key tile, query shard), the KV head's query heads inside
+  // one unit per (key tile, group of query shards, query head), the group
+  // covering ~32K query rows (one shard when shards are that long); packed
+  // documents: one per (key tile, query shard), the KV head's query heads
+  // inside
+  p.qgroup = cu_seqlens != nullptr ? 1 : std::max(1, std::min(n_shards, 32768 / p.Lpad));
+  p.n_groups = (n_shards + p.qgroup - 1) / p.qgroup;
   const long long n_units =
       cu_seqlens != nullptr
           ? static_cast<long long>(dims.b) * dims.n_kv * n_shards * n_shards * p.n_ktiles
-          : static_cast<long long>(dims.b) * dims.h * n_shards * n_shards * p.n_ktiles;
+          : static_cast<long long>(dims.b) * dims.h * n_shards * p.n_groups * p.n_ktiles;
   if (n_units > 0x7fffffffLL) return fail(RA_ERR_UNSUPPORTED, "too many work units (%lld)", n_units);
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaMemsetAsync(dq, 0, static_cast<size_t>(dims.b) * S * dims.h * dims.d * 4, cs);
@@ -632,6 +662,8 @@ ra_status ra_block_step_bwd(const uint16_t *q, const uint16_t *k, const uint16_t
   p.Lpad = p.n_qtiles * kTile;
   p.block = 1;
   p.Lk = static_cast<int>(Lk);
+  p.qgroup = 1;
+  p.n_groups = 1;
   p.q_pos = causal ? q_pos : nullptr;
   p.k_pos = causal ? k_pos : nullptr;
   const size_t rows = static_cast<size_t>(dims.b) * dims.h * p.Lpad;

@@ -150,7 +150,8 @@ enum : unsigned int {
 
 struct KvUnit {
   int bb, kh, j, c;   // batch, kv head, kv shard, kv tile
-  int i, hq;          // the query shard it meets; unpacked: and the query head
+  int i, hq;          // the (first) query shard it meets; unpacked: and the query head
+  int g_cnt;          // unpacked: query shards i .. i + g_cnt - 1 in turn
   int kmin, kmax;     // token positions of the tile's first and last existing key
   int a_lo, a_hi;     // query tiles [a_lo, a_hi) of shard i see a key of the tile
   int a_flo;          // query tiles a >= a_flo see every key of the tile (no mask) ...
@@ -158,12 +159,14 @@ struct KvUnit {
   int ds0, de0, ds1, de1;  // packed: documents of the first and last key
 };
 
-// Units (unpacked): one 128-key tile against one query shard and one query
-// head of its group; dK and dV of the tile are summed over its units with
-// reductions.  Units run grouped by (batch, kv head, query shard, query head)
-// with the key tiles innermost, so the CTAs resident together read the same
-// Q / dO tiles and add their dQ partials into the same 64 KB dq tiles: one
-// group's dq rows (n_qtiles x 64 KB) stay in L2 while every key tile adds
+// Units (unpacked): one 128-key tile against a group of qgroup consecutive
+// query shards (one shard when shards are long; enough of them to make
+// ~32K query rows when they are short) and one query head of its KV group;
+// dK and dV of the tile are summed over its units with reductions.  Units
+// run grouped by (batch, kv head, shard group, query head) with the key
+// tiles innermost, so the CTAs resident together read the same Q / dO
+// tiles and add their dQ partials into the same 64 KB dq tiles: one group's
+// dq rows (~32K rows x 512 B = 16 MB) stay in L2 while every key tile adds
 // to them.
 // Units (packed documents): one 128-key tile against one query shard, with
 // the g query heads of its KV head inside the unit (a tile sees only its own
@@ -183,7 +186,27 @@ __device__ __forceinline__ int lower_bound_pos(const int32_t *pos, int n, int v)
   return lo;
 }
 
-template <bool kDocs, bool kBlock>
+// Unpacked: the query tiles [lo, n_qtiles) of shard i see a key of the unit's
+// key tile (positions kmin .. kmax), and those at or after flo see all of it.
+template <bool kBlock>
+__device__ __forceinline__ void shard_bounds(const BwdParams &p, int kmin, int kmax, int i,
+                                             int &lo, int &flo) {
+  if (!p.causal) {
+    lo = 0;
+    flo = 0;
+    return;
+  }
+  // visible query tiles: those whose last row sees the tile's first key
+  const int r_vis = kBlock ? lower_bound_pos(p.q_pos, p.L, kmin)
+                           : max(0, first_row_at_or_after(p.layout, p.L, p.N, i, kmin));
+  lo = r_vis >= p.L ? p.n_qtiles : r_vis / kTile;
+  // unmasked query tiles: every row sees the tile's last key
+  const int r_full = kBlock ? lower_bound_pos(p.q_pos, p.L, kmax)
+                            : max(0, first_row_at_or_after(p.layout, p.L, p.N, i, kmax));
+  flo = min(p.n_qtiles, (r_full + kTile - 1) / kTile);
+}
+
+template <bool kDocs, bool kBlock, bool kGroup>
 __device__ __forceinline__ KvUnit decode_kv_unit(const BwdParams &p, long long u) {
   KvUnit x;
   x.c = static_cast<int>(u % p.n_ktiles);
@@ -193,13 +216,15 @@ __device__ __forceinline__ KvUnit decode_kv_unit(const BwdParams &p, long long u
   if constexpr (!kDocs) {
     const int hh = static_cast<int>(g % p.g);
     g /= p.g;
-    x.i = static_cast<int>(g % p.N);
-    g /= p.N;
+    x.i = static_cast<int>(g % p.n_groups) * p.qgroup;
+    x.g_cnt = min(p.qgroup, p.N - x.i);
+    g /= p.n_groups;
     x.kh = static_cast<int>(g % p.n_kv);
     x.bb = static_cast<int>(g / p.n_kv);
     x.hq = x.kh * p.g + hh;
   } else {
     x.i = static_cast<int>(g % p.N);
+    x.g_cnt = 1;
     g /= p.N;
     x.kh = static_cast<int>(g % p.n_kv);
     x.bb = static_cast<int>(g / p.n_kv);
@@ -218,18 +243,17 @@ __device__ __forceinline__ KvUnit decode_kv_unit(const BwdParams &p, long long u
   x.a_fhi = p.n_qtiles;
   if constexpr (!kDocs) {
     x.a_hi = p.n_qtiles;
-    if (!p.causal) {
-      x.a_lo = 0;
+    if constexpr (kGroup) {
+      // the unit has work if some shard of its group sees the key tile
+      x.a_lo = p.n_qtiles;
       x.a_flo = 0;
+      for (int gi = 0; gi < x.g_cnt; ++gi) {
+        int lo, flo;
+        shard_bounds<kBlock>(p, x.kmin, x.kmax, x.i + gi, lo, flo);
+        x.a_lo = min(x.a_lo, lo);
+      }
     } else {
-      // visible query tiles: those whose last row sees the tile's first key
-      const int r_vis = kBlock ? lower_bound_pos(p.q_pos, p.L, x.kmin)
-                               : max(0, first_row_at_or_after(p.layout, p.L, p.N, x.i, x.kmin));
-      x.a_lo = r_vis >= p.L ? p.n_qtiles : r_vis / kTile;
-      // unmasked query tiles: every row sees the tile's last key
-      const int r_full = kBlock ? lower_bound_pos(p.q_pos, p.L, x.kmax)
-                                : max(0, first_row_at_or_after(p.layout, p.L, p.N, x.i, x.kmax));
-      x.a_flo = min(p.n_qtiles, (r_full + kTile - 1) / kTile);
+      shard_bounds<kBlock>(p, x.kmin, x.kmax, x.i, x.a_lo, x.a_flo);
     }
   } else {
     // A query at t sees key kp iff kp lies in t's document [ds, de) and,
@@ -254,6 +278,10 @@ __device__ __forceinline__ KvUnit decode_kv_unit(const BwdParams &p, long long u
 
 struct QIter {
   int a = INT_MAX;
+  // unpacked: the current shard of the unit's group and its visible and
+  // unmasked query-tile bounds
+  int gi = -1, lo = 0, flo = 0;
+  bool done = false;
   // packed documents: the query shard, query head, and the documents of the
   // current tile's first and last rows
   int i = 0, hh = 0;
@@ -284,10 +312,11 @@ __device__ __forceinline__ int doc_walk(const int32_t *c, int n_docs, int d, int
 // seeing fewer than kSplitKeys keys.  In the second round of a marked unit
 // (kLo) only the steps the first round took plain come back, each marked
 // split: their residual terms are what the round adds.
-template <bool kDocs, bool kBlock, bool kLo = false>
+template <bool kDocs, bool kBlock, bool kGroup, bool kLo = false>
 __device__ __forceinline__ bool q_next(const BwdParams &p, const KvUnit &x, QIter &it, int &i,
                                        int &a, int &hq, bool &partial, bool &split) {
-  if constexpr (!kDocs) {
+  if constexpr (!kDocs && !kGroup) {
+    // one query shard: its visible tiles from the last down
     for (;;) {
       it.a = it.a == INT_MAX ? p.n_qtiles - 1 : it.a - 1;
       if (it.a < x.a_lo) return false;
@@ -295,12 +324,51 @@ __device__ __forceinline__ bool q_next(const BwdParams &p, const KvUnit &x, QIte
       a = it.a;
       hq = x.hq;
       partial = it.a < x.a_flo;
+      if constexpr (kBlock)
+        split = p.causal ? (__ldg(p.q_pos + it.a * kTile) + 1 < kSplitKeys) : (p.Lk < kSplitKeys);
+      else
+        split = p.causal ? (token_at(p.layout, p.L, p.N, x.i, it.a * kTile) + 1 < kSplitKeys)
+                         : (p.S < kSplitKeys);
+      if constexpr (!kLo) return true;
+      if (!split) {
+        split = true;
+        return true;
+      }
+    }
+  }
+  if constexpr (!kDocs && kGroup) {
+    // the shards of the unit's group in turn, each from its last visible tile
+    for (;;) {
+      if (it.done) return false;
+      if (it.a == INT_MAX || it.a - 1 < it.lo) {
+        // the next shard of the group with a visible tile, from its last tile
+        int gi = it.a == INT_MAX ? 0 : it.gi + 1;
+        int lo = 0, flo = 0;
+        for (; gi < x.g_cnt; ++gi) {
+          shard_bounds<kBlock>(p, x.kmin, x.kmax, x.i + gi, lo, flo);
+          if (lo < p.n_qtiles) break;
+        }
+        if (gi >= x.g_cnt) {
+          it.done = true;
+          return false;
+        }
+        it.gi = gi;
+        it.lo = lo;
+        it.flo = flo;
+        it.a = p.n_qtiles - 1;
+      } else {
+        --it.a;
+      }
+      i = x.i + it.gi;
+      a = it.a;
+      hq = x.hq;
+      partial = it.a < it.flo;
       // a causal row at position t sees t + 1 keys of its sequence; a block
       // step without the causal rule takes its key block's length as the bound
       if constexpr (kBlock)
         split = p.causal ? (__ldg(p.q_pos + it.a * kTile) + 1 < kSplitKeys) : (p.Lk < kSplitKeys);
       else
-        split = p.causal ? (token_at(p.layout, p.L, p.N, x.i, it.a * kTile) + 1 < kSplitKeys)
+        split = p.causal ? (token_at(p.layout, p.L, p.N, i, it.a * kTile) + 1 < kSplitKeys)
                          : (p.S < kSplitKeys);
       if constexpr (!kLo) return true;
       if (!split) {
@@ -414,7 +482,7 @@ __device__ __forceinline__ void store_p_half(const float (&pf)[64], uint32_t tS,
   }
 }
 
-template <int D, bool kDocs, bool kBlock>
+template <int D, bool kDocs, bool kBlock, bool kGroup>
 __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     bwd_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUtensorMap qmap,
                const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
@@ -423,7 +491,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                const __grid_constant__ CUtensorMap dkmap,
                const __grid_constant__ CUtensorMap dvmap) {
   using C = BwdCfg<D>;
-  const KvUnit x = decode_kv_unit<kDocs, kBlock>(p, blockIdx.x);
+  const KvUnit x = decode_kv_unit<kDocs, kBlock, kGroup>(p, blockIdx.x);
   if (x.a_lo >= x.a_hi) return;  // no query of this shard sees the tile: nothing to add
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
@@ -544,11 +612,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         ++n;
         return true;
       };
-      while (q_next<kDocs, kBlock>(p, x, it, i, a, hq, partial, split))
+      while (q_next<kDocs, kBlock, kGroup>(p, x, it, i, a, hq, partial, split))
         if (!load_step()) break;
       if (!*abort_flag && second_round()) {
         QIter it2;
-        while (q_next<kDocs, kBlock, true>(p, x, it2, i, a, hq, partial, split))
+        while (q_next<kDocs, kBlock, kGroup, true>(p, x, it2, i, a, hq, partial, split))
           if (!load_step()) break;
       }
       if (lane == 0 && *abort_flag) {
@@ -583,12 +651,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
           mma_commit(&bars[C::bSFull]);
           return true;
         };
-        bool has = q_next<kDocs, kBlock>(p, x, it, i, a, hq, partial, split);
+        bool has = q_next<kDocs, kBlock, kGroup>(p, x, it, i, a, hq, partial, split);
         if (has && lane == 0) issue_s(0);
         __syncwarp();
         while (has && !*abort_flag) {
           const bool cur_split = split;
-          const bool has_next = q_next<kDocs, kBlock>(p, x, it, i, a, hq, partial, split);
+          const bool has_next = q_next<kDocs, kBlock, kGroup>(p, x, it, i, a, hq, partial, split);
           if (lane == 0) {
             const int st = n % C::kQSt;
             const uint32_t q_s = sbase + C::kQOff + st * C::kTileBytes;
@@ -659,11 +727,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         // their residual terms (every accumulator keeps adding).
         if (!*abort_flag && second_round()) {
           QIter it2;
-          has = q_next<kDocs, kBlock, true>(p, x, it2, i, a, hq, partial, split);
+          has = q_next<kDocs, kBlock, kGroup, true>(p, x, it2, i, a, hq, partial, split);
           if (has && lane == 0) issue_s(n);
           __syncwarp();
           while (has && !*abort_flag) {
-            const bool has_next = q_next<kDocs, kBlock, true>(p, x, it2, i, a, hq, partial, split);
+            const bool has_next = q_next<kDocs, kBlock, kGroup, true>(p, x, it2, i, a, hq, partial, split);
             if (lane == 0) {
               const int st = n % C::kQSt;
               const uint32_t q_s = sbase + C::kQOff + st * C::kTileBytes;
@@ -873,13 +941,13 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       ++n;
       return true;
     };
-    while (q_next<kDocs, kBlock>(p, x, it, i, a, hq, partial, split))
+    while (q_next<kDocs, kBlock, kGroup>(p, x, it, i, a, hq, partial, split))
       if (!sm_step(std::false_type{})) break;
     // round one is over for this warp (and its detections are written)
     if (lane == 0) mbar_arrive(&bars[C::bRound]);
     if (!*abort_flag && second_round()) {
       QIter it2;
-      while (q_next<kDocs, kBlock, true>(p, x, it2, i, a, hq, partial, split))
+      while (q_next<kDocs, kBlock, kGroup, true>(p, x, it2, i, a, hq, partial, split))
         if (!sm_step(std::true_type{})) break;
     }
   } else if (warp < C::kDrainWarp0 + 4) {
@@ -951,11 +1019,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       ++n;
       return true;
     };
-    while (q_next<kDocs, kBlock>(p, x, it, i, a, hq, partial, split))
+    while (q_next<kDocs, kBlock, kGroup>(p, x, it, i, a, hq, partial, split))
       if (!drain_step()) break;
     if (!aborted && second_round()) {
       QIter it2;
-      while (q_next<kDocs, kBlock, true>(p, x, it2, i, a, hq, partial, split))
+      while (q_next<kDocs, kBlock, kGroup, true>(p, x, it2, i, a, hq, partial, split))
         if (!drain_step()) break;
     }
     if (lane == 0) bulk_wait_group0<false>();  // this warp's reductions complete
@@ -1099,8 +1167,12 @@ cudaError_t launch_bwd_t(const BwdParams &p, const float *out, const float *lse,
                       stream>>>(p, out, lse, dout);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  auto kern = p.block ? bwd_kernel<D, false, true>
-                      : (p.cu != nullptr ? bwd_kernel<D, true, false> : bwd_kernel<D, false, false>);
+  // units over a group of query shards walk them with their own iterator,
+  // compiled separately: folded into the one-shard kernel it cost 7 % there
+  auto kern = p.block           ? bwd_kernel<D, false, true, false>
+              : p.cu != nullptr ? bwd_kernel<D, true, false, false>
+              : p.qgroup > 1    ? bwd_kernel<D, false, false, true>
+                                : bwd_kernel<D, false, false, false>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemAlloc);
   if (e != cudaSuccess) return e;
   {

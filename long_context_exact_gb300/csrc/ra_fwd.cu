@@ -348,6 +348,17 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::kThreads, 1)
     fwd_kernel(const __grid_constant__ FwdParams p, const __grid_constant__ CUtensorMap qmap,
                const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap) {
   using C = FwdCfg<D, NQ>;
+  if constexpr (kBlock) {
+    // a prefill pass that covers only part of each query tile's key range:
+    // nothing to do when this CTA's split lies outside it
+    if (p.kt_end != nullptr || p.kt_begin != nullptr) {
+      const Unit y = decode_unit(p, blockIdx.x);
+      int kc0 = y.kc0, kc1 = y.kc1;
+      if (p.kt_end != nullptr) kc1 = min(kc1, __ldg(p.kt_end + y.a));
+      if (p.kt_begin != nullptr) kc0 = max(kc0, __ldg(p.kt_begin + y.a));
+      if (kc0 >= kc1) return;
+    }
+  }
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t *smem = smem_raw + pad;
@@ -388,6 +399,10 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::kThreads, 1)
   const uint32_t tmem = *tmem_holder;
 
   Unit x = decode_unit(p, blockIdx.x);
+  if constexpr (kBlock) {
+    if (p.kt_end != nullptr) x.kc1 = min(x.kc1, __ldg(p.kt_end + x.a));
+    if (p.kt_begin != nullptr) x.kc0 = max(x.kc0, __ldg(p.kt_begin + x.a));
+  }
   unit_qrange<kBlock, kDocs, kBNc>(p, x);
   // Rows that see fewer than kSplitKeys keys take the hi + lo path.  On the
   // ring a row at position t sees t + 1 keys.  A block step counts, over the

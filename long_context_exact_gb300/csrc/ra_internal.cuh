@@ -168,6 +168,11 @@ struct FwdParams {
   float *st_m;              // block: [b, h, Lq]
   float *st_l;              // block: [b, h, Lq]
   float *st_o;              // block: [b, Lq, h, d]
+  // block mode, chunked prefill: per query tile, the key tiles before
+  // kt_end[a] are seen in full by every row of the tile; a pass may stop its
+  // key range there (kt_end) or start it there (kt_begin)
+  const int32_t *kt_end;
+  const int32_t *kt_begin;
 };
 
 struct BwdParams {
@@ -224,6 +229,9 @@ cudaError_t launch_state_init(float *m, float *l, float *o, long long m_rows, in
                               cudaStream_t stream);
 cudaError_t launch_combine(const float *m, const float *l, const float *o, int splits, float *out,
                            float *lse, int b, long long Lq, int h, int d, cudaStream_t stream);
+cudaError_t launch_prefill_visible(const int32_t *q_pos, const int32_t *k_pos, long long Lq,
+                                   long long Lk, int32_t *kmax, int32_t *kt_end,
+                                   cudaStream_t stream);
 cudaError_t launch_ex2_probe(long long iters, float *sink, int blocks, int threads,
                              cudaStream_t stream);
 // Record a message for ra_last_error() on this thread and return `st`.

@@ -3,6 +3,8 @@
 // bounded-wait self test.  Also home of the device error word.
 #include <cmath>
 
+#include <climits>
+
 #include "ra_internal.cuh"
 #include "ra_ptx.cuh"
 
@@ -312,6 +314,67 @@ cudaError_t launch_combine(const float *m, const float *l, const float *o, int s
   if (rows == 0) return cudaSuccess;
   combine_kernel<<<rows_grid(static_cast<long long>(b) * h, Lq, 1), kEwThreads, 0, stream>>>(
       m, l, o, splits, out, lse, b, Lq, h, d);
+  return cudaGetLastError();
+}
+
+// Causal chunked prefill, first pass: the largest key position of every
+// 128-key tile (a warp per tile).
+__global__ void tile_kmax_kernel(const int32_t *k_pos, int Lk, int n_ktiles, int32_t *kmax) {
+  const int lane = threadIdx.x & 31;
+  const int c = static_cast<int>((static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5);
+  if (c >= n_ktiles) return;  // whole warps: 32 lanes share c
+  int mx = INT_MIN;
+  for (int e = lane; e < 128; e += 32) {
+    const int kr = c * 128 + e;
+    if (kr < Lk) mx = max(mx, k_pos[kr]);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+  if (lane == 0) kmax[c] = mx;
+}
+
+// Second pass: for query tile a, the number of leading key tiles whose
+// largest key position is at most the tile's smallest query position --
+// the key tiles every row of the tile sees in full.  A block per query tile.
+__global__ void prefill_visible_kernel(const int32_t *q_pos, int Lq, const int32_t *kmax,
+                                       int n_ktiles, int32_t *kt_end) {
+  __shared__ int qmin_s;
+  __shared__ int first_s;
+  const int a = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) first_s = n_ktiles;
+  if (warp == 0) {
+    int mn = INT_MAX;
+    for (int r = a * 128 + lane; r < min(Lq, a * 128 + 128); r += 32) mn = min(mn, q_pos[r]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, off));
+    if (lane == 0) qmin_s = mn;
+  }
+  __syncthreads();
+  const int qmin = qmin_s;
+  int first = n_ktiles;
+  for (int c = threadIdx.x; c < n_ktiles; c += blockDim.x)
+    if (kmax[c] > qmin) {
+      first = c;
+      break;
+    }
+  if (first < n_ktiles) atomicMin(&first_s, first);
+  __syncthreads();
+  if (threadIdx.x == 0) kt_end[a] = first_s;
+}
+
+cudaError_t launch_prefill_visible(const int32_t *q_pos, const int32_t *k_pos, long long Lq,
+                                   long long Lk, int32_t *kmax, int32_t *kt_end,
+                                   cudaStream_t stream) {
+  const long long n_qtiles = (Lq + 127) / 128;
+  const int n_ktiles = static_cast<int>((Lk + 127) / 128);
+  if (n_qtiles <= 0 || n_ktiles <= 0) return cudaSuccess;
+  tile_kmax_kernel<<<(n_ktiles + 7) / 8, 256, 0, stream>>>(k_pos, static_cast<int>(Lk), n_ktiles,
+                                                           kmax);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  prefill_visible_kernel<<<static_cast<unsigned int>(n_qtiles), 512, 0, stream>>>(
+      q_pos, static_cast<int>(Lq), kmax, n_ktiles, kt_end);
   return cudaGetLastError();
 }
 

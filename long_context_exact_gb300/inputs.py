@@ -55,9 +55,13 @@ WORKLOADS = {
     "causal256k": Workload("long causal GQA b1 h32 kv8 d128 S262144 N8 striped", 1, 262144,
                            32, 8, 128, 8, True, (STRIPED,), 3, amplitude=0.5,
                            rows_per_head=256),
-    # profiling-size case: inputs still larger than L2, ~2 GB on the device
+    # profiling-size cases: inputs still larger than L2, ~2 GB on the device;
+    # with one shard of 32K rows the backward runs the same one-shard units
+    # as the 256K workload (shards of 32K rows)
     "causal32k": Workload("causal GQA fwd+bwd b1 h32 kv8 d128 S32768 N8 striped", 1, 32768, 32,
                           8, 128, 8, True, (STRIPED,), 5, rows_per_head=128, backward=True),
+    "causal32k1": Workload("causal GQA fwd+bwd b1 h32 kv8 d128 S32768 N1", 1, 32768, 32, 8, 128,
+                           1, True, (STRIPED,), 5, rows_per_head=128, backward=True),
     # packed documents (log-uniform lengths 1K..64K) in one causal window
     "packed64k": Workload("packed causal GQA b1 h32 kv8 d128 S65536 N8 striped", 1, 65536, 32,
                           8, 128, 8, True, (STRIPED,), 6, rows_per_head=256),

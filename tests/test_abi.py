@@ -140,12 +140,17 @@ def test_prefill_validation_and_workspace(lib):
                                               binding.Dims]
     lib.ra_prefill_workspace_size.restype = ctypes.c_size_t
     d = _dims(b=1, h=8, n_kv=2, d=128)
-    # explicit split counts: n_splits states of (m, l, O) per query row
-    assert lib.ra_prefill_workspace_size(256, 4096, 4, d) == 4 * 8 * 256 * (2 + 128) * 4
+    # explicit split counts: n_splits states of (m, l, O) per query row, then
+    # one int per 128-query tile and one per 128-key tile (each rounded up to
+    # 16 bytes)
+    def size(splits, Lq=256, Lk=4096):
+        return (splits * 8 * Lq * (2 + 128) * 4 + ((Lq + 127) // 128 * 4 + 15) // 16 * 16 +
+                ((Lk + 127) // 128 * 4 + 15) // 16 * 16)
+    assert lib.ra_prefill_workspace_size(256, 4096, 4, d) == size(4)
     # never more splits than key tiles, and no empty split
-    assert lib.ra_prefill_workspace_size(256, 300, 8, d) == 3 * 8 * 256 * 130 * 4
-    assert lib.ra_prefill_workspace_size(256, 1280, 4, d) == 4 * 8 * 256 * 130 * 4
-    assert lib.ra_prefill_workspace_size(256, 1280, 6, d) == 5 * 8 * 256 * 130 * 4
+    assert lib.ra_prefill_workspace_size(256, 300, 8, d) == size(3, Lk=300)
+    assert lib.ra_prefill_workspace_size(256, 1280, 4, d) == size(4, Lk=1280)
+    assert lib.ra_prefill_workspace_size(256, 1280, 6, d) == size(5, Lk=1280)
     assert lib.ra_prefill_workspace_size(0, 4096, 4, d) == 0
     args = [FAKE] * 7
     assert lib.ra_chunked_prefill(*args, 256, 4096, 65, d, 1, 0.0, FAKE, 1 << 30, None) == \

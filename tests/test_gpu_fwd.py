@@ -352,6 +352,32 @@ def test_chunked_prefill_matches_oracle(orc, Lq, Lk, causal, g, d, splits):
     _cmp(out, lse, ref_o, ref_l)
 
 
+@pytest.mark.parametrize("sort_keys", [True, False])
+def test_chunked_prefill_irregular_positions(orc, sort_keys):
+    """Causal prefill with positions that are neither contiguous nor (for the
+    keys) sorted: the leading key tiles every row of a query tile sees in
+    full run without the mask and the rest with it, so the split point
+    differs from tile to tile; the result must not depend on it."""
+    Lq, Lk, h, n_kv, d = 384, 5000, 4, 2, 128
+    rng = np.random.default_rng(17 + sort_keys)
+    q, _, _ = make_inputs(1, Lq, h, n_kv, d, seed=18)
+    _, k, v = make_inputs(1, Lk, h, n_kv, d, seed=19)
+    q_pos = np.sort(rng.choice(np.arange(2000, 9000), Lq, replace=False)).astype(np.int32)
+    k_pos = rng.choice(9000, Lk, replace=False).astype(np.int32)
+    if sort_keys:
+        k_pos = np.sort(k_pos)
+    st = orc.new_state(1, Lq, h, d)
+    orc.block_update(q, k, v, q_pos, k_pos, True, 1.0 / np.sqrt(d), st)
+    ref_o, ref_l = orc.finalize(st)
+    qd, kd, vd = _dev(q, k, v)
+    qp, kp = (torch.from_numpy(x).cuda() for x in (q_pos, k_pos))
+    for splits in (0, 3):
+        out, lse = _nan_out(1, Lq, h, d)
+        ra.chunked_prefill(qd, kd, vd, qp, kp, True, n_splits=splits, out=out, lse=lse)
+        ra.stream_check()
+        _cmp(out, lse, ref_o, ref_l)
+
+
 def test_chunked_prefill_batch_of_two(orc):
     """b = 2: the split states and their combination are per batch row."""
     b, Lq, Lk, h, n_kv, d = 2, 200, 1500, 4, 2, 128
