@@ -718,6 +718,18 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::kThreads, 1)
         exp_pack_store<kSplit>(s, sl2x2, f2pack(-base, -base), acc, tS);
         if (!spec) break;
         spec = false;
+        if constexpr (!kBlock) {
+          // The ring epilogue needs no exact max: when the tile's P sums to
+          // at most min(2^8, l / 8) in the current shift's units, no P
+          // passes either bound of needs_shift, and the warp skips the max.
+          float b0, b1, b2, b3, b4, b5, b6, b7;
+          f2unpack(acc[0], b0, b1);
+          f2unpack(acc[1], b2, b3);
+          f2unpack(acc[2], b4, b5);
+          f2unpack(acc[3], b6, b7);
+          const float ts = ((b0 + b1) + (b2 + b3)) + ((b4 + b5) + (b6 + b7));
+          if (!__any_sync(kFull, ts > fminf(256.f, l_sum * (1.f / kDominance)))) break;
+        }
         const float mx2 = row_max() * sl2;
         m_max = fmaxf(m_max, mx2);
         const bool need = needs_shift(mx2);
