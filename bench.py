@@ -440,6 +440,34 @@ def prefill_report(w, q, k, v, dev):
     return res
 
 
+def block_step_report(w, q, k, v, dev):
+    """One ring step through ra_block_step at the workload's shard size
+    L = S / N, the per-device step of a ring across GPUs: a key block wholly
+    before the queries (every tile seen in full), the diagonal block (equal
+    positions), a striped step (query shard 1 against key shard 0 of N
+    striped shards) and the non-causal step.  Useful FLOPs count the visible
+    (query, key) pairs: 4 b h d per pair."""
+    import torch
+
+    from long_context_exact_gb300 import binding as ra
+
+    N = w.n_shards
+    L = w.S // N
+    qb, kb, vb = (t[:, :L].contiguous() for t in (q, k, v))
+    ar = torch.arange(L, dtype=torch.int32, device=dev)
+    tri = L * (L + 1) // 2
+    cases = (("off_diagonal", ar + L, ar, True, L * L), ("diagonal", ar, ar, True, tri),
+             ("striped", ar * N + 1, ar * N, True, tri), ("noncausal", ar, ar, False, L * L))
+    res = {"L": L, "b": w.b, "h": w.h, "n_kv": w.n_kv, "d": w.d}
+    st = ra.new_state(w.b, L, w.h, w.d, dev)
+    for name, qp, kp, causal, pairs in cases:
+        ms = _time_ms(lambda: ra.block_step(qb, kb, vb, st, qp, kp, causal), reps=3)
+        res[name] = {"ms": ms, "tflops": 4.0 * w.b * w.h * w.d * pairs / (ms / 1e3) / 1e12}
+    del st, qb, kb, vb
+    ra.stream_check()
+    return res
+
+
 def packed_report(w, q, k, v, do, layout, dev):
     """Packed documents in the workload's window (the third page's section 5,
     branch two: a kernel that skips the masked blocks): document lengths
@@ -697,6 +725,7 @@ def run_ours(a, rank, world, local_rank):
         extras["exp2_roof"] = extra(exp2_roof_report, w, dev, clk)
         extras["hbm_kernels"] = extra(hbm_kernel_report, w, dev, peaks)
         extras["chunked_prefill"] = extra(prefill_report, w, q, k, v, dev)
+        extras["block_steps"] = extra(block_step_report, w, q, k, v, dev)
         if have_bwd:
             extras["packed_documents"] = extra(packed_report, w, q, k, v, do, layout, dev)
 

@@ -314,6 +314,19 @@ ra_status ra_block_step(const uint16_t *q, const uint16_t *k, const uint16_t *v,
   p.st_m = m;
   p.st_l = l;
   p.st_o = o;
+  if (causal) {
+    // Two launches that fold into the same state: the leading key tiles each
+    // query tile sees in full (on a ring step, all tiles off the diagonal)
+    // through the kernel without the causal rule, ~35 % faster per tile;
+    // then the rest through the causal one.  Each CTA finds its own split.
+    FwdParams pv = p;
+    pv.causal = 0;
+    pv.full_prefix = 1;
+    if ((st = launch_attention(pv, dims.d, q, k, v, Lq, Lk, static_cast<cudaStream_t>(stream))) !=
+        RA_OK)
+      return st;
+    p.full_prefix = 2;
+  }
   return launch_attention(p, dims.d, q, k, v, Lq, Lk, static_cast<cudaStream_t>(stream));
 }
 

@@ -53,6 +53,10 @@ constexpr float kRescaleThreshold = 8.0f;
 // key's P is then exactly 1, and no single rounded bf16 P carries a large
 // share of the row (peaked attention on the plain path).
 constexpr float kDominance = 8.0f;
+// Causal block step in two launches: a query tile whose key range also has
+// tiles under the mask moves its fully seen leading tiles to the unmasked
+// launch only when there are at least this many.
+constexpr int kMinPrefixTiles = 32;
 // block mode, causal: words of the CTA's keep bits (then as many mask bits)
 constexpr int kBitWords = kBlockKeyTiles / 32;
 constexpr unsigned int kFull = 0xffffffffu;
@@ -288,6 +292,51 @@ __device__ __forceinline__ bool kv_next(const FwdParams &p, const Unit &x, KvIte
   }
 }
 
+// Block mode: how many key tiles of [kc0, kc1), counted from kc0, every row
+// of query tile a sees in full -- complete tiles whose key positions are all
+// <= the tile's smallest query position (any positions, sorted or not).
+// Warp w walks tiles kc0 + w, kc0 + w + nw, ... four at a time and stops at
+// its first tile that fails; the prefix ends at the smallest of those.
+// Block-collective; `scratch` holds 64 ints.
+__device__ __noinline__ int full_prefix_tiles(const FwdParams &p, int a, int kc0, int kc1,
+                                              int *scratch) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  const int r1 = min((a + 1) * kTile, p.L);
+  int qmin = INT_MAX;
+  for (int r = a * kTile + static_cast<int>(threadIdx.x); r < r1; r += blockDim.x)
+    qmin = min(qmin, __ldg(p.q_pos + r));
+  qmin = warp_min(qmin);
+  if (lane == 0) scratch[warp] = qmin;
+  __syncthreads();
+  qmin = INT_MAX;
+  for (int w = 0; w < nw; ++w) qmin = min(qmin, scratch[w]);
+  const int n_complete = p.Lk / kTile;
+  int first = kc1;
+  for (int c = kc0 + warp; c < kc1 && first == kc1; c += 4 * nw) {
+    bool bad[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int t = c + u * nw;
+      bool b = t >= n_complete && t < kc1;  // the ragged last tile is masked
+      if (t < kc1 && t < n_complete) {
+#pragma unroll
+        for (int e = 0; e < kTile / 32; ++e)
+          b |= __ldg(p.k_pos + static_cast<size_t>(t) * kTile + e * 32 + lane) > qmin;
+      }
+      bad[u] = __any_sync(kFull, b);
+    }
+#pragma unroll
+    for (int u = 3; u >= 0; --u)
+      if (bad[u]) first = c + u * nw;
+  }
+  if (lane == 0) scratch[32 + warp] = first;
+  __syncthreads();
+  int f = kc1;
+  for (int w = 0; w < nw; ++w) f = min(f, scratch[32 + w]);
+  __syncthreads();  // scratch is free again
+  return f - kc0;
+}
+
 template <int D>
 __device__ __forceinline__ void issue_s_mma(uint32_t tS, uint32_t q_saddr, uint32_t k_saddr,
                                             uint32_t idesc) {
@@ -348,6 +397,10 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::kThreads, 1)
     fwd_kernel(const __grid_constant__ FwdParams p, const __grid_constant__ CUtensorMap qmap,
                const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap) {
   using C = FwdCfg<D, NQ>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+  uint8_t *smem = smem_raw + pad;
+  int fp = 0;  // two-launch causal step: leading key tiles seen in full
   if constexpr (kBlock) {
     // a prefill pass that covers only part of each query tile's key range:
     // nothing to do when this CTA's split lies outside it
@@ -358,10 +411,16 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::kThreads, 1)
       if (p.kt_begin != nullptr) kc0 = max(kc0, __ldg(p.kt_begin + y.a));
       if (kc0 >= kc1) return;
     }
+    if (p.full_prefix != 0) {
+      const Unit y = decode_unit(p, blockIdx.x);
+      fp = full_prefix_tiles(p, y.a, y.kc0, y.kc1,
+                             reinterpret_cast<int *>(smem + C::kBitsOff));
+      // a CTA with work in both launches pays a second start and state
+      // merge, which a short prefix does not earn back: it stays whole
+      if (fp < y.kc1 - y.kc0 && fp < kMinPrefixTiles) fp = 0;
+      if (p.full_prefix == 1 ? fp == 0 : y.kc0 + fp >= y.kc1) return;
+    }
   }
-  extern __shared__ uint8_t smem_raw[];
-  const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
-  uint8_t *smem = smem_raw + pad;
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kBarOff);
   uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + C::kMiscOff);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kMiscOff + 4);
@@ -399,9 +458,15 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::kThreads, 1)
   const uint32_t tmem = *tmem_holder;
 
   Unit x = decode_unit(p, blockIdx.x);
+  // the first key tile of the CTA's whole range (a second launch of a
+  // causal step starts later but takes its precision mode from all of it)
+  int kc_all = x.kc0;
   if constexpr (kBlock) {
     if (p.kt_end != nullptr) x.kc1 = min(x.kc1, __ldg(p.kt_end + x.a));
     if (p.kt_begin != nullptr) x.kc0 = max(x.kc0, __ldg(p.kt_begin + x.a));
+    kc_all = x.kc0;
+    if (p.full_prefix == 1) x.kc1 = x.kc0 + fp;
+    if (p.full_prefix == 2) x.kc0 += fp;
   }
   unit_qrange<kBlock, kDocs, kBNc>(p, x);
   // Rows that see fewer than kSplitKeys keys take the hi + lo path.  On the
@@ -412,7 +477,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::kThreads, 1)
   if constexpr (!kBlock) {
     split = x.minvis < kSplitKeys;
   } else {
-    const int k0 = x.kc0 * kTile, k1 = min(p.Lk, x.kc1 * kTile);
+    const int k0 = kc_all * kTile, k1 = min(p.Lk, x.kc1 * kTile);
     const int nt = x.kc1 - x.kc0;
     if (!kBNc && p.causal) {
       int *cnt = reinterpret_cast<int *>(smem + C::kMiscOff + 8);
@@ -449,7 +514,8 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::kThreads, 1)
       for (int o = 16; o > 0; o >>= 1) mine += __shfl_xor_sync(kFull, mine, o);
       if (lane == 0) atomicAdd(cnt, mine);
       __syncthreads();
-      split = k1 - k0 < kSplitKeys || *cnt < kSplitKeys;
+      // keys of the tiles a first launch took (all seen by every row)
+      split = k1 - k0 < kSplitKeys || *cnt + fp * kTile < kSplitKeys;
       x.kbits = bits;
     } else {
       split = k1 - k0 < kSplitKeys;  // without the causal rule every row sees the range

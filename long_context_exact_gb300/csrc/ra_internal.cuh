@@ -173,6 +173,11 @@ struct FwdParams {
   // key range there (kt_end) or start it there (kt_begin)
   const int32_t *kt_end;
   const int32_t *kt_begin;
+  // block mode, causal step in two launches: each CTA finds the leading key
+  // tiles of its range that every row of its query tile sees in full; 1: the
+  // launch (without the causal rule) covers only those, 2: the launch (with
+  // it) covers the rest.  0: the whole range.
+  int full_prefix;
 };
 
 struct BwdParams {

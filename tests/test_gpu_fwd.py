@@ -191,6 +191,68 @@ def test_block_step_matches_oracle_update(orc, Lq, Lk, causal, g, d):
     _cmp(out, lse, r_out, r_lse)
 
 
+def _block_steps_vs_oracle(orc, q, blocks, q_pos, causal=True):
+    """Fold the key/value blocks [(k, v, k_pos), ...] into one state with
+    ra_block_step and with the oracle's update; compare the finalized rows."""
+    b, Lq, h, d = q.shape
+    scale = 1.0 / np.sqrt(d)
+    st_ref = orc.new_state(b, Lq, h, d)
+    st = ra.new_state(b, Lq, h, d, "cuda")
+    qd = _dev(q)[0]
+    qp = torch.from_numpy(q_pos).cuda()
+    for k, v, k_pos in blocks:
+        orc.block_update(q, k, v, q_pos, k_pos, causal, scale, st_ref)
+        kd, vd = _dev(k, v)
+        ra.block_step(qd, kd, vd, st, qp, torch.from_numpy(k_pos).cuda(), causal)
+    ra.stream_check()
+    out, lse = ra.finalize(st, lse=torch.full_like(st[0], float("nan")))
+    r_out, r_lse = orc.finalize(st_ref)
+    _cmp(out, lse, r_out, r_lse)
+
+
+@pytest.mark.parametrize("sort_keys", [True, False])
+def test_block_step_irregular_positions(orc, sort_keys):
+    """A causal block step runs, per query tile, the leading key tiles every
+    row sees in full without the mask and the rest with it; with positions
+    neither contiguous nor (for the keys) sorted that split point differs
+    from tile to tile, and the result must not depend on it.  With sorted
+    keys the three query tiles see 23, 40 and 56 leading tiles in
+    full: the first stays in one launch (a short prefix), the others split."""
+    Lq, Lk, h, n_kv, d = 384, 9000, 4, 2, 128
+    rng = np.random.default_rng(27 + sort_keys)
+    q, _, _ = make_inputs(1, Lq, h, n_kv, d, seed=28)
+    _, k, v = make_inputs(1, Lk, h, n_kv, d, seed=29)
+    q_pos = np.sort(rng.choice(np.arange(4000, 12000), Lq, replace=False)).astype(np.int32)
+    k_pos = rng.choice(12000, Lk, replace=False).astype(np.int32)
+    if sort_keys:
+        k_pos = np.sort(k_pos)
+    _block_steps_vs_oracle(orc, q, [(k, v, k_pos)], q_pos)
+
+
+def test_block_step_key_block_wholly_before_or_after(orc):
+    """Ring steps off the diagonal: a key block wholly before the queries
+    (every tile seen in full: the masked launch has nothing left) and one
+    wholly after them (the unmasked launch has nothing: the state stays as
+    it was, bit for bit)."""
+    Lq, Lk, h, n_kv, d = 256, 1152, 4, 2, 64
+    q, _, _ = make_inputs(1, Lq, h, n_kv, d, seed=31)
+    _, k, v = make_inputs(1, Lk, h, n_kv, d, seed=32)
+    _, k2, v2 = make_inputs(1, Lk, h, n_kv, d, seed=33)
+    q_pos = np.arange(5000, 5000 + Lq, dtype=np.int32)
+    before = np.arange(0, 2 * Lk, 2, dtype=np.int32)           # all <= 5000
+    after = np.arange(6000, 6000 + Lk, dtype=np.int32)         # all > every query
+    _block_steps_vs_oracle(orc, q, [(k, v, before)], q_pos)
+    st = ra.new_state(1, Lq, h, d, "cuda")
+    qd, kd, vd, k2d, v2d = _dev(q, k, v, k2, v2)
+    qp = torch.from_numpy(q_pos).cuda()
+    ra.block_step(qd, kd, vd, st, qp, torch.from_numpy(before).cuda(), True)
+    saved = [t.clone() for t in st]
+    ra.block_step(qd, k2d, v2d, st, qp, torch.from_numpy(after).cuda(), True)
+    ra.stream_check()
+    for a, b_ in zip(st, saved):
+        assert torch.equal(a, b_)
+
+
 # ------------------------------------------------------------------ peaked attention
 # Inputs from parity_util.peaked_inputs: every query has one key aligned with
 # it, placed in the last shard of its ring order that holds a key it sees, so
