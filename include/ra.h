@@ -117,11 +117,11 @@ typedef struct {
  * Initial state: m = -inf, l = 0, o = 0.  Rows with no visible key in this
  * block are left unchanged.  Lq or Lk == 0 is a no-op.  A causal step takes
  * at most 8,388,608 keys (each CTA classifies its whole key range once, in
- * shared memory); RA_ERR_UNSUPPORTED above that.  A causal step is two
- * kernel launches on `stream`: per 128-query tile, the leading key tiles
- * every row sees in full (at least 32 of them, or all) go through a kernel
- * without the mask, the rest through the masked one; both fold into the
- * state, so no workspace is needed. */
+ * shared memory); RA_ERR_UNSUPPORTED above that.  A causal step over at
+ * least 16,384 keys is two kernel launches on `stream`: per 128-query tile,
+ * the leading key tiles every row sees in full (at least 32 of them, or
+ * all) go through a kernel without the mask, the rest through the masked
+ * one; both fold into the state, so no workspace is needed. */
 ra_status ra_block_step(const uint16_t *q, const uint16_t *k, const uint16_t *v, float *m,
                         float *l, float *o, const int32_t *q_pos, const int32_t *k_pos,
                         int64_t Lq, int64_t Lk, ra_dims dims, int causal, float scale,

@@ -217,6 +217,14 @@ ra_status launch_attention(const FwdParams &p, int d, const void *q, const void 
   return RA_OK;
 }
 
+// A causal block step over at least this many key tiles (16,384 keys) runs
+// in two launches (the fully seen leading tiles of each query tile unmasked,
+// the rest masked).  Below it the second launch's fixed cost -- every CTA
+// starts and scans the positions once more -- and the tails of two short
+// launches outweigh the faster tiles: 8K x 8K diagonal steps lost 6-11 %,
+// 16K ones gained 2 %, 32K ones 13 % (off the diagonal 25 %).
+constexpr int kTwoLaunchKeyTiles = 128;
+
 // Key splits for a chunked prefill: n_splits if given (capped by the key
 // tiles and kMaxSplits), else enough splits for about eight waves of CTAs
 // (so the last, partly filled wave costs little) with at least four key
@@ -314,7 +322,7 @@ ra_status ra_block_step(const uint16_t *q, const uint16_t *k, const uint16_t *v,
   p.st_m = m;
   p.st_l = l;
   p.st_o = o;
-  if (causal) {
+  if (causal && p.n_ktiles >= kTwoLaunchKeyTiles) {
     // Two launches that fold into the same state: the leading key tiles each
     // query tile sees in full (on a ring step, all tiles off the diagonal)
     // through the kernel without the causal rule, ~35 % faster per tile;

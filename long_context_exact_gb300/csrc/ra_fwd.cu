@@ -295,9 +295,42 @@ __device__ __forceinline__ bool kv_next(const FwdParams &p, const Unit &x, KvIte
 // Block mode: how many key tiles of [kc0, kc1), counted from kc0, every row
 // of query tile a sees in full -- complete tiles whose key positions are all
 // <= the tile's smallest query position (any positions, sorted or not).
-// Warp w walks tiles kc0 + w, kc0 + w + nw, ... four at a time and stops at
-// its first tile that fails; the prefix ends at the smallest of those.
+// Warp w walks tiles kc0 + w, kc0 + w + nw, ... eight at a time (one 16-byte
+// load per lane and tile when k_pos is 16-byte aligned) and stops at its
+// first tile that fails; the prefix ends at the smallest of those.
 // Block-collective; `scratch` holds 64 ints.
+template <bool kVec>
+__device__ __forceinline__ int first_failing_tile(const FwdParams &p, int kc0, int kc1, int qmin,
+                                                  int warp, int lane, int nw) {
+  constexpr int kBatch = 8;
+  const int n_complete = p.Lk / kTile;
+  int first = kc1;
+  for (int c = kc0 + warp; c < kc1 && first == kc1; c += kBatch * nw) {
+    int hi[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int t = c + u * nw;
+      hi[u] = INT_MIN;
+      if (t < kc1 && t < n_complete) {
+        const int32_t *kp = p.k_pos + static_cast<size_t>(t) * kTile;
+        if constexpr (kVec) {
+          const int4 v4 = __ldg(reinterpret_cast<const int4 *>(kp) + lane);
+          hi[u] = max(max(v4.x, v4.y), max(v4.z, v4.w));
+        } else {
+#pragma unroll
+          for (int e = 0; e < kTile / 32; ++e) hi[u] = max(hi[u], __ldg(kp + e * 32 + lane));
+        }
+      } else if (t < kc1) {
+        hi[u] = INT_MAX;  // the ragged last tile is masked
+      }
+    }
+#pragma unroll
+    for (int u = kBatch - 1; u >= 0; --u)
+      if (__any_sync(kFull, hi[u] > qmin)) first = c + u * nw;
+  }
+  return first;
+}
+
 __device__ __noinline__ int full_prefix_tiles(const FwdParams &p, int a, int kc0, int kc1,
                                               int *scratch) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
@@ -310,25 +343,9 @@ __device__ __noinline__ int full_prefix_tiles(const FwdParams &p, int a, int kc0
   __syncthreads();
   qmin = INT_MAX;
   for (int w = 0; w < nw; ++w) qmin = min(qmin, scratch[w]);
-  const int n_complete = p.Lk / kTile;
-  int first = kc1;
-  for (int c = kc0 + warp; c < kc1 && first == kc1; c += 4 * nw) {
-    bool bad[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int t = c + u * nw;
-      bool b = t >= n_complete && t < kc1;  // the ragged last tile is masked
-      if (t < kc1 && t < n_complete) {
-#pragma unroll
-        for (int e = 0; e < kTile / 32; ++e)
-          b |= __ldg(p.k_pos + static_cast<size_t>(t) * kTile + e * 32 + lane) > qmin;
-      }
-      bad[u] = __any_sync(kFull, b);
-    }
-#pragma unroll
-    for (int u = 3; u >= 0; --u)
-      if (bad[u]) first = c + u * nw;
-  }
+  const int first = (reinterpret_cast<uintptr_t>(p.k_pos) & 15u) == 0
+                        ? first_failing_tile<true>(p, kc0, kc1, qmin, warp, lane, nw)
+                        : first_failing_tile<false>(p, kc0, kc1, qmin, warp, lane, nw);
   if (lane == 0) scratch[32 + warp] = first;
   __syncthreads();
   int f = kc1;

@@ -191,9 +191,11 @@ def test_block_step_matches_oracle_update(orc, Lq, Lk, causal, g, d):
     _cmp(out, lse, r_out, r_lse)
 
 
-def _block_steps_vs_oracle(orc, q, blocks, q_pos, causal=True):
+def _block_steps_vs_oracle(orc, q, blocks, q_pos, causal=True, k_pos_offset=0):
     """Fold the key/value blocks [(k, v, k_pos), ...] into one state with
-    ra_block_step and with the oracle's update; compare the finalized rows."""
+    ra_block_step and with the oracle's update; compare the finalized rows.
+    k_pos_offset > 0 hands the library k_pos at that many int32 past a
+    16-byte boundary (the position scans then load one int at a time)."""
     b, Lq, h, d = q.shape
     scale = 1.0 / np.sqrt(d)
     st_ref = orc.new_state(b, Lq, h, d)
@@ -203,30 +205,35 @@ def _block_steps_vs_oracle(orc, q, blocks, q_pos, causal=True):
     for k, v, k_pos in blocks:
         orc.block_update(q, k, v, q_pos, k_pos, causal, scale, st_ref)
         kd, vd = _dev(k, v)
-        ra.block_step(qd, kd, vd, st, qp, torch.from_numpy(k_pos).cuda(), causal)
+        kp = torch.zeros(len(k_pos) + k_pos_offset, dtype=torch.int32, device="cuda")
+        kp[k_pos_offset:] = torch.from_numpy(k_pos).cuda()
+        kp = kp[k_pos_offset:]
+        assert kp.data_ptr() % 16 == 4 * k_pos_offset
+        ra.block_step(qd, kd, vd, st, qp, kp, causal)
     ra.stream_check()
     out, lse = ra.finalize(st, lse=torch.full_like(st[0], float("nan")))
     r_out, r_lse = orc.finalize(st_ref)
     _cmp(out, lse, r_out, r_lse)
 
 
-@pytest.mark.parametrize("sort_keys", [True, False])
-def test_block_step_irregular_positions(orc, sort_keys):
-    """A causal block step runs, per query tile, the leading key tiles every
-    row sees in full without the mask and the rest with it; with positions
-    neither contiguous nor (for the keys) sorted that split point differs
-    from tile to tile, and the result must not depend on it.  With sorted
-    keys the three query tiles see 23, 40 and 56 leading tiles in
-    full: the first stays in one launch (a short prefix), the others split."""
-    Lq, Lk, h, n_kv, d = 384, 9000, 4, 2, 128
+@pytest.mark.parametrize("sort_keys,k_pos_offset", [(True, 0), (False, 0), (True, 1)])
+def test_block_step_irregular_positions(orc, sort_keys, k_pos_offset):
+    """A causal block step over >= 16K keys runs, per query tile, the leading
+    key tiles every row sees in full without the mask and the rest with it;
+    with positions neither contiguous nor (for the keys) sorted that split
+    point differs from tile to tile, and the result must not depend on it.
+    With sorted keys the three query tiles see 24, 71 and 116 leading tiles
+    in full: the first stays in the masked launch (a short prefix), the
+    others split; the last key tile is ragged (20,000 keys)."""
+    Lq, Lk, h, n_kv, d = 384, 20000, 4, 2, 128
     rng = np.random.default_rng(27 + sort_keys)
     q, _, _ = make_inputs(1, Lq, h, n_kv, d, seed=28)
     _, k, v = make_inputs(1, Lk, h, n_kv, d, seed=29)
-    q_pos = np.sort(rng.choice(np.arange(4000, 12000), Lq, replace=False)).astype(np.int32)
-    k_pos = rng.choice(12000, Lk, replace=False).astype(np.int32)
+    q_pos = np.sort(rng.choice(np.arange(4000, 26000), Lq, replace=False)).astype(np.int32)
+    k_pos = rng.choice(26000, Lk, replace=False).astype(np.int32)
     if sort_keys:
         k_pos = np.sort(k_pos)
-    _block_steps_vs_oracle(orc, q, [(k, v, k_pos)], q_pos)
+    _block_steps_vs_oracle(orc, q, [(k, v, k_pos)], q_pos, k_pos_offset=k_pos_offset)
 
 
 def test_block_step_key_block_wholly_before_or_after(orc):
@@ -234,18 +241,20 @@ def test_block_step_key_block_wholly_before_or_after(orc):
     (every tile seen in full: the masked launch has nothing left) and one
     wholly after them (the unmasked launch has nothing: the state stays as
     it was, bit for bit)."""
-    Lq, Lk, h, n_kv, d = 256, 1152, 4, 2, 64
+    Lq, Lk, h, n_kv, d = 256, 16512, 4, 2, 64   # 129 key tiles: the two-launch path
     q, _, _ = make_inputs(1, Lq, h, n_kv, d, seed=31)
     _, k, v = make_inputs(1, Lk, h, n_kv, d, seed=32)
     _, k2, v2 = make_inputs(1, Lk, h, n_kv, d, seed=33)
-    q_pos = np.arange(5000, 5000 + Lq, dtype=np.int32)
-    before = np.arange(0, 2 * Lk, 2, dtype=np.int32)           # all <= 5000
-    after = np.arange(6000, 6000 + Lk, dtype=np.int32)         # all > every query
+    q_pos = np.arange(40000, 40000 + Lq, dtype=np.int32)
+    before = np.arange(0, 2 * Lk, 2, dtype=np.int32)           # all < 40000
+    after = np.arange(50000, 50000 + Lk, dtype=np.int32)       # all > every query
     _block_steps_vs_oracle(orc, q, [(k, v, before)], q_pos)
     st = ra.new_state(1, Lq, h, d, "cuda")
     qd, kd, vd, k2d, v2d = _dev(q, k, v, k2, v2)
     qp = torch.from_numpy(q_pos).cuda()
+    n0 = ra.launch_count()
     ra.block_step(qd, kd, vd, st, qp, torch.from_numpy(before).cuda(), True)
+    assert ra.launch_count() - n0 == 2       # unmasked launch, then masked
     saved = [t.clone() for t in st]
     ra.block_step(qd, k2d, v2d, st, qp, torch.from_numpy(after).cuda(), True)
     ra.stream_check()
