@@ -282,10 +282,12 @@ struct QIter {
   // unmasked query-tile bounds
   int gi = -1, lo = 0, flo = 0;
   bool done = false;
-  // packed documents: the query shard, query head, and the documents of the
-  // current tile's first and last rows
+  // packed documents: the query shard, query head, the documents of the
+  // current tile's first and last rows, and whether the tile has a row that
+  // sees fewer than kSplitKeys keys (found once per tile, kept for its heads)
   int i = 0, hh = 0;
   int d0 = -1, d1 = -1;
+  bool tile_split = false;
 };
 
 // Document index of position t, starting from a document index at or after
@@ -394,20 +396,21 @@ __device__ __forceinline__ bool q_next(const BwdParams &p, const KvUnit &x, QIte
     a = it.a;
     hq = x.kh * p.g + it.hh;
     partial = it.a < x.a_flo || it.a >= x.a_fhi;
-    const int t0 = token_at(p.layout, p.L, p.N, it.i, it.a * kTile);
-    int minvis;
-    {
+    if (it.hh == 0) {  // a new query tile
+      const int t0 = token_at(p.layout, p.L, p.N, it.i, it.a * kTile);
       const int t1 = token_at(p.layout, p.L, p.N, it.i, min(it.a * kTile + kTile, p.L) - 1);
       const int32_t *cb = p.cu + static_cast<size_t>(x.bb) * (p.n_docs + 1);
       it.d0 = doc_walk(cb, p.n_docs, it.d0, t0);
       it.d1 = doc_walk(cb, p.n_docs, it.d1, t1);
       const int ds0 = cb[it.d0], de0 = cb[it.d0 + 1], ds1 = cb[it.d1], de1 = cb[it.d1 + 1];
+      int minvis;
       if (p.causal)
         minvis = ds1 > t0 ? 1 : t0 - ds0 + 1;  // a document starting inside: 1
       else
         minvis = de0 < ds1 ? 1 : min(de0 - ds0, de1 - ds1);
+      it.tile_split = minvis < kSplitKeys;
     }
-    split = minvis < kSplitKeys;
+    split = it.tile_split;
     if constexpr (!kLo) return true;
     if (!split) {
       split = true;
