@@ -38,7 +38,7 @@ WORKLOAD = "causal256k"
 # (5.19 GB) and scaled to this workload: the compulsory 2.3 GB with S (x 8),
 # the rest with the causal step count (x 64).
 TRAFFIC = {
-    "bwd": {"bytes_per_launch": 204e9, "src_sha": "4ac805f625d439fb",
+    "bwd": {"bytes_per_launch": 204e9, "src_sha": "621eee2074e81eb6",
             "method": "ncu on the causal32k1 case (5.19 GB), scaled: 2.3 GB x 8 + 2.89 GB x 64"},
 }
 
