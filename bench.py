@@ -46,7 +46,10 @@ TRAFFIC = {
 def _args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=3)
+    # ten steps: the e2e pipeline's first uploads and last downloads are not
+    # hidden (~0.4 s per run where pinned copies move ~27 GB/s), and fewer
+    # steps would charge them to too little work
+    ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=WORKLOAD)
