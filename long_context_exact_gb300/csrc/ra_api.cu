@@ -325,7 +325,7 @@ ra_status ra_block_step(const uint16_t *q, const uint16_t *k, const uint16_t *v,
   if (causal && p.n_ktiles >= kTwoLaunchKeyTiles) {
     // Two launches that fold into the same state: the leading key tiles each
     // query tile sees in full (on a ring step, all tiles off the diagonal)
-    // through the kernel without the causal rule, ~35 % faster per tile;
+    // through the kernel without the causal rule, ~25 % faster per tile;
     // then the rest through the causal one.  Each CTA finds its own split.
     FwdParams pv = p;
     pv.causal = 0;

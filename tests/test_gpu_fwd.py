@@ -236,20 +236,21 @@ def test_block_step_irregular_positions(orc, sort_keys, k_pos_offset):
     _block_steps_vs_oracle(orc, q, [(k, v, k_pos)], q_pos, k_pos_offset=k_pos_offset)
 
 
-def test_block_step_key_block_wholly_before_or_after(orc):
+@pytest.mark.parametrize("b", [1, 2])
+def test_block_step_key_block_wholly_before_or_after(orc, b):
     """Ring steps off the diagonal: a key block wholly before the queries
     (every tile seen in full: the masked launch has nothing left) and one
     wholly after them (the unmasked launch has nothing: the state stays as
     it was, bit for bit)."""
     Lq, Lk, h, n_kv, d = 256, 16512, 4, 2, 64   # 129 key tiles: the two-launch path
-    q, _, _ = make_inputs(1, Lq, h, n_kv, d, seed=31)
-    _, k, v = make_inputs(1, Lk, h, n_kv, d, seed=32)
-    _, k2, v2 = make_inputs(1, Lk, h, n_kv, d, seed=33)
+    q, _, _ = make_inputs(b, Lq, h, n_kv, d, seed=31)
+    _, k, v = make_inputs(b, Lk, h, n_kv, d, seed=32)
+    _, k2, v2 = make_inputs(b, Lk, h, n_kv, d, seed=33)
     q_pos = np.arange(40000, 40000 + Lq, dtype=np.int32)
     before = np.arange(0, 2 * Lk, 2, dtype=np.int32)           # all < 40000
     after = np.arange(50000, 50000 + Lk, dtype=np.int32)       # all > every query
     _block_steps_vs_oracle(orc, q, [(k, v, before)], q_pos)
-    st = ra.new_state(1, Lq, h, d, "cuda")
+    st = ra.new_state(b, Lq, h, d, "cuda")
     qd, kd, vd, k2d, v2d = _dev(q, k, v, k2, v2)
     qp = torch.from_numpy(q_pos).cuda()
     n0 = ra.launch_count()
