@@ -734,7 +734,7 @@ def run_ours(a, rank, world, local_rank):
 
     cpu = None
     if rank == 0 and world == 1 and not a.no_cpu_baseline:
-        fwd_rows, bwd_rows = 48, 12   # ~10-15 s of oracle work on 16 host cores
+        fwd_rows, bwd_rows = 64, 16   # ~10 s of oracle work on 16 host cores
         flops, _, secs, threads, _ = _cpu_oracle_sample(w, fwd_rows, bwd_rows, seed=123)
         st_secs, st_tflops = _cpu_oracle_single_thread_tiny()
         cpu = {"value": flops / secs / 1e12, "unit": "TFLOP/s", "cores": threads,
