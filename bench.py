@@ -57,6 +57,9 @@ def _args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the layout / causal-imbalance measurements")
+    ap.add_argument("--block-steps", action="store_true",
+                    help="only the ring-step (ra_block_step) timings at the workload's shard "
+                         "size, as one JSON line (for profiling the block-step kernels)")
     ap.add_argument("--ring", action="store_true",
                     help="the real ring across the ranks: the workload's sequence split over "
                          "them, key/value blocks exchanged point to point (ring.py)")
@@ -863,6 +866,29 @@ def run_ring(a, rank, world, local_rank):
         print(json.dumps(line), flush=True)
 
 
+def run_block_steps(a):
+    """The ring-step timings of block_step_report alone, on seeded device
+    inputs of one shard's shape (the workload's seed and amplitude)."""
+    import torch
+
+    from long_context_exact_gb300 import binding as ra
+    from long_context_exact_gb300.inputs import WORKLOADS
+
+    ra.load()
+    dev = torch.device("cuda", 0)
+    w = WORKLOADS[a.workload]
+    gen = torch.Generator(device=dev).manual_seed(w.seed)
+
+    def rnd(*shape):
+        x = torch.randn(shape, generator=gen, device=dev, dtype=torch.float32)
+        return x.mul_(w.amplitude).to(torch.bfloat16)
+
+    L = w.S // w.n_shards
+    q, k, v = rnd(w.b, L, w.h, w.d), rnd(w.b, L, w.n_kv, w.d), rnd(w.b, L, w.n_kv, w.d)
+    rep = block_step_report(w, q, k, v, dev)
+    print(json.dumps({"mode": "block_steps", "workload": w.name, "block_steps": rep}), flush=True)
+
+
 def main():
     a = _args()
     rank = int(os.environ.get("RANK", "0"))
@@ -876,7 +902,9 @@ def main():
         torch.cuda.set_device(local_rank)
         torch.distributed.init_process_group("nccl")
     try:
-        if a.ring:
+        if a.block_steps:
+            run_block_steps(a)
+        elif a.ring:
             run_ring(a, rank, world, local_rank)
         else:
             run_ours(a, rank, world, local_rank)

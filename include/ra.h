@@ -120,8 +120,10 @@ typedef struct {
  * shared memory); RA_ERR_UNSUPPORTED above that.  A causal step over at
  * least 16,384 keys is two kernel launches on `stream`: per 128-query tile,
  * the leading key tiles every row sees in full (at least 32 of them, or
- * all) go through a kernel without the mask, the rest through the masked
- * one; both fold into the state, so no workspace is needed. */
+ * all) and the one tile after them go through a kernel with only a
+ * per-element position mask on that one tile, the rest (if any key of it
+ * is visible) through the kernel with the full causal classification;
+ * both fold into the state, so no workspace is needed. */
 ra_status ra_block_step(const uint16_t *q, const uint16_t *k, const uint16_t *v, float *m,
                         float *l, float *o, const int32_t *q_pos, const int32_t *k_pos,
                         int64_t Lq, int64_t Lk, ra_dims dims, int causal, float scale,

@@ -125,6 +125,9 @@ struct Unit {
   // block mode, causal: the CTA's keep bits (kBitWords words) and then its
   // mask bits in shared memory
   const uint32_t *kbits;
+  // block mode, first launch of a two-launch causal step: the tile after the
+  // fully seen ones, masked by position in that launch (-1: none)
+  int kbound;
 };
 
 // Work-unit order: groups of (batch, kv head, query shard); inside a group the
@@ -145,6 +148,7 @@ __device__ __forceinline__ Unit decode_unit(const FwdParams &p, long long u) {
   x.qmin = 0;
   x.qmax = 0;
   x.kbits = nullptr;
+  x.kbound = -1;
   // block mode with a key split: blockIdx.y selects split_tiles key tiles
   x.kc0 = p.split_tiles > 0 ? static_cast<int>(blockIdx.y) * p.split_tiles : 0;
   x.kc1 = p.split_tiles > 0 ? min(p.n_ktiles, x.kc0 + p.split_tiles) : p.n_ktiles;
@@ -265,7 +269,7 @@ __device__ __forceinline__ bool kv_next(const FwdParams &p, const Unit &x, KvIte
       if (it.c >= x.kc1) return false;
       c = it.c++;
       j = 0;
-      partial = c >= n_complete;
+      partial = c >= n_complete || c == x.kbound;
       return true;
     } else {
       // classified once per CTA: bit t for tile kc0 + t
@@ -298,7 +302,7 @@ __device__ __forceinline__ bool kv_next(const FwdParams &p, const Unit &x, KvIte
 // Warp w walks tiles kc0 + w, kc0 + w + nw, ... eight at a time (one 16-byte
 // load per lane and tile when k_pos is 16-byte aligned) and stops at its
 // first tile that fails; the prefix ends at the smallest of those.
-// Block-collective; `scratch` holds 64 ints.
+// Block-collective; `scratch` holds 128 ints.
 template <bool kVec>
 __device__ __forceinline__ int first_failing_tile(const FwdParams &p, int kc0, int kc1, int qmin,
                                                   int warp, int lane, int nw) {
@@ -331,25 +335,83 @@ __device__ __forceinline__ int first_failing_tile(const FwdParams &p, int kc0, i
   return first;
 }
 
+// Whether some key tile of [t0, kc1) has a key that a row of the query tile
+// (latest position qmax) sees; warp-parallel like first_failing_tile, each
+// warp stopping at its first such tile.
+template <bool kVec>
+__device__ __forceinline__ bool any_visible_tile(const FwdParams &p, int t0, int kc1, int qmax,
+                                                 int warp, int lane, int nw) {
+  constexpr int kBatch = 8;
+  bool found = false;
+  for (int c = t0 + warp; c < kc1 && !found; c += kBatch * nw) {
+    int lo[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int t = c + u * nw;
+      lo[u] = INT_MAX;
+      if (t < kc1) {
+        const int32_t *kp = p.k_pos + static_cast<size_t>(t) * kTile;
+        if (kVec && (t + 1) * kTile <= p.Lk) {
+          const int4 v4 = __ldg(reinterpret_cast<const int4 *>(kp) + lane);
+          lo[u] = min(min(v4.x, v4.y), min(v4.z, v4.w));
+        } else {
+#pragma unroll
+          for (int e = 0; e < kTile / 32; ++e)
+            if (t * kTile + e * 32 + lane < p.Lk) lo[u] = min(lo[u], __ldg(kp + e * 32 + lane));
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) found |= __any_sync(kFull, lo[u] <= qmax);
+  }
+  return found;
+}
+
+// The leading fully seen tiles (returned, counted from kc0) and, when
+// `want_tail`, whether a key after the first tile that is not fully seen is
+// visible to some row of the tile (tail_vis; left true otherwise).
 __device__ __noinline__ int full_prefix_tiles(const FwdParams &p, int a, int kc0, int kc1,
-                                              int *scratch) {
+                                              int *scratch, bool want_tail, bool &tail_vis) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
   const int r1 = min((a + 1) * kTile, p.L);
-  int qmin = INT_MAX;
-  for (int r = a * kTile + static_cast<int>(threadIdx.x); r < r1; r += blockDim.x)
-    qmin = min(qmin, __ldg(p.q_pos + r));
+  int qmin = INT_MAX, qmax = INT_MIN;
+  for (int r = a * kTile + static_cast<int>(threadIdx.x); r < r1; r += blockDim.x) {
+    const int v = __ldg(p.q_pos + r);
+    qmin = min(qmin, v);
+    qmax = max(qmax, v);
+  }
   qmin = warp_min(qmin);
-  if (lane == 0) scratch[warp] = qmin;
+  qmax = warp_max(qmax);
+  if (lane == 0) {
+    scratch[warp] = qmin;
+    scratch[32 + warp] = qmax;
+  }
   __syncthreads();
   qmin = INT_MAX;
-  for (int w = 0; w < nw; ++w) qmin = min(qmin, scratch[w]);
-  const int first = (reinterpret_cast<uintptr_t>(p.k_pos) & 15u) == 0
-                        ? first_failing_tile<true>(p, kc0, kc1, qmin, warp, lane, nw)
+  qmax = INT_MIN;
+  for (int w = 0; w < nw; ++w) {
+    qmin = min(qmin, scratch[w]);
+    qmax = max(qmax, scratch[32 + w]);
+  }
+  const bool vec = (reinterpret_cast<uintptr_t>(p.k_pos) & 15u) == 0;
+  const int first = vec ? first_failing_tile<true>(p, kc0, kc1, qmin, warp, lane, nw)
                         : first_failing_tile<false>(p, kc0, kc1, qmin, warp, lane, nw);
-  if (lane == 0) scratch[32 + warp] = first;
+  __syncthreads();  // every warp has read qmin / qmax
+  if (lane == 0) scratch[64 + warp] = first;
   __syncthreads();
   int f = kc1;
-  for (int w = 0; w < nw; ++w) f = min(f, scratch[32 + w]);
+  for (int w = 0; w < nw; ++w) f = min(f, scratch[64 + w]);
+  tail_vis = true;
+  if (want_tail) {
+    const bool any = vec ? any_visible_tile<true>(p, f + 1, kc1, qmax, warp, lane, nw)
+                         : any_visible_tile<false>(p, f + 1, kc1, qmax, warp, lane, nw);
+    __syncthreads();  // every warp has read the firsts
+    if (lane == 0) scratch[96 + warp] = any ? 1 : 0;
+    __syncthreads();
+    int v = 0;
+    for (int w = 0; w < nw; ++w) v |= scratch[96 + w];
+    tail_vis = v != 0;
+  }
   __syncthreads();  // scratch is free again
   return f - kc0;
 }
@@ -430,12 +492,17 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::kThreads, 1)
     }
     if (p.full_prefix != 0) {
       const Unit y = decode_unit(p, blockIdx.x);
-      fp = full_prefix_tiles(p, y.a, y.kc0, y.kc1,
-                             reinterpret_cast<int *>(smem + C::kBitsOff));
+      bool tail_vis = true;
+      fp = full_prefix_tiles(p, y.a, y.kc0, y.kc1, reinterpret_cast<int *>(smem + C::kBitsOff),
+                             p.full_prefix == 2, tail_vis);
       // a CTA with work in both launches pays a second start and state
       // merge, which a short prefix does not earn back: it stays whole
       if (fp < y.kc1 - y.kc0 && fp < kMinPrefixTiles) fp = 0;
-      if (p.full_prefix == 1 ? fp == 0 : y.kc0 + fp >= y.kc1) return;
+      // the first launch also takes the tile after the prefix, masked by
+      // position: on a ring step that is the diagonal tile, and the second
+      // launch is left with nothing
+      if (p.full_prefix == 1 ? fp == 0 : (fp > 0 && (y.kc0 + fp + 1 >= y.kc1 || !tail_vis)))
+        return;
     }
   }
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kBarOff);
@@ -482,8 +549,11 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::kThreads, 1)
     if (p.kt_end != nullptr) x.kc1 = min(x.kc1, __ldg(p.kt_end + x.a));
     if (p.kt_begin != nullptr) x.kc0 = max(x.kc0, __ldg(p.kt_begin + x.a));
     kc_all = x.kc0;
-    if (p.full_prefix == 1) x.kc1 = x.kc0 + fp;
-    if (p.full_prefix == 2) x.kc0 += fp;
+    if (p.full_prefix == 1) {
+      x.kc1 = min(x.kc1, x.kc0 + fp + 1);
+      if (x.kc0 + fp < x.kc1) x.kbound = x.kc0 + fp;
+    }
+    if (p.full_prefix == 2 && fp > 0) x.kc0 += fp + 1;
   }
   unit_qrange<kBlock, kDocs, kBNc>(p, x);
   // Rows that see fewer than kSplitKeys keys take the hi + lo path.  On the
@@ -531,7 +601,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::kThreads, 1)
       for (int o = 16; o > 0; o >>= 1) mine += __shfl_xor_sync(kFull, mine, o);
       if (lane == 0) atomicAdd(cnt, mine);
       __syncthreads();
-      // keys of the tiles a first launch took (all seen by every row)
+      // keys of the fully seen tiles a first launch took (a lower bound)
       split = k1 - k0 < kSplitKeys || *cnt + fp * kTile < kSplitKeys;
       x.kbits = bits;
     } else {
@@ -687,7 +757,7 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::kThreads, 1)
     const int r_abs = x.a * kTile + row;
     const bool row_exists = r_abs < p.L;
     const int r_cl = row_exists ? r_abs : p.L - 1;
-    const int qp = kBlock ? ((!kBNc && p.causal) ? p.q_pos[r_cl] : 0)
+    const int qp = kBlock ? ((!kBNc && p.causal) || (kBNc && x.kbound >= 0) ? p.q_pos[r_cl] : 0)
                                 : token_at(p.layout, p.L, p.N, x.i, r_cl);
     // ring mode: this row sees key positions [q_wlo, q_whi]
     int q_wlo = 0, q_whi = 0;
@@ -739,7 +809,9 @@ __global__ void __launch_bounds__(FwdCfg<D, NQ>::kThreads, 1)
 #pragma unroll
           for (int e = 0; e < kTile; ++e) {
             const int kr = c * kTile + e;
-            const bool vis = kr < p.Lk && (kBNc || !p.causal || __ldg(p.k_pos + kr) <= qp);
+            const bool vis =
+                kr < p.Lk && (kBNc ? (c != x.kbound || __ldg(p.k_pos + kr) <= qp)
+                                   : (!p.causal || __ldg(p.k_pos + kr) <= qp));
             if (!vis) s[e] = -INFINITY;
           }
         }
