@@ -236,13 +236,15 @@ def test_block_step_irregular_positions(orc, sort_keys, k_pos_offset):
     _block_steps_vs_oracle(orc, q, [(k, v, k_pos)], q_pos, k_pos_offset=k_pos_offset)
 
 
-@pytest.mark.parametrize("b", [1, 2])
-def test_block_step_key_block_wholly_before_or_after(orc, b):
+@pytest.mark.parametrize("b,Lk", [(1, 16512), (2, 16512), (1, 16400)])
+def test_block_step_key_block_wholly_before_or_after(orc, b, Lk):
     """Ring steps off the diagonal: a key block wholly before the queries
     (every tile seen in full: the masked launch has nothing left) and one
     wholly after them (the unmasked launch has nothing: the state stays as
-    it was, bit for bit)."""
-    Lq, Lk, h, n_kv, d = 256, 16512, 4, 2, 64   # 129 key tiles: the two-launch path
+    it was, bit for bit).  129 key tiles: the two-launch path; with 16,400
+    keys the last tile is ragged and is the first launch's position-masked
+    tile after the 128 complete ones."""
+    Lq, h, n_kv, d = 256, 4, 2, 64
     q, _, _ = make_inputs(b, Lq, h, n_kv, d, seed=31)
     _, k, v = make_inputs(b, Lk, h, n_kv, d, seed=32)
     _, k2, v2 = make_inputs(b, Lk, h, n_kv, d, seed=33)
