@@ -9,6 +9,8 @@ N(0,1) x 0.5).  Useful FLOPs: 2 b S^2 h d forward (causal), 2.5x that for the
 backward.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+       python bench.py --block-steps     (ring-step timings only)
+       python bench.py --ring            (under torchrun: the ring across the ranks)
 Prints one JSON line (rank 0).  Under torchrun each rank runs its own replica
 (weak scaling, no collective on the data path).
 """
