@@ -160,10 +160,27 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- oracle arm
-def _cpu_oracle_sample(w, fwd_rows: int, bwd_rows: int, seed: int):
+def _workload_config(w, layout: int, have_bwd: bool, world: int) -> dict:
+    """The JSON line's `config` for a workload (both arms print the same)."""
+    return {"workload": w.name, "b": w.b, "S": w.S, "h": w.h, "n_kv": w.n_kv, "d": w.d,
+            "n_shards": w.n_shards,
+            "layout": {0: "contiguous", 1: "striped", 2: "zigzag"}[layout],
+            "causal": w.causal, "backward": have_bwd,
+            "l2": "inputs larger than L2 (Q alone is "
+                  f"{w.b * w.S * w.h * w.d * 2 / 1e9:.2f} GB); no flush",
+            "parallelism": f"replica x{world}"}
+
+
+def _workload_layout(w) -> int:
+    from long_context_exact_gb300.inputs import STRIPED
+    return STRIPED if STRIPED in w.layouts else w.layouts[0]
+
+
+def _cpu_oracle_sample(w, fwd_rows: int, bwd_rows: int, seed: int, inputs=None):
     """Time the fp64 oracle on a bounded sample of the workload: forward on
     `fwd_rows` random query rows (all heads), backward on `bwd_rows`.
-    Returns (useful FLOPs done, seconds, threads)."""
+    `inputs` = (q, k, v, dO) from make_inputs, drawn here when not given.
+    Returns (useful FLOPs done, forward seconds, seconds, threads, torch)."""
     import numpy as np
     import torch
 
@@ -172,7 +189,9 @@ def _cpu_oracle_sample(w, fwd_rows: int, bwd_rows: int, seed: int):
     from oracle import oracle
 
     oracle.build()
-    q, k, v, do = make_inputs(w.b, w.S, w.h, w.n_kv, w.d, w.seed, w.amplitude, with_dout=True)
+    if inputs is None:
+        inputs = make_inputs(w.b, w.S, w.h, w.n_kv, w.d, w.seed, w.amplitude, with_dout=True)
+    q, k, v, do = inputs
     rng = np.random.default_rng(seed)
     rows_f = np.sort(rng.choice(w.S, fwd_rows, replace=False))
     rows_b = np.sort(rng.choice(w.S, bwd_rows, replace=False))
@@ -212,15 +231,19 @@ def _cpu_oracle_single_thread_tiny():
 def run_reference(a, rank, world):
     if rank != 0:
         return
-    from long_context_exact_gb300.inputs import WORKLOADS
+    from long_context_exact_gb300.inputs import WORKLOADS, make_inputs
     w = WORKLOADS[a.workload]
     fwd_rows, bwd_rows = 8, 2
     vals = []
     threads = 1
+    # the workload's inputs once (drawing 256K rows per step would take longer
+    # than the oracle's sample itself)
+    inputs = make_inputs(w.b, w.S, w.h, w.n_kv, w.d, w.seed, w.amplitude, with_dout=True)
     for _ in range(a.warmup):
-        _cpu_oracle_sample(w, fwd_rows, bwd_rows, seed=0)
+        _cpu_oracle_sample(w, fwd_rows, bwd_rows, seed=0, inputs=inputs)
     for s in range(a.steps):
-        flops, _, secs, threads, _ = _cpu_oracle_sample(w, fwd_rows, bwd_rows, seed=s + 1)
+        flops, _, secs, threads, _ = _cpu_oracle_sample(w, fwd_rows, bwd_rows, seed=s + 1,
+                                                        inputs=inputs)
         vals.append((flops, secs))
     tot_f = sum(f for f, _ in vals)
     tot_s = sum(s for _, s in vals)
@@ -232,8 +255,7 @@ def run_reference(a, rank, world):
         "n_gpus": a.gpus, "steps": a.steps, "warmup": a.warmup,
         "ms_per_step": tot_s / a.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "b": w.b, "S": w.S, "h": w.h, "n_kv": w.n_kv, "d": w.d,
-                   "n_shards": w.n_shards, "layout": "striped", "causal": w.causal},
+        "config": _workload_config(w, _workload_layout(w), True, world),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
@@ -759,13 +781,7 @@ def run_ours(a, rank, world, local_rank):
             "steps": a.steps, "warmup": a.warmup, "ms_per_step": elapsed_ms / a.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
-            "config": {"workload": w.name, "b": w.b, "S": w.S, "h": w.h, "n_kv": w.n_kv,
-                       "d": w.d, "n_shards": w.n_shards,
-                       "layout": {0: "contiguous", 1: "striped", 2: "zigzag"}[layout],
-                       "causal": w.causal, "backward": have_bwd,
-                       "l2": "inputs larger than L2 (Q alone is "
-                             f"{q.numel() * 2 / 1e9:.2f} GB); no flush",
-                       "parallelism": f"replica x{world}"},
+            "config": _workload_config(w, layout, have_bwd, world),
             "pct_of_bf16_peak": 100.0 * value / world / peaks["bf16_sustained"],
             "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
             "fwd_tflops": f_fwd / (fwd_ms / 1e3) / 1e12,

@@ -25,6 +25,12 @@ def test_reference_arm_prints_one_contract_line():
     assert d["value"] > 0 and d["unit"] == "TFLOP/s" and d["higher_is_better"] is True
     assert d["n_gpus"] == 1 and d["steps"] == 1 and d["warmup"] == 1
     assert d["config"]["workload"].startswith("tiny")
+    # the same config as the library's own arm prints for this workload
+    sys.path.insert(0, ROOT)
+    import bench
+    from long_context_exact_gb300.inputs import WORKLOADS
+    w = WORKLOADS["tiny"]
+    assert d["config"] == bench._workload_config(w, bench._workload_layout(w), True, 1)
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"]
     assert cb["sample"]
