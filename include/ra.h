@@ -123,7 +123,8 @@ typedef struct {
  * all) and the one tile after them go through a kernel with only a
  * per-element position mask on that one tile, the rest (if any key of it
  * is visible) through the kernel with the full causal classification;
- * both fold into the state, so no workspace is needed. */
+ * both fold into the state, so no workspace is needed.  Should the second
+ * launch fail (RA_ERR_CUDA), the state already holds the first one's part. */
 ra_status ra_block_step(const uint16_t *q, const uint16_t *k, const uint16_t *v, float *m,
                         float *l, float *o, const int32_t *q_pos, const int32_t *k_pos,
                         int64_t Lq, int64_t Lk, ra_dims dims, int causal, float scale,
