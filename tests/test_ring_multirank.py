@@ -109,6 +109,8 @@ CASES = [
     (2, (2, 256, 4, 1, 16, 0, True)),
     (4, (1, 256, 4, 2, 16, 2, True)),
     (4, (1, 128, 2, 2, 8, 1, False)),
+    (3, (1, 192, 6, 2, 8, 1, True)),     # odd ring, g = 3
+    (3, (1, 192, 6, 2, 8, 2, True)),     # zig-zag over three ranks
 ]
 
 
